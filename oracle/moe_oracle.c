@@ -1,0 +1,328 @@
+/*
+ * moe_oracle.c -- plain fp64 CPU oracle for the forward pass of a sparse
+ * Mixture-of-Experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or constant with the CUDA library: it is written from the
+ * pages' definitions alone, as loops over tokens and experts, in double
+ * precision, with no blocking, fusion or reordering.  Inputs are read in the
+ * storage type the caller hands over (fp64, fp32 or bf16 bit patterns); every
+ * arithmetic step is done in double.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [Intro]  "混合专家模型MoE入门实战：从零搭建可运行的小型MoE模型" (0539edu.com/news/5495887)
+ *   [Arch]   "MoE架构解析：混合专家模型原理与工程实践" (jsqmd.com/news/1258680)
+ *   [Sparse] "MoE混合专家模型原理与实战：稀疏激活如何实现万亿参数高效推理" (framerc.cn/news/2939593)
+ *   [Basic]  "混合专家 MOE 是什么" (dgblog.top/posts/ai/moe)
+ *   [Switch] "MoE 混合专家模型串讲：从 Switch Transformer 到 DeepSeekMoE" (uestc.de5.net/blog/mixture-of-experts)
+ *
+ * Readings where the pages are silent (each is also listed in the design notes):
+ *   - top-k ties go to the lower expert index; slots are ordered by score descending;
+ *   - capacity C = floor(T*cf/E) with no factor k; cf <= 0 means "no limit";
+ *   - capacity priority is ascending token order (slot order inside a token cannot
+ *     matter: a token never picks the same expert twice);
+ *   - f_i counts the router's selection before capacity drops, normalised by T*k;
+ *   - residual mode 0 adds x only to tokens whose routed slots were all dropped,
+ *     mode 1 adds x to every token;
+ *   - SwiGLU (absent from the pages) is W2 (silu(W1 x) * (W3 x)), silu(z) = z/(1+e^-z).
+ *
+ * Every function here is pinned by CPU tests against values the pages print,
+ * closed forms, invariants and brute force (tests/test_oracle_pins.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Storage codes of the caller's arrays (decoding only). */
+enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2 };
+
+/* Expert activation codes. */
+enum { ORC_RELU = 0, ORC_GELU_TANH = 1, ORC_GELU_ERF = 2, ORC_SWIGLU = 3 };
+
+/* Read element i of an array stored as fp64, fp32 or bf16, exactly, as a double. */
+static double rd(const void* p, int code, size_t i)
+{
+    if (code == ORC_F64) return ((const double*)p)[i];
+    if (code == ORC_F32) return (double)((const float*)p)[i];
+    uint32_t u = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Expert capacity.  [Arch] §3.1 "容量因子": int(batch_size * capacity_factor /
+ * num_experts); [Intro] §4.2 gives the worked number 1000 tokens, 8 experts,
+ * factor 1.25 -> 156.  Returns -1 for "no capacity limit" (cf <= 0). */
+long long orc_capacity(long long T, long long E, double cf)
+{
+    if (cf <= 0.0) return -1;
+    return (long long)floor((double)T * cf / (double)E);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1 -- router logits.  [Basic] §"公式：三步走" first formula: the router
+ * is W_g x with W_g of shape experts x input dim; [Intro] §3.3 and [Switch]
+ * §"从传统 MoE 到 Switch Routing" use the same linear router (with an optional
+ * bias, as nn.Linear has).  logits[t,e] = sum_i x[t,i] * Wg[e,i] + bg[e]. */
+void orc_router_logits(int T, int d, int E,
+                       const void* x, int x_code,
+                       const void* wg, int wg_code,
+                       const void* bg, int bg_code,
+                       double* logits)
+{
+    #pragma omp parallel for schedule(static)
+    for (long t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int i = 0; i < d; ++i)
+                s += rd(x, x_code, (size_t)t * d + i) * rd(wg, wg_code, (size_t)e * d + i);
+            if (bg) s += rd(bg, bg_code, (size_t)e);
+            logits[(size_t)t * E + e] = s;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2 -- softmax over the E routed experts.  [Basic] §"一个小算例":
+ * softmax(z)_i = e^{z_i} / sum_j e^{z_j}.  The maximum is subtracted first;
+ * that leaves every ratio unchanged. */
+void orc_softmax(int T, int E, const double* logits, double* probs)
+{
+    #pragma omp parallel for schedule(static)
+    for (long t = 0; t < T; ++t) {
+        const double* l = logits + (size_t)t * E;
+        double m = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > m) m = l[e];
+        double den = 0.0;
+        for (int e = 0; e < E; ++e) den += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp(l[e] - m) / den;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 3 -- top-k selection.  [Intro] §3.3 (torch.topk on the softmax
+ * weights), [Arch] §2.1 (top_k on the logits): softmax is monotone, so both
+ * pick the same experts.  Slot j holds the j-th largest score; equal scores
+ * go to the lower expert index. */
+void orc_topk(int T, int E, int k, const double* scores, int32_t* idx)
+{
+    #pragma omp parallel
+    {
+        unsigned char* taken = (unsigned char*)malloc((size_t)E);
+        #pragma omp for schedule(static)
+        for (long t = 0; t < T; ++t) {
+            const double* s = scores + (size_t)t * E;
+            memset(taken, 0, (size_t)E);
+            for (int j = 0; j < k; ++j) {
+                int best = -1;
+                for (int e = 0; e < E; ++e) {
+                    if (taken[e]) continue;
+                    if (best < 0 || s[e] > s[best]) best = e;
+                }
+                taken[best] = 1;
+                idx[(size_t)t * k + j] = best;
+            }
+        }
+        free(taken);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 4 -- gates.  The gate of slot j is the router probability of its
+ * expert.  With renormalize != 0 the k gates are divided by their sum
+ * ([Intro] §3.3, "重新归一化 Top-K 权重"); otherwise they are the raw
+ * probabilities (Switch routing keeps p of the chosen expert, [Switch] §"门控
+ * 网络与稀疏路由"; DeepSeekMoE sets g = s inside the top-K, [Switch]
+ * §"数学定义"). */
+void orc_gates(int T, int E, int k, const double* probs, const int32_t* idx,
+               int renormalize, double* gates)
+{
+    for (long t = 0; t < T; ++t) {
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double g = probs[(size_t)t * E + idx[(size_t)t * k + j]];
+            gates[(size_t)t * k + j] = g;
+            sum += g;
+        }
+        if (renormalize)
+            for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] /= sum;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps 5-6 -- routed counts and capacity in token order.
+ * counts[e] = number of (t, j) with idx[t,j] == e, before any drop ([Intro]
+ * §3.4, the one_hot frequency).  Walking tokens in ascending order, the slot
+ * (t, j) gets position pos = number of earlier tokens routed to the same
+ * expert; it is kept iff C < 0 or pos < C.  A token over capacity skips the
+ * expert ([Switch] §"专家容量": f(x) = 0 for dropped tokens).
+ * perm_row is the slot's row in the expert-contiguous, token-ascending,
+ * unpadded order (offset of the expert's kept rows + pos), -1 if dropped. */
+void orc_dispatch(int T, int E, int k, const int32_t* idx, long long C,
+                  int32_t* counts, int32_t* pos, uint8_t* dropped, int32_t* perm_row)
+{
+    long long* seen = (long long*)calloc((size_t)E, sizeof(long long));
+    long long* start = (long long*)calloc((size_t)E + 1, sizeof(long long));
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (long t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            size_t s = (size_t)t * k + j;
+            int e = idx[s];
+            counts[e] += 1;
+            long long p = seen[e]++;
+            pos[s] = (int32_t)p;
+            dropped[s] = (uint8_t)(C >= 0 && p >= C);
+        }
+    }
+    for (int e = 0; e < E; ++e) {
+        long long kept = counts[e];
+        if (C >= 0 && kept > C) kept = C;
+        start[e + 1] = start[e] + kept;
+    }
+    for (size_t s = 0; s < (size_t)T * k; ++s)
+        perm_row[s] = dropped[s] ? -1 : (int32_t)(start[idx[s]] + pos[s]);
+    free(seen);
+    free(start);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Switch load-balancing statistic N * sum_i f_i * P_i.  [Intro] §3.4 (code and
+ * text: equals about 1 when balanced, larger when not), [Switch]
+ * §"负载均衡损失函数" (f_i hard assignment fraction, P_i mean router
+ * probability; f = P = 1/N gives the minimum).  f_i = counts_i / (T*k). */
+double orc_aux(int T, int E, int k, const int32_t* counts, const double* probs)
+{
+    double aux = 0.0;
+    for (int e = 0; e < E; ++e) {
+        double P = 0.0;
+        for (long t = 0; t < T; ++t) P += probs[(size_t)t * E + e];
+        P /= (double)T;
+        double f = (double)counts[e] / ((double)T * (double)k);
+        aux += f * P;
+    }
+    return (double)E * aux;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Activations.  GELU(tanh) and GELU(erf) after Hendrycks & Gimpel; ReLU;
+ * silu(z) = z / (1 + e^-z). */
+static double act_fn(int act, double z)
+{
+    switch (act) {
+    case ORC_RELU: return z > 0.0 ? z : 0.0;
+    case ORC_GELU_TANH: {
+        const double c = sqrt(2.0 / M_PI);
+        return 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+    }
+    case ORC_GELU_ERF: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+    default: return z / (1.0 + exp(-z)); /* silu */
+    }
+}
+
+double orc_act(int act, double z) { return act_fn(act, z); }
+
+/* Step 7 -- one expert on one token.  Expert e is a two-layer MLP ([Intro]
+ * §3.2: Linear -> GELU -> Linear; [Sparse] §3.1), weights in nn.Linear
+ * layout: W1[e] is [F, d], W2[e] is [d, F].  SwiGLU uses W3[e] ([F, d]) as
+ * the linear branch.  xr is the token's row (d doubles), h scratch of F,
+ * out receives d doubles. */
+static void expert_ffn(int d, int F, int act, int e,
+                       const void* W1, const void* W3, const void* W2, int wc,
+                       const void* b1, const void* b2, int bc,
+                       const double* xr, double* h, double* out)
+{
+    const size_t w1 = (size_t)e * F * d;
+    for (int f = 0; f < F; ++f) {
+        double a = 0.0;
+        for (int i = 0; i < d; ++i) a += rd(W1, wc, w1 + (size_t)f * d + i) * xr[i];
+        if (b1) a += rd(b1, bc, (size_t)e * F + f);
+        if (act == ORC_SWIGLU) {
+            double b = 0.0;
+            for (int i = 0; i < d; ++i) b += rd(W3, wc, w1 + (size_t)f * d + i) * xr[i];
+            h[f] = act_fn(ORC_SWIGLU, a) * b;
+        } else {
+            h[f] = act_fn(act, a);
+        }
+    }
+    const size_t w2 = (size_t)e * d * F;
+    for (int o = 0; o < d; ++o) {
+        double s = 0.0;
+        for (int f = 0; f < F; ++f) s += rd(W2, wc, w2 + (size_t)o * F + f) * h[f];
+        if (b2) s += rd(b2, bc, (size_t)e * d + o);
+        out[o] = s;
+    }
+}
+
+/* Steps 7-9 -- layer output for a list of tokens.
+ *   y[t] = sum over kept slots j of gates[t,j] * FFN_{idx[t,j]}(x[t])    ([Intro] §3.4, [Basic] third formula)
+ *        + sum over shared experts s < S of FFN_{E+s}(x[t])               ([Switch] §"共享专家隔离": always on, gate 1)
+ *        + pass(t) * x[t]                                                 ([Switch] §"专家容量": 0 + x = x)
+ * pass(t) = 1 if residual_mode == 1; with residual_mode == 0 it is 1 only when
+ * k >= 1 and every routed slot of t was dropped.  Expert arrays hold E + S
+ * experts, routed first.  tokens lists n_rows token ids; y is [n_rows, d]. */
+void orc_output_rows(int T, int d, int F, int E, int S, int k, int act, int residual_mode,
+                     const void* x, int x_code,
+                     const void* W1, const void* W3, const void* W2, int w_code,
+                     const void* b1, const void* b2, int b_code,
+                     const int32_t* idx, const double* gates, const uint8_t* dropped,
+                     int n_rows, const int32_t* tokens, double* y)
+{
+    (void)T;
+    (void)E;
+    #pragma omp parallel
+    {
+        double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+        double* h = (double*)malloc(sizeof(double) * (size_t)F);
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        #pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < n_rows; ++r) {
+            const long t = tokens[r];
+            double* yr = y + (size_t)r * d;
+            for (int i = 0; i < d; ++i) {
+                xr[i] = rd(x, x_code, (size_t)t * d + i);
+                yr[i] = 0.0;
+            }
+            int n_dropped = 0;
+            for (int j = 0; j < k; ++j) {
+                size_t s = (size_t)t * k + j;
+                if (dropped[s]) {
+                    ++n_dropped;
+                    continue;
+                }
+                expert_ffn(d, F, act, idx[s], W1, W3, W2, w_code, b1, b2, b_code, xr, h, o);
+                for (int i = 0; i < d; ++i) yr[i] += gates[s] * o[i];
+            }
+            for (int sh = 0; sh < S; ++sh) {
+                expert_ffn(d, F, act, E + sh, W1, W3, W2, w_code, b1, b2, b_code, xr, h, o);
+                for (int i = 0; i < d; ++i) yr[i] += o[i];
+            }
+            int pass = residual_mode == 1 || (k >= 1 && n_dropped == k);
+            if (pass)
+                for (int i = 0; i < d; ++i) yr[i] += xr[i];
+        }
+        free(xr);
+        free(h);
+        free(o);
+    }
+}
+
+/* Number of threads the parallel loops above use (reported with timings). */
+int orc_num_threads(void)
+{
+    int n = 1;
+    #pragma omp parallel
+    {
+        #pragma omp single
+        {
+#ifdef _OPENMP
+            extern int omp_get_num_threads(void);
+            n = omp_get_num_threads();
+#endif
+        }
+    }
+    return n;
+}

@@ -1,0 +1,275 @@
+"""fp64 CPU oracle for the sparse MoE FFN forward pass (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  It shares no code with the CUDA library:
+the arithmetic lives in ``moe_oracle.c`` (plain double-precision loops over
+tokens and experts, written from the pages' definitions); this wrapper only
+marshals arrays and chains the steps in the pages' order:
+
+1. router logits, 2. softmax, 3. top-k, 4. gates, 5. counts, 6. capacity in
+token order, 7-9. expert FFNs, shared experts and the gate-weighted combine,
+plus the Switch load-balancing statistic N * sum_i f_i P_i.
+
+Sources are cited by page title and section in ``moe_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_SO = os.path.join(_HERE, "libmoe_oracle.so")
+
+F64, F32, BF16 = 0, 1, 2
+ACTS = {"relu": 0, "gelu_tanh": 1, "gelu_erf": 2, "swiglu": 3}
+
+_lib_handle = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into libmoe_oracle.so next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
+               "-o", _SO, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+    return _SO
+
+
+def _lib():
+    global _lib_handle
+    if _lib_handle is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        vp, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        L.orc_capacity.restype = ctypes.c_longlong
+        L.orc_capacity.argtypes = [ctypes.c_longlong, ctypes.c_longlong, dbl]
+        L.orc_router_logits.restype = None
+        L.orc_router_logits.argtypes = [i32, i32, i32, vp, i32, vp, i32, vp, i32, vp]
+        L.orc_softmax.restype = None
+        L.orc_softmax.argtypes = [i32, i32, vp, vp]
+        L.orc_topk.restype = None
+        L.orc_topk.argtypes = [i32, i32, i32, vp, vp]
+        L.orc_gates.restype = None
+        L.orc_gates.argtypes = [i32, i32, i32, vp, vp, i32, vp]
+        L.orc_dispatch.restype = None
+        L.orc_dispatch.argtypes = [i32, i32, i32, vp, ctypes.c_longlong, vp, vp, vp, vp]
+        L.orc_aux.restype = dbl
+        L.orc_aux.argtypes = [i32, i32, i32, vp, vp]
+        L.orc_act.restype = dbl
+        L.orc_act.argtypes = [i32, dbl]
+        L.orc_output_rows.restype = None
+        L.orc_output_rows.argtypes = [i32] * 8 + [vp, i32, vp, vp, vp, i32, vp, vp, i32,
+                                                  vp, vp, vp, i32, vp, vp]
+        L.orc_num_threads.restype = i32
+        L.orc_num_threads.argtypes = []
+        _lib_handle = L
+    return _lib_handle
+
+
+# --------------------------------------------------------------------------
+# array marshalling (no arithmetic)
+
+def _as_array(a):
+    """Return (contiguous numpy array kept alive, storage code).
+
+    Accepts numpy arrays (float64/float32) and CPU torch tensors
+    (float64/float32/bfloat16).  bf16 tensors are passed as their raw 16-bit
+    patterns; the C side widens them exactly.
+    """
+    if a is None:
+        return None, F64
+    if isinstance(a, np.ndarray):
+        if a.dtype == np.float64:
+            return np.ascontiguousarray(a), F64
+        if a.dtype == np.float32:
+            return np.ascontiguousarray(a), F32
+        raise TypeError(f"unsupported numpy dtype {a.dtype}")
+    import torch  # only for tensors handed in by the caller
+    if not isinstance(a, torch.Tensor):
+        return _as_array(np.asarray(a, dtype=np.float64))
+    t = a.detach().to("cpu").contiguous()
+    if t.dtype == torch.float64:
+        return t.numpy(), F64
+    if t.dtype == torch.float32:
+        return t.numpy(), F32
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy(), BF16
+    raise TypeError(f"unsupported tensor dtype {t.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+# --------------------------------------------------------------------------
+# single steps
+
+def capacity(T: int, E: int, cf) -> int:
+    """floor(T*cf/E); -1 when cf is None or <= 0 (no limit)."""
+    return int(_lib().orc_capacity(T, E, -1.0 if cf is None else float(cf)))
+
+
+def router_logits(x, Wg, bg=None) -> np.ndarray:
+    xa, xc = _as_array(x)
+    wa, wc = _as_array(Wg)
+    ba, bc = _as_array(bg)
+    T, d = xa.shape
+    E = wa.shape[0]
+    out = np.empty((T, E), dtype=np.float64)
+    _lib().orc_router_logits(T, d, E, _ptr(xa), xc, _ptr(wa), wc, _ptr(ba), bc, _ptr(out))
+    return out
+
+
+def softmax(logits) -> np.ndarray:
+    la = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
+    T, E = la.shape
+    out = np.empty_like(la)
+    _lib().orc_softmax(T, E, _ptr(la), _ptr(out))
+    return out
+
+
+def topk(scores, k: int) -> np.ndarray:
+    """Indices of the k largest scores per row, descending; ties -> lower index.
+
+    ``scores`` may be fp32 (e.g. device logits): the comparison is exact after
+    widening to double, so the selection is the one fp32 comparisons make.
+    """
+    sa = np.ascontiguousarray(np.asarray(scores, dtype=np.float64))
+    T, E = sa.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    idx = np.empty((T, k), dtype=np.int32)
+    _lib().orc_topk(T, E, k, _ptr(sa), _ptr(idx))
+    return idx
+
+
+def gates(probs, idx, renormalize: bool) -> np.ndarray:
+    pa = np.ascontiguousarray(np.asarray(probs, dtype=np.float64))
+    ia = _i32(idx)
+    T, E = pa.shape
+    k = ia.shape[1]
+    out = np.empty((T, k), dtype=np.float64)
+    _lib().orc_gates(T, E, k, _ptr(pa), _ptr(ia), int(bool(renormalize)), _ptr(out))
+    return out
+
+
+@dataclass
+class Dispatch:
+    counts: np.ndarray    # [E] int32, router selection before drops
+    pos: np.ndarray       # [T,k] int32, token-order position inside the expert
+    dropped: np.ndarray   # [T,k] uint8
+    perm_row: np.ndarray  # [T,k] int32, unpadded expert-contiguous row or -1
+
+
+def dispatch(idx, E: int, C: int) -> Dispatch:
+    ia = _i32(idx)
+    T, k = ia.shape
+    counts = np.empty(E, dtype=np.int32)
+    pos = np.empty((T, k), dtype=np.int32)
+    dropped = np.empty((T, k), dtype=np.uint8)
+    perm_row = np.empty((T, k), dtype=np.int32)
+    _lib().orc_dispatch(T, E, k, _ptr(ia), int(C), _ptr(counts), _ptr(pos), _ptr(dropped),
+                        _ptr(perm_row))
+    return Dispatch(counts, pos, dropped, perm_row)
+
+
+def aux(counts, probs, k: int) -> float:
+    ca = _i32(counts)
+    pa = np.ascontiguousarray(np.asarray(probs, dtype=np.float64))
+    T, E = pa.shape
+    return float(_lib().orc_aux(T, E, k, _ptr(ca), _ptr(pa)))
+
+
+def act(name: str, z: float) -> float:
+    return float(_lib().orc_act(ACTS[name], float(z)))
+
+
+def output_rows(x, W1, W3, W2, b1, b2, idx, gate_vals, dropped, *, E: int, S: int,
+                act_name: str, residual_mode: int, tokens=None) -> np.ndarray:
+    """Layer output (fp64) for the listed tokens (all tokens if None)."""
+    xa, xc = _as_array(x)
+    w1, wc = _as_array(W1)
+    w3, wc3 = _as_array(W3)
+    w2, wc2 = _as_array(W2)
+    if W3 is not None and wc3 != wc or wc2 != wc:
+        raise TypeError("W1, W3 and W2 must share a storage type")
+    ba1, bc = _as_array(b1)
+    ba2, bc2 = _as_array(b2)
+    if b1 is not None and b2 is not None and bc != bc2:
+        raise TypeError("b1 and b2 must share a storage type")
+    if b1 is None:
+        bc = bc2
+    T, d = xa.shape
+    F = w1.shape[1]
+    ia = _i32(idx)
+    k = ia.shape[1]
+    ga = np.ascontiguousarray(np.asarray(gate_vals, dtype=np.float64))
+    da = np.ascontiguousarray(np.asarray(dropped, dtype=np.uint8))
+    tok = _i32(np.arange(T) if tokens is None else tokens)
+    y = np.empty((tok.shape[0], d), dtype=np.float64)
+    _lib().orc_output_rows(T, d, F, E, S, k, ACTS[act_name], int(residual_mode),
+                           _ptr(xa), xc, _ptr(w1), _ptr(w3), _ptr(w2), wc,
+                           _ptr(ba1), _ptr(ba2), bc,
+                           _ptr(ia), _ptr(ga), _ptr(da), tok.shape[0], _ptr(tok), _ptr(y))
+    return y
+
+
+def num_threads() -> int:
+    return int(_lib().orc_num_threads())
+
+
+# --------------------------------------------------------------------------
+# chained steps
+
+@dataclass
+class Routing:
+    logits: np.ndarray
+    probs: np.ndarray
+    idx: np.ndarray
+    gates: np.ndarray
+    counts: np.ndarray
+    pos: np.ndarray
+    dropped: np.ndarray
+    perm_row: np.ndarray
+    aux: float
+    C: int
+
+
+def route_from_logits(logits, *, k: int, renormalize: bool, cf) -> Routing:
+    """Steps 2-6 and the aux statistic on a given [T,E] logits array.
+
+    Fed with the device's fp32 logits this is the bit-exact re-run of the
+    selection, counts, capacity drops and permutation order.
+    """
+    la = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
+    T, E = la.shape
+    probs = softmax(la)
+    idx = topk(la, k)
+    g = gates(probs, idx, renormalize)
+    C = capacity(T, E, cf)
+    dsp = dispatch(idx, E, C)
+    a = aux(dsp.counts, probs, k)
+    return Routing(la, probs, idx, g, dsp.counts, dsp.pos, dsp.dropped, dsp.perm_row, a, C)
+
+
+def route(x, Wg, bg=None, *, k: int, renormalize: bool, cf) -> Routing:
+    """Steps 1-6 and the aux statistic in fp64."""
+    return route_from_logits(router_logits(x, Wg, bg), k=k, renormalize=renormalize, cf=cf)
+
+
+def forward(x, Wg, bg, W1, W3, W2, b1, b2, *, E: int, S: int, k: int, act_name: str,
+            renormalize: bool, cf, residual_mode: int = 0, tokens=None):
+    """Whole layer in fp64: returns (y rows for ``tokens``, Routing)."""
+    r = route(x, Wg, bg, k=k, renormalize=renormalize, cf=cf)
+    y = output_rows(x, W1, W3, W2, b1, b2, r.idx, r.gates, r.dropped, E=E, S=S,
+                    act_name=act_name, residual_mode=residual_mode, tokens=tokens)
+    return y, r
