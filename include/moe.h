@@ -1,0 +1,178 @@
+/*
+ * moe.h -- C ABI of the B300 sparse Mixture-of-Experts FFN forward library
+ * (libmoe_b300.so, sm_103a).
+ *
+ * The library computes, on one GPU, the forward pass of a sparse MoE FFN layer:
+ * a softmax router over E experts, top-k selection with optional capacity and
+ * residual pass-through, dispatch of tokens into expert-contiguous buffers, the
+ * per-expert FFNs (plus always-on shared experts), the gate-weighted combine,
+ * and the Switch load-balancing statistic N * sum_i f_i * P_i.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [Intro]  "混合专家模型MoE入门实战：从零搭建可运行的小型MoE模型" (0539edu.com/news/5495887)
+ *   [Arch]   "MoE架构解析：混合专家模型原理与工程实践" (jsqmd.com/news/1258680)
+ *   [Sparse] "MoE混合专家模型原理与实战：稀疏激活如何实现万亿参数高效推理" (framerc.cn/news/2939593)
+ *   [Basic]  "混合专家 MOE 是什么" (dgblog.top/posts/ai/moe)
+ *   [Switch] "MoE 混合专家模型串讲：从 Switch Transformer 到 DeepSeekMoE" (uestc.de5.net/blog/mixture-of-experts)
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are row-major and owned by the caller.  Pointers in
+ *     moe_inputs_t / moe_outputs_t and the workspace are DEVICE pointers of the
+ *     current CUDA device; every one must be 16-byte aligned.
+ *   - Weights use the nn.Linear [out, in] layout: W1/W3 are [E+S, d_ff, d_model],
+ *     W2 is [E+S, d_model, d_ff]; the E routed experts come first, the S shared
+ *     experts last.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every entry
+ *     point only enqueues work on it: no allocation, no host synchronisation
+ *     (moe_last_device_status excepted), no global state.  A workspace may be
+ *     used by one stream at a time.
+ *   - Validation happens before any launch.  On a non-OK status nothing was
+ *     enqueued.  Asynchronous device faults surface at the caller's next
+ *     synchronisation as usual.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad sizes, null or unaligned pointers, k > E ... */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid combination this build does not implement */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = 5 /* a bounded device wait expired (moe_last_device_status) */
+} moe_status_t;
+
+typedef enum {
+    MOE_ACT_RELU = 0,      /* max(z, 0) */
+    MOE_ACT_GELU_TANH = 1, /* 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) */
+    MOE_ACT_GELU_ERF = 2,  /* 0.5 z (1 + erf(z / sqrt 2)) */
+    MOE_ACT_SWIGLU = 3     /* W2 (silu(W1 x) * (W3 x)); no biases */
+} moe_act_t;
+
+typedef enum {
+    MOE_F32 = 0, /* x, expert weights, biases and y in fp32 (CUDA-core FFMA experts) */
+    MOE_BF16 = 1 /* x, expert weights, biases and y in bf16 (tensor-core experts) */
+} moe_dtype_t;
+
+/* moe_params_t.flags */
+#define MOE_FLAG_FFMA_EXPERTS 1u /* run bf16 experts on the CUDA-core FFMA grouped GEMM
+                                    (cross-check kernel) instead of the tcgen05 one */
+
+/* Limits of this build. */
+#define MOE_MAX_EXPERTS 512 /* E (routed) */
+#define MOE_MAX_TOPK 32     /* k */
+
+typedef struct {
+    int32_t T;          /* tokens (rows of x) >= 1 */
+    int32_t d_model;    /* d, multiple of 8 */
+    int32_t d_ff;       /* F, hidden width of one expert, multiple of 8 */
+    int32_t E;          /* routed experts, 1..MOE_MAX_EXPERTS */
+    int32_t k;          /* experts per token, 1..min(E, MOE_MAX_TOPK) */
+    int32_t n_shared;   /* S always-on shared experts (gate 1); SwiGLU only */
+    float capacity_factor; /* <= 0: no limit; else C = floor(T * cf / E) rows per expert */
+    int32_t renormalize;   /* 1: gates = p / sum of the k selected p; 0: gates = p */
+    int32_t residual_mode; /* 0: y = x added only to tokens whose routed slots were all
+                              dropped; 1: y += x for every token */
+    int32_t act;        /* moe_act_t */
+    int32_t dtype;      /* moe_dtype_t */
+    uint32_t flags;     /* MOE_FLAG_* */
+} moe_params_t;
+
+typedef struct {
+    const void* x;       /* [T, d] dtype */
+    const float* W_gate; /* [E, d] fp32 router weights */
+    const float* b_gate; /* [E] fp32 router bias, or NULL */
+    const void* W1;      /* [E+S, F, d] dtype */
+    const void* W3;      /* [E+S, F, d] dtype; required iff act == SWIGLU, else NULL */
+    const void* W2;      /* [E+S, d, F] dtype */
+    const void* b1;      /* [E+S, F] dtype or NULL (must be NULL for SwiGLU) */
+    const void* b2;      /* [E+S, d] dtype or NULL (must be NULL for SwiGLU) */
+} moe_inputs_t;
+
+typedef struct {
+    void* y;             /* [T, d] dtype: the layer output */
+    int32_t* expert_idx; /* [T, k] selected experts, by router logit descending, ties to
+                            the lower index */
+    float* gates;        /* [T, k] fp32 gate of each slot (before drops) */
+    int32_t* counts;     /* [E] tokens routed to each expert before capacity drops */
+    uint8_t* dropped;    /* [T, k] 1 = slot dropped by the capacity limit */
+    float* aux;          /* [1] E * sum_e (counts_e / (T k)) * (mean_t p[t,e]) */
+    float* logits;       /* [T, E] fp32 router logits, or NULL (not written) */
+    float* probs;        /* [T, E] fp32 router probabilities, or NULL */
+    int32_t* perm_row;   /* [T, k] row of the slot in the expert-contiguous, token-ascending,
+                            unpadded order of kept slots; -1 if dropped; or NULL */
+} moe_outputs_t;
+
+/* Bytes of device workspace moe_forward needs for these params.  Depends only
+ * on the params.  The workspace must be 256-byte aligned and must be zeroed
+ * once before its first use (the library keeps it consistent afterwards). */
+moe_status_t moe_workspace_size(const moe_params_t* params, size_t* bytes);
+
+/* The whole layer: moe_router, moe_dispatch, moe_grouped_gemm, moe_combine in
+ * that order on `stream`.  Writes every output of moe_outputs_t. */
+moe_status_t moe_forward(const moe_params_t* params, const moe_inputs_t* inputs,
+                         moe_outputs_t* outputs, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Stage 1, router.  logits[t,e] = sum_i x[t,i] W_gate[e,i] + b_gate[e] in fp32
+ * ([Basic] §"公式：三步走"; the router runs in fp32 as [Switch] §"选择性精度"
+ * prescribes), p = softmax over the E routed experts ([Basic] §"一个小算例"),
+ * the k largest logits per token (warp-shuffle top-k; [Intro] §3.3, [Arch]
+ * §2.1), gates = p or p renormalised over the k ([Intro] §3.3), and per-block
+ * column sums of p for the balance statistic.  Writes expert_idx, gates and the
+ * optional logits/probs; the rest lives in the workspace. */
+moe_status_t moe_router(const moe_params_t* params, const moe_inputs_t* inputs,
+                        moe_outputs_t* outputs, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Stage 2, dispatch.  Per-expert histogram in shared memory and a device-wide
+ * scan over token chunks give counts and token-order positions; capacity
+ * C = floor(T cf / E) ([Arch] §3.1 expert_capacity, [Switch] §"专家容量")
+ * drops the slots at position >= C; every kept token row is copied (16-byte
+ * vectors) into an expert-contiguous buffer whose expert segments are padded
+ * to 128 rows ([Intro] §2.4 scatter-gather).  Also computes the balance
+ * statistic ([Intro] §3.4, [Switch] §"负载均衡损失函数").  Writes counts,
+ * dropped, aux and perm_row.  Requires moe_router on the same workspace. */
+moe_status_t moe_dispatch(const moe_params_t* params, const moe_inputs_t* inputs,
+                          moe_outputs_t* outputs, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Stage 3, experts.  For every expert segment, H = act(Xp W1^T + b1) or SwiGLU
+ * silu(Xp W1^T) * (Xp W3^T), then Yp = H W2^T + b2 ([Intro] §3.2, [Sparse]
+ * §3.1); shared experts run on all T tokens as one SwiGLU of hidden S*d_ff
+ * ([Switch] §"共享专家隔离").  bf16: tcgen05/TMEM grouped GEMM fed by TMA;
+ * fp32: CUDA-core FFMA grouped GEMM.  Results stay in the workspace.
+ * Requires moe_dispatch on the same workspace. */
+moe_status_t moe_grouped_gemm(const moe_params_t* params, const moe_inputs_t* inputs,
+                              moe_outputs_t* outputs, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Stage 4, combine.  y[t] = sum over kept slots of gate * expert output (fp32
+ * accumulation, slot order) + shared output + x[t] when residual_mode says so
+ * ([Intro] §3.4, [Basic] third formula, [Switch] §"专家容量": a dropped token
+ * gets 0 + x = x).  Writes y.  Requires moe_grouped_gemm on the same workspace. */
+moe_status_t moe_combine(const moe_params_t* params, const moe_inputs_t* inputs,
+                         moe_outputs_t* outputs, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Synchronises `stream`, reads and clears the workspace's device error word.
+ * Returns MOE_ERR_DEVICE_TIMEOUT if a bounded device wait expired since the last
+ * call, MOE_ERR_CUDA if the synchronisation failed, else MOE_OK.  For tests and
+ * debugging; not needed on the hot path. */
+moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

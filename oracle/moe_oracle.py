@@ -15,6 +15,7 @@ Sources are cited by page title and section in ``moe_oracle.c``.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 from dataclasses import dataclass
@@ -31,12 +32,22 @@ ACTS = {"relu": 0, "gelu_tanh": 1, "gelu_erf": 2, "swiglu": 3}
 _lib_handle = None
 
 
+def _src_hash() -> str:
+    with open(_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile moe_oracle.c into libmoe_oracle.so next to it (gcc, OpenMP)."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+    stamp = _SO + ".srchash"
+    fresh = (os.path.exists(_SO) and os.path.exists(stamp)
+             and open(stamp).read().strip() == _src_hash())
+    if force or not fresh:
         cmd = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
                "-o", _SO, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
+        with open(stamp, "w") as f:
+            f.write(_src_hash())
     return _SO
 
 

@@ -1,0 +1,491 @@
+// api.cu -- the C ABI (include/moe.h): validation, workspace layout, TMA tensor
+// maps and the launch sequence of the four stages on the caller's stream.
+//
+// Nothing here allocates device memory or synchronises the host (except
+// moe_last_device_status).  Every check happens before the first launch of a
+// call, so a non-OK status means nothing was enqueued.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "moe.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kRegionAlign = 1024;
+
+struct Layout {
+    int T, d, F, E, S, k;
+    int C;             // capacity, -1 = none
+    int n_rblk;        // router blocks
+    int nchunks;       // dispatch-scan blocks
+    int rows_cap;      // rows of the permuted buffers (multiple of 128)
+    int t_pad;         // T rounded up to 128 (shared-expert buffers)
+    size_t esz;        // element size of the activation dtype
+    size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
+        off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys, total;
+};
+
+long long capacity_of(const moe_params_t& p)
+{
+    if (!(p.capacity_factor > 0.0f)) return -1;
+    // "MoE架构解析" §3.1: int(batch_size * capacity_factor / num_experts)
+    const double c = std::floor((double)p.T * (double)p.capacity_factor / (double)p.E);
+    return (long long)std::min(c, (double)p.T);  // C >= T never drops anything
+}
+
+moe_status_t validate_params(const moe_params_t* p)
+{
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+    if (p->T < 1 || p->d_model < 8 || p->d_ff < 8) return MOE_ERR_INVALID_ARG;
+    if (p->d_model % 8 != 0 || p->d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (p->E < 1 || p->E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+    if (p->k < 1 || p->k > p->E || p->k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (p->n_shared < 0) return MOE_ERR_INVALID_ARG;
+    if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
+    if (p->residual_mode != 0 && p->residual_mode != 1) return MOE_ERR_INVALID_ARG;
+    if (p->act < MOE_ACT_RELU || p->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+    if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if ((p->flags & ~MOE_FLAG_FFMA_EXPERTS) != 0u) return MOE_ERR_INVALID_ARG;
+    if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    // every index and row count below must fit in int32
+    const long long slots = (long long)p->T * p->k;
+    const long long rows = slots + (long long)p->E * kSegRows + kSegRows;
+    const long long t_pad = ((long long)p->T + kSegRows - 1) / kSegRows * kSegRows;
+    if (rows >= (1ll << 31) || (long long)(p->E + p->n_shared) * p->d_ff >= (1ll << 31) ||
+        (long long)(p->E + p->n_shared) * p->d_model >= (1ll << 31) ||
+        (long long)p->n_shared * p->d_ff >= (1ll << 31) || t_pad >= (1ll << 31))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+Layout make_layout(const moe_params_t& p)
+{
+    Layout L{};
+    L.T = p.T;
+    L.d = p.d_model;
+    L.F = p.d_ff;
+    L.E = p.E;
+    L.S = p.n_shared;
+    L.k = p.k;
+    L.C = (int)capacity_of(p);
+    L.n_rblk = router_blocks(p.T);
+    const long long slots = (long long)p.T * p.k;
+    L.nchunks = (int)((slots + kScanChunk - 1) / kScanChunk);
+    long long cap = slots + (long long)p.E * (kSegRows - 1);
+    if (L.C >= 0) cap = std::min(cap, (long long)p.E * (((long long)L.C + kSegRows - 1) / kSegRows * kSegRows));
+    L.rows_cap = (int)((cap + kSegRows - 1) / kSegRows * kSegRows);
+    L.t_pad = (p.T + kSegRows - 1) / kSegRows * kSegRows;
+    L.esz = (p.dtype == MOE_BF16) ? 2 : 4;
+
+    size_t o = kRegionAlign;  // header: [0] device error word, [1] scan arrival counter
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, kRegionAlign);
+        return at;
+    };
+    L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
+    L.off_hist = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
+    L.off_base = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
+    L.off_rank = take(sizeof(int32_t) * (size_t)slots);
+    L.off_slot_row = take(sizeof(int32_t) * (size_t)slots);
+    L.off_kept = take(sizeof(int32_t) * L.E);
+    L.off_row_off = take(sizeof(int32_t) * L.E);
+    L.off_kept_off = take(sizeof(int32_t) * L.E);
+    L.off_mtile = take(sizeof(int32_t) * (L.E + 1));
+    L.off_xp = take(L.esz * (size_t)L.rows_cap * L.d);
+    L.off_h = take(L.esz * (size_t)L.rows_cap * L.F);
+    L.off_yp = take(L.esz * (size_t)L.rows_cap * L.d);
+    L.off_hs = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.S * L.F : 0);
+    L.off_ys = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.d : 0);
+    L.total = o;
+    return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const moe_outputs_t* out)
+{
+    if (in == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+    const bool swiglu = p.act == MOE_ACT_SWIGLU;
+    if (!in->x || !in->W_gate || !in->W1 || !in->W2) return MOE_ERR_INVALID_ARG;
+    if (swiglu != (in->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (swiglu && (in->b1 || in->b2)) return MOE_ERR_INVALID_ARG;
+    if (!out->y || !out->expert_idx || !out->gates || !out->counts || !out->dropped || !out->aux)
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
+                          out->y, out->expert_idx, out->gates, out->counts, out->dropped, out->aux,
+                          out->logits, out->probs, out->perm_row};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+struct DeviceCache {
+    std::once_flag once;
+    int sms = 0;
+};
+DeviceCache g_dev[64];
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    DeviceCache& c = g_dev[dev];
+    std::call_once(c.once, [&] {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) c.sms = n;
+    });
+    return c.sms;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box {64, box_rows},
+// 128-byte swizzle, zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Ctx {
+    moe_params_t p;
+    const moe_inputs_t* in;
+    moe_outputs_t* out;
+    char* ws;
+    Layout L;
+    cudaStream_t st;
+    int sms;
+    bool bf16, use_tc;
+    int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
+    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2;
+    template <typename T>
+    T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+    uint32_t* err() const { return reinterpret_cast<uint32_t*>(ws); }
+    unsigned* scan_done() const { return reinterpret_cast<unsigned*>(ws) + 1; }
+};
+
+int pick_bn(int N) { return N >= 256 ? 256 : 128; }
+
+moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_outputs_t* out, void* ws,
+                     size_t ws_bytes, void* stream, Ctx& c)
+{
+    moe_status_t s = validate_params(params);
+    if (s != MOE_OK) return s;
+    c.p = *params;
+    s = validate_io(c.p, in, out);
+    if (s != MOE_OK) return s;
+    c.in = in;
+    c.out = out;
+    c.L = make_layout(c.p);
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < c.L.total) return MOE_ERR_WORKSPACE;
+    c.ws = static_cast<char*>(ws);
+    c.st = static_cast<cudaStream_t>(stream);
+    c.sms = sm_count();
+    if (c.sms <= 0) return MOE_ERR_CUDA;
+    c.bf16 = c.p.dtype == MOE_BF16;
+    c.use_tc = c.bf16 && !(c.p.flags & MOE_FLAG_FFMA_EXPERTS);
+    if (c.use_tc) {
+        const Layout& L = c.L;
+        const bool gated = c.p.act == MOE_ACT_SWIGLU;
+        c.bn1 = gated ? 256 : pick_bn(L.F);
+        c.bn2 = pick_bn(L.d);
+        const int b1_rows = gated ? c.bn1 / 2 : c.bn1;
+        const uint64_t ES = (uint64_t)(L.E + L.S);
+        bool ok = encode_bf16_2d(&c.mB1, in->W1, ES * L.F, L.d, b1_rows) &&
+                  encode_bf16_2d(&c.mB2, in->W2, ES * L.d, L.F, c.bn2);
+        ok = ok && encode_bf16_2d(&c.mB3, gated ? in->W3 : in->W1, ES * L.F, L.d, b1_rows);
+        if (L.rows_cap > 0)
+            ok = ok && encode_bf16_2d(&c.mA1, c.at<void>(L.off_xp), L.rows_cap, L.d, 128) &&
+                 encode_bf16_2d(&c.mA2, c.at<void>(L.off_h), L.rows_cap, L.F, 128);
+        if (L.S > 0)
+            ok = ok && encode_bf16_2d(&c.mAs1, in->x, L.T, L.d, 128) &&
+                 encode_bf16_2d(&c.mAs2, c.at<void>(L.off_hs), L.t_pad, (uint64_t)L.S * L.F, 128);
+        if (!ok) return MOE_ERR_UNSUPPORTED;
+    }
+    return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t stage_router(Ctx& c)
+{
+    RouterArgs a{};
+    a.x = c.in->x;
+    a.Wg = c.in->W_gate;
+    a.bg = c.in->b_gate;
+    a.T = c.L.T;
+    a.d = c.L.d;
+    a.E = c.L.E;
+    a.k = c.L.k;
+    a.renormalize = c.p.renormalize;
+    a.idx = c.out->expert_idx;
+    a.gates = c.out->gates;
+    a.logits = c.out->logits;
+    a.probs = c.out->probs;
+    a.psum_part = c.at<float>(c.L.off_psum);
+    a.scan_done = c.scan_done();
+    return cuda_status(launch_router(a, c.bf16, c.st));
+}
+
+moe_status_t stage_dispatch(Ctx& c)
+{
+    DispatchArgs a{};
+    a.idx = c.out->expert_idx;
+    a.gates = c.out->gates;
+    a.T = c.L.T;
+    a.k = c.L.k;
+    a.E = c.L.E;
+    a.C = c.L.C;
+    a.nchunks = c.L.nchunks;
+    a.n_router_blocks = c.L.n_rblk;
+    a.psum_part = c.at<float>(c.L.off_psum);
+    a.local_rank = c.at<int32_t>(c.L.off_rank);
+    a.chunk_hist = c.at<int32_t>(c.L.off_hist);
+    a.chunk_base = c.at<int32_t>(c.L.off_base);
+    a.scan_done = c.scan_done();
+    a.counts = c.out->counts;
+    a.kept = c.at<int32_t>(c.L.off_kept);
+    a.row_off = c.at<int32_t>(c.L.off_row_off);
+    a.kept_off = c.at<int32_t>(c.L.off_kept_off);
+    a.mtile_off = c.at<int32_t>(c.L.off_mtile);
+    a.aux = c.out->aux;
+    a.x = c.in->x;
+    a.xp = c.at<void>(c.L.off_xp);
+    a.row_bytes = (int)(c.L.d * c.L.esz);
+    a.dropped = c.out->dropped;
+    a.perm_row = c.out->perm_row;
+    a.slot_row = c.at<int32_t>(c.L.off_slot_row);
+    return cuda_status(launch_dispatch(a, c.sms, c.st));
+}
+
+moe_status_t stage_gemm(Ctx& c)
+{
+    const Layout& L = c.L;
+    const bool gated = c.p.act == MOE_ACT_SWIGLU;
+    const int act1 = c.p.act;  // moe_act_t values equal the kernels' ActKind values
+    GroupedGemmArgs g1{};
+    g1.mtile_off = c.at<int>(L.off_mtile);
+    g1.row_off = c.at<int>(L.off_row_off);
+    g1.rows = c.at<int>(L.off_kept);
+    g1.G = L.E;
+    g1.N = L.F;
+    g1.K = L.d;
+    g1.k_segments = 1;
+    g1.b_rows_per_group = L.F;
+    g1.b_group0 = 0;
+    g1.out = c.at<void>(L.off_h);
+    g1.ldo = L.F;
+    g1.bias = c.in->b1;
+    g1.a_rows_alloc = L.rows_cap;
+    g1.err = c.err();
+
+    GroupedGemmArgs g2 = g1;
+    g2.N = L.d;
+    g2.K = L.F;
+    g2.b_rows_per_group = L.d;
+    g2.out = c.at<void>(L.off_yp);
+    g2.ldo = L.d;
+    g2.bias = c.in->b2;
+
+    // shared experts: one group of all T tokens, hidden S*F (concatenated experts)
+    GroupedGemmArgs s1 = g1;
+    s1.mtile_off = nullptr;
+    s1.row_off = nullptr;
+    s1.rows = nullptr;
+    s1.G = 1;
+    s1.fixed_rows = L.T;
+    s1.N = L.S * L.F;
+    s1.b_group0 = L.E;
+    s1.out = c.at<void>(L.off_hs);
+    s1.ldo = L.S * L.F;
+    s1.a_rows_alloc = L.T;
+    GroupedGemmArgs s2 = g2;
+    s2.mtile_off = nullptr;
+    s2.row_off = nullptr;
+    s2.rows = nullptr;
+    s2.G = 1;
+    s2.fixed_rows = L.T;
+    s2.k_segments = L.S;
+    s2.b_group0 = L.E;
+    s2.out = c.at<void>(L.off_ys);
+    s2.a_rows_alloc = L.T;
+
+    const int mt_routed = L.rows_cap / kSegRows;
+    const int mt_shared = L.t_pad / kSegRows;
+    auto grid_for = [&](int tiles, int per_sm) { return std::max(1, std::min(tiles, c.sms * per_sm)); };
+    cudaError_t e = cudaSuccess;
+    if (c.use_tc) {
+        const int out1 = gated ? c.bn1 / 2 : c.bn1;
+        g1.n_tiles = ceil_div(L.F, out1);
+        g2.n_tiles = ceil_div(L.d, c.bn2);
+        if (mt_routed > 0) {
+            e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st);
+            if (e == cudaSuccess)
+                e = launch_gemm_tc(c.mA2, c.mB2, c.mB2, g2, kActNone, c.bn2, grid_for(mt_routed * g2.n_tiles, 1),
+                                   c.st);
+        }
+        if (e == cudaSuccess && L.S > 0) {
+            s1.n_tiles = ceil_div(s1.N, out1);
+            s2.n_tiles = ceil_div(L.d, c.bn2);
+            e = launch_gemm_tc(c.mAs1, c.mB1, c.mB3, s1, act1, c.bn1, grid_for(mt_shared * s1.n_tiles, 1), c.st);
+            if (e == cudaSuccess)
+                e = launch_gemm_tc(c.mAs2, c.mB2, c.mB2, s2, kActNone, c.bn2, grid_for(mt_shared * s2.n_tiles, 1),
+                                   c.st);
+        }
+    } else {
+        g1.n_tiles = ceil_div(L.F, kFfmaTileN);
+        g2.n_tiles = ceil_div(L.d, kFfmaTileN);
+        if (mt_routed > 0) {
+            e = launch_gemm_ffma(c.at<void>(L.off_xp), L.d, c.in->W1, c.in->W3, L.d, g1, act1, c.bf16,
+                                 grid_for(mt_routed * g1.n_tiles, 4), c.st);
+            if (e == cudaSuccess)
+                e = launch_gemm_ffma(c.at<void>(L.off_h), L.F, c.in->W2, nullptr, L.F, g2, kActNone, c.bf16,
+                                     grid_for(mt_routed * g2.n_tiles, 4), c.st);
+        }
+        if (e == cudaSuccess && L.S > 0) {
+            s1.n_tiles = ceil_div(s1.N, kFfmaTileN);
+            s2.n_tiles = ceil_div(L.d, kFfmaTileN);
+            e = launch_gemm_ffma(c.in->x, L.d, c.in->W1, c.in->W3, L.d, s1, act1, c.bf16,
+                                 grid_for(mt_shared * s1.n_tiles, 4), c.st);
+            if (e == cudaSuccess)
+                e = launch_gemm_ffma(c.at<void>(L.off_hs), L.S * L.F, c.in->W2, nullptr, L.F, s2, kActNone,
+                                     c.bf16, grid_for(mt_shared * s2.n_tiles, 4), c.st);
+        }
+    }
+    return cuda_status(e);
+}
+
+moe_status_t stage_combine(Ctx& c)
+{
+    CombineArgs a{};
+    a.yp = c.at<void>(c.L.off_yp);
+    a.ys = c.L.S > 0 ? c.at<void>(c.L.off_ys) : nullptr;
+    a.x = c.in->x;
+    a.slot_row = c.at<int32_t>(c.L.off_slot_row);
+    a.gates = c.out->gates;
+    a.y = c.out->y;
+    a.T = c.L.T;
+    a.k = c.L.k;
+    a.d = c.L.d;
+    a.residual_mode = c.p.residual_mode;
+    return cuda_status(launch_combine(a, c.bf16, c.sms, c.st));
+}
+
+using StageFn = moe_status_t (*)(Ctx&);
+
+moe_status_t run_stages(const moe_params_t* params, const moe_inputs_t* in, moe_outputs_t* out, void* ws,
+                        size_t ws_bytes, void* stream, std::initializer_list<StageFn> stages)
+{
+    Ctx c;
+    moe_status_t s = prepare(params, in, out, ws, ws_bytes, stream, c);
+    if (s != MOE_OK) return s;
+    for (StageFn f : stages) {
+        s = f(c);
+        if (s != MOE_OK) return s;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_workspace_size(const moe_params_t* params, size_t* bytes)
+{
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = validate_params(params);
+    if (s != MOE_OK) return s;
+    *bytes = make_layout(*params).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,
+                         void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream,
+                      {stage_router, stage_dispatch, stage_gemm, stage_combine});
+}
+
+moe_status_t moe_router(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,
+                        void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream, {stage_router});
+}
+
+moe_status_t moe_dispatch(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,
+                          void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream, {stage_dispatch});
+}
+
+moe_status_t moe_grouped_gemm(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,
+                              void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream, {stage_gemm});
+}
+
+moe_status_t moe_combine(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,
+                         void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream, {stage_combine});
+}
+
+moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (workspace == nullptr || workspace_bytes < sizeof(uint32_t)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_ERR_DEVICE_TIMEOUT;
+    }
+    return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t status)
+{
+    switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

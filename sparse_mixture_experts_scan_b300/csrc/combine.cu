@@ -1,0 +1,130 @@
+// combine.cu -- stage 4 of the layer: gate-weighted un-permute and accumulate.
+//
+// y[t] = sum over the kept slots j of token t (slot order) of g[t,j] * Yp[row(t,j)]
+//      + Ys[t]                (shared experts, gate 1; "MoE 混合专家模型串讲" §"共享专家隔离")
+//      + x[t] if pass(t)      (dropped token: 0 + x = x; "MoE 混合专家模型串讲" §"专家容量")
+// accumulated in fp32 and rounded once ("混合专家模型MoE入门实战" §3.4 output[mask]
+// += weight * expert_output; "混合专家 MOE 是什么" y = sum_i g_i e_i(x)).
+// pass(t) is 1 for every token when residual_mode == 1; with residual_mode 0 it
+// is 1 only when all k routed slots of t were dropped.
+//
+// One warp per token; each lane handles 16-byte vectors of the row; no atomics,
+// so the result is deterministic.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const void* p, float (&v)[8])
+    {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static void store(void* p, const float (&v)[8])
+    {
+        uint4 u;
+        u.x = pack_bf16x2(v[0], v[1]);
+        u.y = pack_bf16x2(v[2], v[3]);
+        u.z = pack_bf16x2(v[4], v[5]);
+        u.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const void* p, float (&v)[4])
+    {
+        const float4 u = *reinterpret_cast<const float4*>(p);
+        v[0] = u.x;
+        v[1] = u.y;
+        v[2] = u.z;
+        v[3] = u.w;
+    }
+    __device__ static void store(void* p, const float (&v)[4])
+    {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_combine(CombineArgs a)
+{
+    constexpr int V = Vec<T>::N;
+    __shared__ int s_row[8][kMaxTopK];
+    __shared__ float s_gate[8][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = a.d / V;
+    const size_t row_bytes = (size_t)a.d * sizeof(T);
+    const unsigned all_k = (a.k >= 32) ? 0xffffffffu : ((1u << a.k) - 1u);
+
+    for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
+        int r = -1;
+        float g = 0.0f;
+        if (lane < a.k) {
+            r = a.slot_row[(size_t)t * a.k + lane];
+            g = a.gates[(size_t)t * a.k + lane];
+            s_row[warp][lane] = r;
+            s_gate[warp][lane] = g;
+        }
+        const unsigned dropped = __ballot_sync(0xffffffffu, lane < a.k && r < 0);
+        const bool pass = a.residual_mode == 1 || dropped == all_k;
+        __syncwarp();
+        const char* xrow = static_cast<const char*>(a.x) + (size_t)t * row_bytes;
+        const char* ysrow = a.ys ? static_cast<const char*>(a.ys) + (size_t)t * row_bytes : nullptr;
+        char* yrow = static_cast<char*>(a.y) + (size_t)t * row_bytes;
+        for (int v = lane; v < nvec; v += 32) {
+            float acc[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+            for (int j = 0; j < a.k; ++j) {
+                const int rj = s_row[warp][j];
+                if (rj < 0) continue;
+                const float gj = s_gate[warp][j];
+                float u[V];
+                Vec<T>::load(static_cast<const char*>(a.yp) + (size_t)rj * row_bytes + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] = fmaf(gj, u[i], acc[i]);
+            }
+            if (ysrow) {
+                float u[V];
+                Vec<T>::load(ysrow + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += u[i];
+            }
+            if (pass) {
+                float u[V];
+                Vec<T>::load(xrow + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += u[i];
+            }
+            Vec<T>::store(yrow + v * 16, acc);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st)
+{
+    long long grid = ((long long)a.T + 7) / 8;
+    if (grid > (long long)num_sms * 32) grid = (long long)num_sms * 32;
+    if (bf16) k_combine<__nv_bfloat16><<<(int)grid, 256, 0, st>>>(a);
+    else k_combine<float><<<(int)grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,313 @@
+// common.cuh -- shared device helpers of the B300 MoE library (sm_103a).
+//
+// Inline-PTX wrappers for mbarriers, TMA (cp.async.bulk.tensor), and the
+// 5th-generation tensor core (tcgen05: TMEM allocation, MMA, commit, loads),
+// written from the PTX ISA description of those instructions; plus the
+// workspace layout that the host API and every kernel agree on.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Expert segments in the permuted buffers are padded to this many rows: the
+// grouped GEMM's tile height, so a tile never straddles two experts.
+constexpr int kSegRows = 128;
+// Slots per dispatch-scan block (one thread per slot).
+constexpr int kScanChunk = 1024;
+// Tokens per router block.
+constexpr int kRouterTokens = 32;
+// Limits of this build (mirrored by MOE_MAX_EXPERTS / MOE_MAX_TOPK in moe.h).
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+
+// Device error word bits (sticky until moe_last_device_status reads them).
+enum : uint32_t {
+    kErrTimeoutProducer = 1u,
+    kErrTimeoutMma = 2u,
+    kErrTimeoutEpilogue = 4u,
+    kErrTimeoutDrain = 8u,
+};
+
+// Bounded waits give up after this long and flag kErrTimeout*.
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s
+
+__host__ __device__ constexpr inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+// ---------------------------------------------------------------------------
+// Scalar helpers
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Gives up
+// (returns false) after kWaitTimeoutNs or as soon as *abort is set, so that no
+// wait can spin forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled load of box {c0 (innermost), c1} into shared memory; completion is
+// signalled on `bar` as transaction bytes.  c0 * element size must be a
+// multiple of 16 bytes (callers pass multiples of 64 bf16 elements).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, uint64_t cache_policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+        "cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1),
+        "l"(cache_policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor core, accumulators in tensor memory)
+
+// Allocate `ncols` TMEM columns (power of two >= 32); the TMEM address is
+// written to shared memory.  Executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile stored with the
+// 128-byte swizzle: rows of 64 bf16 (128 B), 8-row core groups 1024 B apart.
+// Fields: start address >> 4 (bits 0-13), leading-dimension byte offset >> 4
+// (bits 16-29, unused for swizzled K-major), stride-dimension byte offset >> 4
+// (bits 32-45), descriptor version 1 (bits 46-47), swizzle mode 2 = 128-byte
+// (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Each thread of the warp loads 32 consecutive fp32 columns of its TMEM lane.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Activations (fp32).  GELU(tanh), GELU(erf): Hendrycks & Gimpel; silu(z) = z / (1 + e^-z).
+
+enum ActKind : int { kActNone = -1, kActRelu = 0, kActGeluTanh = 1, kActGeluErf = 2, kActSwiglu = 3 };
+
+template <int ACT>
+__device__ __forceinline__ float activate(float z)
+{
+    if constexpr (ACT == kActRelu) {
+        return fmaxf(z, 0.0f);
+    } else if constexpr (ACT == kActGeluTanh) {
+        const float c = 0.7978845608028654f;  // sqrt(2/pi)
+        return 0.5f * z * (1.0f + tanhf(c * (z + 0.044715f * z * z * z)));
+    } else if constexpr (ACT == kActGeluErf) {
+        return 0.5f * z * (1.0f + erff(z * 0.7071067811865476f));
+    } else if constexpr (ACT == kActSwiglu) {
+        return z / (1.0f + expf(-z));
+    } else {
+        return z;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM problem description (shared by the tcgen05 and FFMA kernels).
+//
+// Groups are experts.  Group g owns rows [row_off(g), row_off(g) + rows(g)) of
+// A and of the output; its M-tiles are numbered mtile_off[g] .. mtile_off[g+1]-1.
+// Either the three arrays come from the dispatch scan (routed experts) or,
+// when mtile_off == nullptr, there is one group of `fixed_rows` rows at row 0
+// (shared experts over all tokens).
+// B is the 2-D view [groups * b_rows_per_group, K] of a weight tensor; group g,
+// K-segment s and output column n read B row
+//   (b_group0 + g + s) * b_rows_per_group + n.
+// A column of K-segment s is s * K + kk.  The output is [rows, ldo]; bias (if
+// any) of output column n is sum_s bias[(b_group0 + g + s) * b_rows_per_group + n].
+struct GroupedGemmArgs {
+    const int* mtile_off;  // [G+1] device, or nullptr for one fixed group
+    const int* row_off;    // [G] device padded row offsets
+    const int* rows;       // [G] device valid rows per group
+    int G;
+    int fixed_rows;
+    int N;                 // valid output columns per group
+    int n_tiles;           // output column tiles per group
+    int K;                 // reduction length of one K-segment
+    int k_segments;
+    int b_rows_per_group;
+    int b_group0;
+    void* out;
+    int ldo;
+    const void* bias;
+    int a_rows_alloc;      // rows of A that exist (FFMA bounds)
+    uint32_t* err;
+};
+
+}  // namespace moe

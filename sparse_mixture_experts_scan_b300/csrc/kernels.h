@@ -1,0 +1,84 @@
+// kernels.h -- internal launch interface between the host API (api.cu) and the
+// device kernels.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---- stage 1: router -------------------------------------------------------
+struct RouterArgs {
+    const void* x;        // [T, d] fp32 or bf16
+    const float* Wg;      // [E, d]
+    const float* bg;      // [E] or nullptr
+    int T, d, E, k, renormalize;
+    int32_t* idx;         // [T, k]
+    float* gates;         // [T, k]
+    float* logits;        // [T, E] or nullptr
+    float* probs;         // [T, E] or nullptr
+    float* psum_part;     // [router_blocks(T), E] per-block column sums of p
+    unsigned* scan_done;  // dispatch-scan arrival counter, reset here
+};
+int router_blocks(int T);
+cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st);
+
+// ---- stage 2: dispatch -----------------------------------------------------
+struct DispatchArgs {
+    const int32_t* idx;   // [T, k]
+    const float* gates;   // [T, k]
+    int T, k, E;
+    int C;                // capacity, -1 = none
+    int nchunks;          // ceil(T*k / kScanChunk)
+    int n_router_blocks;
+    const float* psum_part;
+    int32_t* local_rank;  // [T*k] rank of the slot among its chunk's slots of the same expert
+    int32_t* chunk_hist;  // [nchunks, E]
+    int32_t* chunk_base;  // [nchunks, E] exclusive prefix over chunks
+    unsigned* scan_done;
+    int32_t* counts;      // [E] (user output)
+    int32_t* kept;        // [E]
+    int32_t* row_off;     // [E] padded segment start rows
+    int32_t* kept_off;    // [E] unpadded start rows
+    int32_t* mtile_off;   // [E+1]
+    float* aux;           // [1] (user output)
+    // permute
+    const void* x;        // [T, d]
+    void* xp;             // [rows_cap, d]
+    int row_bytes;        // d * element size
+    uint8_t* dropped;     // [T, k]
+    int32_t* perm_row;    // [T, k] or nullptr
+    int32_t* slot_row;    // [T, k] padded row of the slot or -1
+};
+size_t dispatch_scan_smem(int E);
+cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st);
+
+// ---- stage 3: grouped GEMMs ------------------------------------------------
+// tcgen05 kernel: act is kActNone (plain GEMM), kActRelu, kActGeluTanh,
+// kActGeluErf (bias allowed) or kActSwiglu (gated: B rows from W1 and W3).
+cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                           const GroupedGemmArgs& args, int act, int bn, int grid,
+                           cudaStream_t st);
+size_t gemm_tc_smem(int bn);
+// FFMA kernel over fp32 or bf16 operands (A [a_rows_alloc, lda], B [*, ldb]).
+cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
+                             const GroupedGemmArgs& args, int act, bool bf16, int grid,
+                             cudaStream_t st);
+constexpr int kFfmaTileN = 64;
+
+// ---- stage 4: combine ------------------------------------------------------
+struct CombineArgs {
+    const void* yp;       // [rows_cap, d]
+    const void* ys;       // [T_pad, d] shared-expert output or nullptr
+    const void* x;        // [T, d]
+    const int32_t* slot_row;
+    const float* gates;
+    void* y;              // [T, d]
+    int T, k, d, residual_mode;
+};
+cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,194 @@
+// router.cu -- stage 1 of the layer: the fp32 softmax router and top-k.
+//
+// logits[t,e] = sum_i x[t,i] * W_gate[e,i] (+ b_gate[e]), accumulated in fp32
+// ("混合专家 MOE 是什么" §"公式：三步走": g = softmax(W_g x); the router is
+// computed in fp32 as "MoE 混合专家模型串讲" §"选择性精度" prescribes).
+// p = softmax over the E routed experts; the k largest logits are selected
+// with a warp-shuffle argmax, ties to the lower expert index ("混合专家模型MoE
+// 入门实战" §3.3 torch.topk; "MoE架构解析" §2.1 top_k on the logits - the same
+// experts, softmax being monotone).  Gates are p, or p divided by the sum of
+// the k selected p ("混合专家模型MoE入门实战" §3.3 重新归一化).
+//
+// One block = 32 tokens = 8 warps x 4 tokens; lane l of a warp owns experts
+// l, l+32, ... (EJ of them), so after the d-loop every warp holds full logit
+// rows of its tokens in registers and finishes softmax/top-k with shuffles.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouterBK = 16;  // d-chunk staged in shared memory
+constexpr int kTokPerWarp = kRouterTokens / 8;
+
+template <typename TX, int EJ>
+__global__ void __launch_bounds__(256) k_router(RouterArgs a)
+{
+    constexpr int kWsStride = kRouterBK + 1;  // conflict-free column reads
+    __shared__ float xs[kRouterTokens][kRouterBK];
+    __shared__ float ws[32 * EJ * kWsStride];  // reused for the column sums afterwards
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRouterTokens;
+    const TX* x = static_cast<const TX*>(a.x);
+
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
+
+    float acc[kTokPerWarp][EJ];
+#pragma unroll
+    for (int i = 0; i < kTokPerWarp; ++i)
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) acc[i][j] = 0.0f;
+
+    for (int k0 = 0; k0 < a.d; k0 += kRouterBK) {
+        // x tile: 32 tokens x 16 columns, one element per thread pair
+        for (int v = threadIdx.x; v < kRouterTokens * kRouterBK; v += 256) {
+            const int r = v / kRouterBK, c = v % kRouterBK;
+            const int t = t0 + r, col = k0 + c;
+            xs[r][c] = (t < a.T && col < a.d) ? to_f32(x[(size_t)t * a.d + col]) : 0.0f;
+        }
+        for (int v = threadIdx.x; v < 32 * EJ * kRouterBK; v += 256) {
+            const int r = v / kRouterBK, c = v % kRouterBK;
+            const int col = k0 + c;
+            ws[r * kWsStride + c] = (r < a.E && col < a.d) ? a.Wg[(size_t)r * a.d + col] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kRouterBK; ++kk) {
+            float xv[kTokPerWarp];
+#pragma unroll
+            for (int i = 0; i < kTokPerWarp; ++i) xv[i] = xs[warp * kTokPerWarp + i][kk];
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) {
+                const float wv = ws[(lane + 32 * j) * kWsStride + kk];
+#pragma unroll
+                for (int i = 0; i < kTokPerWarp; ++i) acc[i][j] = fmaf(xv[i], wv, acc[i][j]);
+            }
+        }
+        __syncthreads();
+    }
+
+    float bias[EJ];
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) {
+        const int e = lane + 32 * j;
+        bias[j] = (a.bg != nullptr && e < a.E) ? a.bg[e] : 0.0f;
+    }
+
+    float psum[EJ];
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) psum[j] = 0.0f;
+
+#pragma unroll
+    for (int i = 0; i < kTokPerWarp; ++i) {
+        const int t = t0 + warp * kTokPerWarp + i;
+        if (t >= a.T) break;  // warp-uniform
+        float l[EJ];
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            l[j] = (e < a.E) ? acc[i][j] + bias[j] : -INFINITY;
+            m = fmaxf(m, l[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float p[EJ];
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            p[j] = (e < a.E) ? expf(l[j] - m) : 0.0f;
+            s += p[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            p[j] *= inv;
+            psum[j] += p[j];
+            if (e < a.E) {
+                if (a.logits) a.logits[(size_t)t * a.E + e] = l[j];
+                if (a.probs) a.probs[(size_t)t * a.E + e] = p[j];
+            }
+        }
+
+        // top-k: k rounds of a warp argmax over (logit desc, expert asc)
+        uint32_t taken = 0;
+        int my_e = 0;
+        float my_p = 0.0f, gsum = 0.0f;
+        for (int r = 0; r < a.k; ++r) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+            float bp = 0.0f;
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) {
+                const int e = lane + 32 * j;
+                if (e < a.E && !((taken >> j) & 1u) && (l[j] > bv || be == 0x7fffffff)) {
+                    bv = l[j];
+                    be = e;
+                    bp = p[j];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                    bp = op;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            if (lane == r) {
+                my_e = be;
+                my_p = bp;
+            }
+            gsum += bp;
+        }
+        if (lane < a.k) {
+            a.idx[(size_t)t * a.k + lane] = my_e;
+            a.gates[(size_t)t * a.k + lane] = a.renormalize ? my_p / gsum : my_p;
+        }
+    }
+
+    // deterministic block column sums of p: warps in order, tokens in order
+    float* psum_s = ws;  // 8 x 32*EJ floats; the d-loop ended with a barrier
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) psum_s[warp * 32 * EJ + lane + 32 * j] = psum[j];
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += 256) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += psum_s[w * 32 * EJ + e];
+        a.psum_part[(size_t)blockIdx.x * a.E + e] = s;
+    }
+}
+
+template <typename TX>
+cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st)
+{
+    const int grid = ceil_div(a.T, kRouterTokens);
+    if (a.E <= 32) k_router<TX, 1><<<grid, 256, 0, st>>>(a);
+    else if (a.E <= 64) k_router<TX, 2><<<grid, 256, 0, st>>>(a);
+    else if (a.E <= 128) k_router<TX, 4><<<grid, 256, 0, st>>>(a);
+    else if (a.E <= 256) k_router<TX, 8><<<grid, 256, 0, st>>>(a);
+    else k_router<TX, 16><<<grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int router_blocks(int T) { return ceil_div(T, kRouterTokens); }
+
+cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st)
+{
+    return bf16 ? launch_router_t<__nv_bfloat16>(a, st) : launch_router_t<float>(a, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,109 @@
+"""Torch-facing convenience over the C ABI: allocation and pointer marshalling.
+
+PyTorch provides device memory and streams only; every step of the layer runs
+in libmoe_b300.so through the C entry points of `_lib`.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from .inputs import LayerConfig
+
+ACT_CODES = {"relu": _lib.MOE_ACT_RELU, "gelu_tanh": _lib.MOE_ACT_GELU_TANH,
+             "gelu_erf": _lib.MOE_ACT_GELU_ERF, "swiglu": _lib.MOE_ACT_SWIGLU}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_lib.moe_status_string(status)} ({status})")
+        self.status = status
+
+
+def check(status: int, where: str = "moe") -> None:
+    if status != _lib.MOE_OK:
+        raise MoEError(status, where)
+
+
+def make_params(cfg: LayerConfig, *, flags: int = 0, residual_mode: int | None = None,
+                T: int | None = None) -> _lib.moe_params_t:
+    return _lib.moe_params_t(
+        T=cfg.T if T is None else T, d_model=cfg.d, d_ff=cfg.F, E=cfg.E, k=cfg.k, n_shared=cfg.S,
+        capacity_factor=0.0 if cfg.cf is None else float(cfg.cf),
+        renormalize=int(cfg.renormalize),
+        residual_mode=cfg.residual_mode if residual_mode is None else residual_mode,
+        act=ACT_CODES[cfg.act], dtype=_lib.MOE_BF16 if cfg.dtype == "bf16" else _lib.MOE_F32,
+        flags=flags)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class MoELayer:
+    """Outputs and workspace for one layer configuration, preallocated on `device`.
+
+    `run()` is one C call (moe_forward by default) on the current torch stream.
+    """
+
+    def __init__(self, cfg: LayerConfig, weights: dict, device="cuda", *, flags: int = 0,
+                 residual_mode: int | None = None, want_logits: bool = False,
+                 want_probs: bool = False, want_perm: bool = True):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.params = make_params(cfg, flags=flags, residual_mode=residual_mode)
+        st, nbytes = _lib.moe_workspace_size(self.params)
+        check(st, "moe_workspace_size")
+        self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        self.workspace_bytes = nbytes
+        self.weights = {k: (None if v is None else v.contiguous()) for k, v in weights.items()}
+        T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+        dev = self.device
+        self.out = {
+            "y": torch.empty(T, d, dtype=cfg.torch_dtype, device=dev),
+            "expert_idx": torch.empty(T, k, dtype=torch.int32, device=dev),
+            "gates": torch.empty(T, k, dtype=torch.float32, device=dev),
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "dropped": torch.empty(T, k, dtype=torch.uint8, device=dev),
+            "aux": torch.empty(1, dtype=torch.float32, device=dev),
+            "logits": torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None,
+            "probs": torch.empty(T, E, dtype=torch.float32, device=dev) if want_probs else None,
+            "perm_row": torch.empty(T, k, dtype=torch.int32, device=dev) if want_perm else None,
+        }
+        w = self.weights
+        self.inputs = _lib.moe_inputs_t(
+            x=_ptr(w["x"]), W_gate=_ptr(w["W_gate"]), b_gate=_ptr(w.get("b_gate")), W1=_ptr(w["W1"]),
+            W3=_ptr(w.get("W3")), W2=_ptr(w["W2"]), b1=_ptr(w.get("b1")), b2=_ptr(w.get("b2")))
+        o = self.out
+        self.outputs = _lib.moe_outputs_t(
+            y=_ptr(o["y"]), expert_idx=_ptr(o["expert_idx"]), gates=_ptr(o["gates"]),
+            counts=_ptr(o["counts"]), dropped=_ptr(o["dropped"]), aux=_ptr(o["aux"]),
+            logits=_ptr(o["logits"]), probs=_ptr(o["probs"]), perm_row=_ptr(o["perm_row"]))
+
+    def set_x(self, x: torch.Tensor) -> None:
+        """Point the layer at a new [T, d] input (kept alive by the layer)."""
+        x = x.contiguous()
+        self.weights["x"] = x
+        self.inputs.x = x.data_ptr()
+
+    def run(self, stage: str = "moe_forward", stream=None) -> dict:
+        fn = getattr(_lib, stage)
+        check(fn(self.params, self.inputs, self.outputs, self.workspace.data_ptr(),
+                 self.workspace_bytes, _stream_handle(stream)), stage)
+        return self.out
+
+    def device_status(self, stream=None) -> int:
+        return _lib.moe_last_device_status(self.workspace.data_ptr(), self.workspace_bytes,
+                                           _stream_handle(stream))
+
+
+def forward(cfg: LayerConfig, weights: dict, **kw) -> dict:
+    """One-shot layer forward: allocate, run moe_forward, return the outputs."""
+    layer = MoELayer(cfg, weights, device=weights["x"].device, **kw)
+    return layer.run()

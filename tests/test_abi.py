@@ -1,0 +1,127 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+
+import pytest
+
+from sparse_mixture_experts_scan_b300 import _lib, config, make_params
+
+
+def test_library_exports_every_header_function():
+    names = _lib.header_functions()
+    assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
+                          "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
+                          "moe_status_string"}
+    L = _lib.load()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_UNSUPPORTED"),
+                       (3, "MOE_ERR_WORKSPACE"), (4, "MOE_ERR_CUDA"), (5, "MOE_ERR_DEVICE_TIMEOUT")]:
+        assert _lib.moe_status_string(code) == name
+
+
+def test_struct_layouts_match_header():
+    # moe_params_t: 11 int32/float fields + uint32 flags
+    assert ctypes.sizeof(_lib.moe_params_t) == 12 * 4
+    assert ctypes.sizeof(_lib.moe_inputs_t) == 8 * 8
+    assert ctypes.sizeof(_lib.moe_outputs_t) == 9 * 8
+
+
+@pytest.mark.parametrize("name", ["tiny", "switch", "mixtral", "deepseek", "skewed", "decode"])
+def test_workspace_size_of_configs(name):
+    cfg = config(name)
+    st, n = _lib.moe_workspace_size(make_params(cfg))
+    assert st == _lib.MOE_OK and n > 0
+    # the permuted activations alone need at least the kept rows of x (bf16 / fp32)
+    esz = 2 if cfg.dtype == "bf16" else 4
+    assert n >= min(cfg.T * cfg.k, cfg.T * cfg.k) * cfg.d * esz or cfg.cf is not None
+
+
+def test_workspace_grows_with_tokens():
+    cfg = config("switch")
+    sizes = [_lib.moe_workspace_size(make_params(cfg, T=t))[1] for t in (128, 1024, 8192, 65536)]
+    assert sizes == sorted(sizes) and len(set(sizes)) == 4
+
+
+@pytest.mark.parametrize("field,value", [
+    ("k", 0), ("k", 9), ("E", 0), ("E", 513), ("d_model", 12), ("d_ff", 20), ("T", 0),
+    ("renormalize", 2), ("residual_mode", 5), ("act", 7), ("dtype", 3), ("flags", 8),
+    ("n_shared", -1)])
+def test_invalid_params_rejected(field, value):
+    p = make_params(config("mixtral"))
+    setattr(p, field, value)
+    st, _ = _lib.moe_workspace_size(p)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_k_above_topk_limit_rejected():
+    p = make_params(config("skewed"))
+    p.k = 33
+    assert _lib.moe_workspace_size(p)[0] == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_shared_experts_need_swiglu():
+    p = make_params(config("switch"))
+    p.n_shared = 1
+    assert _lib.moe_workspace_size(p)[0] == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_nan_capacity_rejected():
+    p = make_params(config("switch"))
+    p.capacity_factor = float("nan")
+    assert _lib.moe_workspace_size(p)[0] == _lib.MOE_ERR_INVALID_ARG
+
+
+def _fake_io(cfg, aligned=True):
+    """Structs filled with fake (never dereferenced) 256-byte aligned addresses."""
+    base = 1 << 40
+    a = lambda i: base + i * (1 << 30) + (0 if aligned else 4)  # noqa: E731
+    ins = _lib.moe_inputs_t(x=a(0), W_gate=a(1), b_gate=None, W1=a(2),
+                            W3=a(3) if cfg.act == "swiglu" else None, W2=a(4))
+    outs = _lib.moe_outputs_t(y=a(5), expert_idx=a(6), gates=a(7), counts=a(8), dropped=a(9),
+                              aux=a(10))
+    return ins, outs
+
+
+@pytest.mark.parametrize("stage", _lib.STAGES)
+def test_host_validation_happens_before_any_launch(stage):
+    cfg = config("mixtral")
+    p = make_params(cfg)
+    ins, outs = _fake_io(cfg)
+    _, need = _lib.moe_workspace_size(p)
+    ws = 1 << 44
+    fn = getattr(_lib, stage)
+    bad = make_params(cfg)
+    bad.k = 0
+    assert fn(bad, ins, outs, ws, need, None) == _lib.MOE_ERR_INVALID_ARG
+    # workspace missing, too small, unaligned
+    assert fn(p, ins, outs, None, need, None) == _lib.MOE_ERR_WORKSPACE
+    assert fn(p, ins, outs, ws, need - 1, None) == _lib.MOE_ERR_WORKSPACE
+    assert fn(p, ins, outs, ws + 16, need, None) == _lib.MOE_ERR_WORKSPACE
+    # required pointers
+    ins2, outs2 = _fake_io(cfg)
+    ins2.W3 = None  # SwiGLU needs W3
+    assert fn(p, ins2, outs2, ws, need, None) == _lib.MOE_ERR_INVALID_ARG
+    ins3, outs3 = _fake_io(cfg)
+    outs3.aux = None
+    assert fn(p, ins3, outs3, ws, need, None) == _lib.MOE_ERR_INVALID_ARG
+    ins4, outs4 = _fake_io(cfg, aligned=False)
+    assert fn(p, ins4, outs4, ws, need, None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_relu_layer_rejects_w3_and_swiglu_rejects_biases():
+    cfg = config("switch")
+    p = make_params(cfg)
+    ins, outs = _fake_io(cfg)
+    ins.W3 = ins.W1
+    _, need = _lib.moe_workspace_size(p)
+    assert _lib.moe_forward(p, ins, outs, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+    cfg2 = config("mixtral")
+    p2 = make_params(cfg2)
+    ins2, outs2 = _fake_io(cfg2)
+    ins2.b1 = ins2.W1
+    _, need2 = _lib.moe_workspace_size(p2)
+    assert _lib.moe_forward(p2, ins2, outs2, 1 << 44, need2, None) == _lib.MOE_ERR_INVALID_ARG

@@ -1,0 +1,164 @@
+"""GPU parity on small layers the oracle computes in full: every token, every
+output element, for each kernel path (tcgen05 and FFMA experts), plus the edge
+cases of the method (ragged sizes, k = E, one expert, capacity 0, exact ties,
+all tokens on one expert, shared experts, biases, residual modes)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from sparse_mixture_experts_scan_b300 import _lib, config, make_inputs
+from parity_utils import (check_dropped_tokens_pass_x, check_output, check_router_vs_fp64,
+                          check_routing_bitexact, run_device, to_cpu)
+
+pytestmark = pytest.mark.gpu
+
+FFMA = _lib.MOE_FLAG_FFMA_EXPERTS
+
+
+def _case(base, **kw):
+    return config(base, **kw)
+
+
+SMALL = {
+    # name: config
+    "swiglu_renorm": _case("mixtral", T=300, d=256, E=8, k=2, F=512),
+    "relu_capacity": _case("switch", T=1000, d=192, E=16, k=1, F=384, cf=1.0),
+    "switch_like_k1": _case("switch", T=2048, d=256, E=32, k=1, F=512, cf=1.25),
+    "gelu_tanh_bias": _case("tiny", T=257, d=128, E=4, k=2, F=256, dtype="bf16"),
+    "gelu_erf_k_eq_E": _case("tiny", T=130, d=64, E=3, k=3, F=64, act="gelu_erf", dtype="bf16"),
+    "shared_experts": _case("deepseek", T=200, d=128, E=16, k=4, F=200),
+    "single_expert": _case("mixtral", T=1000, d=128, E=1, k=1, F=256),
+    "ragged_dims": _case("mixtral", T=77, d=200, E=5, k=2, F=328),
+    "many_experts_drops": _case("skewed", T=512, d=128, E=256, k=8, F=128),
+    "max_experts": _case("mixtral", T=256, d=64, E=512, k=4, F=64),
+    "one_token": _case("mixtral", T=1, d=64, E=8, k=2, F=64),
+    "tiny_fp32": config("tiny"),
+    "fp32_swiglu_shared": _case("deepseek", T=100, d=64, E=8, k=2, F=48, dtype="f32"),
+}
+
+
+def _inputs(cfg, seed=0, random_bias=False):
+    inp = make_inputs(cfg, seed, device="cuda")
+    if random_bias and inp["b1"] is not None:
+        g = torch.Generator(device="cuda").manual_seed(seed + 7)
+        inp["b1"] = (torch.randn(inp["b1"].shape, generator=g, device="cuda") * 0.5).to(inp["b1"].dtype)
+        inp["b2"] = (torch.randn(inp["b2"].shape, generator=g, device="cuda") * 0.5).to(inp["b2"].dtype)
+        inp["b_gate"] = torch.randn(cfg.E, generator=g, device="cuda") * 0.1
+    return inp
+
+
+def _full_check(cfg, inp, flags=0, residual_mode=None):
+    out = run_device(cfg, inp, flags=flags, residual_mode=residual_mode)
+    cpu = to_cpu(inp)
+    r = check_routing_bitexact(cfg, out)
+    check_router_vs_fp64(cfg, cpu, out)
+    err = check_output(cfg, cpu, out, r, residual_mode=residual_mode)
+    check_dropped_tokens_pass_x(cfg, cpu, out, residual_mode)
+    return out, err
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_layer_matches_oracle(name):
+    cfg = SMALL[name]
+    _full_check(cfg, _inputs(cfg, random_bias=True))
+
+
+@pytest.mark.parametrize("name", ["swiglu_renorm", "relu_capacity", "gelu_tanh_bias", "shared_experts",
+                                  "ragged_dims"])
+def test_small_layer_ffma_experts_match_oracle(name):
+    cfg = SMALL[name]
+    _full_check(cfg, _inputs(cfg, random_bias=True), flags=FFMA)
+
+
+def test_worked_example_on_gpu():
+    # the 3-expert example embedded in d = F = 8 (extra rows/columns zero): logits
+    # [1,2,3], expert outputs 10/20/30 on component 0; y_0 = 25.752..., page 25.8
+    cfg = config("tiny", T=1, d=8, E=3, k=3, F=8, act="relu", bias=False)
+    x = torch.zeros(1, 8)
+    x[0, 0] = 1.0
+    Wg = torch.zeros(3, 8)
+    Wg[:, 0] = torch.tensor([1.0, 2.0, 3.0])
+    W1 = torch.zeros(3, 8, 8)
+    W1[:, 0, 0] = 1.0
+    W2 = torch.zeros(3, 8, 8)
+    W2[:, 0, 0] = torch.tensor([10.0, 20.0, 30.0])
+    inp = {"x": x.cuda(), "W_gate": Wg.cuda(), "b_gate": None, "W1": W1.cuda(), "W3": None,
+           "W2": W2.cuda(), "b1": None, "b2": None}
+    out = run_device(cfg, inp)
+    np.testing.assert_allclose(out["logits"][0].numpy(), [1.0, 2.0, 3.0])
+    np.testing.assert_array_equal(out["expert_idx"][0].numpy(), [2, 1, 0])
+    np.testing.assert_allclose(out["gates"][0].numpy(), [0.66524096, 0.24472847, 0.09003057],
+                               atol=1e-6)
+    assert round(float(out["y"][0, 0]), 1) == 25.8
+    assert abs(float(out["y"][0, 0]) - 25.7521038) < 1e-4
+    assert torch.count_nonzero(out["y"][0, 1:]) == 0
+
+
+def test_capacity_zero_returns_x_exactly():
+    cfg = _case("switch", T=64, d=128, E=256, k=2, F=128, cf=1.0)  # C = floor(64/256) = 0
+    inp = _inputs(cfg)
+    out = run_device(cfg, inp)
+    assert out["dropped"].bool().all()
+    assert torch.equal(out["y"], inp["x"].cpu())
+    check_routing_bitexact(cfg, out)
+
+
+def test_residual_mode_one_adds_x_everywhere():
+    cfg = SMALL["swiglu_renorm"]
+    inp = _inputs(cfg)
+    _full_check(cfg, inp, residual_mode=1)
+
+
+def test_exact_logit_ties_pick_lower_expert():
+    cfg = _case("mixtral", T=256, d=64, E=8, k=2, F=64)
+    inp = _inputs(cfg)
+    Wg = inp["W_gate"].clone()
+    Wg[5] = Wg[2]  # experts 2 and 5 score identically for every token
+    Wg[7] = Wg[0]
+    inp["W_gate"] = Wg
+    out, _ = _full_check(cfg, inp)
+    idx = out["expert_idx"].numpy()
+    # equal logits: whenever expert 5 (7) is selected, expert 2 (0) is selected too
+    for t in range(cfg.T):
+        row = set(idx[t].tolist())
+        assert not ({5} <= row and 2 not in row), idx[t]
+        assert not ({7} <= row and 0 not in row), idx[t]
+
+
+def test_all_tokens_on_one_expert():
+    cfg = _case("mixtral", T=700, d=128, E=8, k=1, F=256, renormalize=False)
+    inp = _inputs(cfg)
+    bg = torch.zeros(cfg.E, device="cuda")
+    bg[3] = 60.0
+    inp["b_gate"] = bg
+    out, _ = _full_check(cfg, inp)
+    assert (out["expert_idx"] == 3).all()
+    assert out["counts"][3] == cfg.T
+
+
+def test_stage_entry_points_equal_forward():
+    cfg = SMALL["shared_experts"]
+    inp = _inputs(cfg)
+    a = run_device(cfg, inp)
+    b = run_device(cfg, inp, stages=["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"])
+    for k in ("y", "expert_idx", "gates", "counts", "dropped", "aux", "perm_row", "logits"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_repeated_calls_are_deterministic():
+    cfg = SMALL["relu_capacity"]
+    inp = _inputs(cfg)
+    a = run_device(cfg, inp)
+    b = run_device(cfg, inp)
+    for k in ("y", "gates", "aux", "probs", "perm_row"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_tcgen05_and_ffma_experts_agree():
+    cfg = _case("mixtral", T=2048, d=512, E=8, k=2, F=1024)
+    inp = _inputs(cfg)
+    a = run_device(cfg, inp)
+    b = run_device(cfg, inp, flags=FFMA)
+    ya, yb = a["y"].double(), b["y"].double()
+    assert float((ya - yb).norm() / yb.norm()) < 1e-2
