@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MoE FFN layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Default workload: the Switch top-1 layer (T=8192, d=768, E=128, k=1, d_ff=3072,
+capacity factor 1.25, bf16 experts, fp32 router) on seeded synthetic inputs.
+A step is one pass of the whole layer (router, dispatch, grouped GEMM,
+combine) through the C ABI, timed with CUDA events on the launching stream;
+L2 is flushed (a 2x-L2 buffer is written) between steps, outside the timed
+events.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on the host cores instead: every
+step routes all T tokens and runs the experts on a seeded sample of tokens,
+the expert part extrapolated per kept slot to the whole batch.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+layer shards over tokens with no data-path exchange); timings are reduced with
+a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd tokens/s on 1 B300; % of bf16 TC peak and HBM GB/s"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="switch")
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_name(cfg) -> str:
+    cap = "none" if cfg.cf is None else f"{cfg.cf:g}"
+    shared = f"+{cfg.S}shared" if cfg.S else ""
+    return (f"{cfg.name} MoE FFN layer: T={cfg.T} d_model={cfg.d} E={cfg.E}{shared} k={cfg.k} "
+            f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts, fp32 router")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, path: str):
+        self.index, self.path, self.proc = index, path, None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(power)
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": top}
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_step(cfg, cpu_inp, n_sample: int, seed: int = 7):
+    """One bounded oracle pass: route all T tokens, experts on a token sample.
+
+    Returns (seconds-equivalent for the whole batch, description, threads)."""
+    import numpy as np
+    from oracle import moe_oracle as orc
+
+    t0 = time.perf_counter()
+    r = orc.route(cpu_inp["x"], cpu_inp["W_gate"], cpu_inp["b_gate"], k=cfg.k,
+                  renormalize=cfg.renormalize, cf=cfg.cf)
+    t_route = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    tok = np.sort(rng.choice(cfg.T, size=min(n_sample, cfg.T), replace=False))
+    t1 = time.perf_counter()
+    orc.output_rows(cpu_inp["x"], cpu_inp["W1"], cpu_inp["W3"], cpu_inp["W2"], cpu_inp["b1"],
+                    cpu_inp["b2"], r.idx, r.gates, r.dropped, E=cfg.E, S=cfg.S,
+                    act_name=cfg.act, residual_mode=cfg.residual_mode, tokens=tok)
+    t_ffn = time.perf_counter() - t1
+    kept_all = int((r.dropped == 0).sum()) + cfg.S * cfg.T
+    kept_smp = int((r.dropped[tok] == 0).sum()) + cfg.S * len(tok)
+    scale = kept_all / max(kept_smp, 1)
+    secs = t_route + t_ffn * scale
+    desc = (f"routing of all {cfg.T} tokens timed directly ({t_route:.2f} s); experts on a seeded "
+            f"sample of {len(tok)} tokens ({kept_smp} kept slots, {t_ffn:.2f} s) extrapolated "
+            f"per kept slot to {kept_all} slots")
+    return secs, desc, orc.num_threads()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from sparse_mixture_experts_scan_b300 import config, make_inputs
+
+    cfg = config(args.config)
+    inp = make_inputs(cfg, 0, device="cpu")
+    # size the per-step token sample so that warm-up + timed steps take ~2 minutes
+    t0 = time.perf_counter()
+    oracle_step(cfg, inp, 16)
+    probe = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(args.steps + args.warmup, 1)
+    n_sample = int(max(16, min(cfg.T, 16 * per_step_budget / max(probe, 1e-3))))
+    for _ in range(max(args.warmup - 1, 0)):
+        oracle_step(cfg, inp, n_sample)
+    secs, descs, threads = [], None, 1
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        s, descs, threads = oracle_step(cfg, inp, n_sample)
+        secs.append(s)
+    wall = time.perf_counter() - t_wall
+    per_step = sum(secs) / len(secs)
+    value = cfg.T / per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": descs + f"; {args.steps} steps in {wall:.1f} s wall"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def algorithmic_gemm_work(cfg, out):
+    """Bytes and flops the grouped-GEMM stage must move/do for this batch.
+
+    Bytes: weights of every expert that received >= 1 kept row (W1, W3, W2), the
+    permuted activations read once, the hidden activations written and read once,
+    the expert outputs written once (shared experts: all T rows).  Flops: 2 per
+    multiply-add on kept rows only."""
+    import torch
+    kept = (out["dropped"] == 0)
+    idx = out["expert_idx"].long()
+    kept_per_e = torch.zeros(cfg.E, dtype=torch.long, device=idx.device)
+    kept_per_e.scatter_add_(0, idx[kept], torch.ones_like(idx[kept]))
+    touched = int((kept_per_e > 0).sum()) + cfg.S
+    rows = int(kept.sum())
+    esz = 2 if cfg.dtype == "bf16" else 4
+    nmat = 3 if cfg.act == "swiglu" else 2
+    w_bytes = touched * nmat * cfg.d * cfg.F * esz
+    srows = cfg.S * cfg.T
+    act_bytes = (rows * (cfg.d + 2 * cfg.F + cfg.d) + cfg.T * cfg.d * (1 if cfg.S else 0)
+                 + srows * (2 * cfg.F + cfg.d)) * esz
+    flops = cfg.expert_flops(rows)
+    return {"bytes": w_bytes + act_bytes, "weight_bytes": w_bytes, "flops": flops,
+            "kept_rows": rows, "touched_experts": touched}
+
+
+def stage_bytes(cfg, out, gemm):
+    """Minimum HBM bytes of the memory-bound stages (router, dispatch, combine)."""
+    esz = 2 if cfg.dtype == "bf16" else 4
+    T, d, k, E = cfg.T, cfg.d, cfg.k, cfg.E
+    rows = gemm["kept_rows"]
+    router = T * d * esz + E * d * 4 + T * k * 8
+    dispatch = T * k * 4 + rows * d * esz * 2 + T * k * (1 + 4 + 4)
+    pass_tok = int((out["dropped"].bool().all(dim=1)).sum()) if cfg.residual_mode == 0 else T
+    combine = rows * d * esz + T * d * esz + pass_tok * d * esz + T * k * 8 + \
+        (T * d * esz if cfg.S else 0)
+    return {"moe_router": router, "moe_dispatch": dispatch, "moe_combine": combine}
+
+
+def traffic_from_profiles(kernel_file: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "sparse_mixture_experts_scan_b300", "csrc", kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    pat = re.compile(r"^traffic\s+(\S+)\s+(\S+)\s+bytes_per_step=(\d+)\s+source=([0-9a-f]+)")
+    with open(path) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(1) == kernel_file and m.group(2) == workload and m.group(4) == h:
+                return int(m.group(3))
+    return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mixture_experts_scan_b300 import MoELayer, config, make_inputs
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = config(args.config)
+    inp = make_inputs(cfg, seed=rank, device=dev)
+    layer = MoELayer(cfg, inp, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    stages = ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        for i, s in enumerate(stages):
+            if evs is not None:
+                evs[i].record(stream)
+            layer.run(s, stream)
+        if evs is not None:
+            evs[-1].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    clk = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                       if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with clk:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall0
+    stage_ms = {s: 0.0 for s in stages}
+    total_ms = 0.0
+    for i in range(K):
+        for j, s in enumerate(stages):
+            stage_ms[s] += evs[i][j].elapsed_time(evs[i][j + 1])
+        total_ms += evs[i][0].elapsed_time(evs[i][-1])
+    stage_ms = {s: v / K for s, v in stage_ms.items()}
+    ms_step = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * cfg.T / (ms_step * 1e-3)
+
+    out = layer.out
+    gemm = algorithmic_gemm_work(cfg, out)
+    sbytes = stage_bytes(cfg, out, gemm)
+    pk = peaks()
+    g_ms = stage_ms["moe_grouped_gemm"]
+    hbm_bound = gemm["flops"] / gemm["bytes"] < pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if hbm_bound:
+        achieved = gemm["bytes"] / (g_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"]}
+    else:
+        achieved = gemm["flops"] / (g_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"]}
+    wl_key = args.config
+    tr = traffic_from_profiles("grouped_gemm_tc.cu", wl_key)
+    roof.update({"traffic": tr, "kernel": "moe_grouped_gemm (tcgen05 grouped GEMM, GEMM1+GEMM2)",
+                 "algorithmic_bytes": gemm["bytes"], "algorithmic_flops": gemm["flops"],
+                 "touched_experts": gemm["touched_experts"], "kept_rows": gemm["kept_rows"],
+                 "peak_source": pk["source"] + " (burst)",
+                 "tensor_tflops": gemm["flops"] / (g_ms * 1e-3) / 1e12,
+                 "tensor_frac": gemm["flops"] / (g_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                 "hbm_gbs": gemm["bytes"] / (g_ms * 1e-3) / 1e9,
+                 "hbm_frac": gemm["bytes"] / (g_ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+    mem_stages = {}
+    for s in ("moe_router", "moe_dispatch", "moe_combine"):
+        gbs = sbytes[s] / (stage_ms[s] * 1e-3) / 1e9
+        mem_stages[s] = {"ms": stage_ms[s], "bytes": sbytes[s], "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]}
+    rdc_bytes = sum(sbytes.values())
+    rdc_ms = sum(stage_ms[s] for s in ("moe_router", "moe_dispatch", "moe_combine"))
+
+    # router 1, dispatch 2 (scan, permute), GEMM1+GEMM2 unless capacity is 0, shared 2, combine 1
+    cap_zero = cfg.cf is not None and int(cfg.T * cfg.cf / cfg.E) == 0
+    launches_per_step = 1 + 2 + (0 if cap_zero else 2) + (2 if cfg.S else 0) + 1
+
+    # ---- end to end: host x -> device, layer, y + aux -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp["x"].cpu().pin_memory()
+        y_host = torch.empty_like(out["y"], device="cpu").pin_memory()
+        aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+        layer.set_x(x_dev)
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for _ in range(max(args.warmup, 1)):
+            x_dev.copy_(x_host, non_blocking=True)
+            layer.run()
+            y_host.copy_(out["y"], non_blocking=True)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            e_s[i].record(stream)
+            x_dev.copy_(x_host, non_blocking=True)
+            layer.run("moe_forward", stream)
+            y_host.copy_(out["y"], non_blocking=True)
+            aux_host.copy_(out["aux"], non_blocking=True)
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K)) / K
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        esz = x_host.element_size()
+        e2e = {"value": world * cfg.T / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": x_host.numel() * esz,
+               "d2h_bytes_per_step": y_host.numel() * y_host.element_size() + 4,
+               "ms_per_step": e_ms}
+
+    status = layer.device_status()
+    if status != 0:
+        print(f"device status {status}", file=sys.stderr)
+        return 1
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu_base = None
+    if not args.no_cpu_baseline:
+        cpu_inp = {k: (None if v is None else v.cpu()) for k, v in inp.items()}
+        # about 10 G multiply-adds of expert work: ~10-30 s on the host cores
+        per_tok = cfg.d * cfg.F * (3 if cfg.act == "swiglu" else 2) * (cfg.k + cfg.S)
+        secs, desc, threads = oracle_step(cfg, cpu_inp, int(max(16, min(cfg.T, 1e10 / per_tok))))
+        cpu_base = {"value": cfg.T / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; shapes and distributions of the workload; random-init weights)",
+        "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
+                   "l2": "flushed between steps (2x L2 buffer written outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "stage_ms": stage_ms,
+                   "memory_stages": mem_stages,
+                   "router_dispatch_combine": {"bytes": rdc_bytes, "ms": rdc_ms,
+                                               "GB/s": rdc_bytes / (rdc_ms * 1e-3) / 1e9,
+                                               "frac": rdc_bytes / (rdc_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+                   "wall_s_timed_region": t_wall},
+        "roofline": roof,
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
