@@ -168,6 +168,33 @@ moe_status_t moe_combine(const moe_params_t* params, const moe_inputs_t* inputs,
  * debugging; not needed on the hot path. */
 moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free dispatch positions.  The pages have no counterpart: this is an
+ * addition for callers that cannot allocate device memory when they route tokens
+ * (an engine that owns all device memory through its own fixed pool and forbids
+ * libraries from allocating, or a latency-critical path that cannot pay for
+ * cudaMalloc's implicit synchronisation) and so cannot provide the workspace of
+ * moe_workspace_size.
+ *
+ * From the router's expert_idx [T, k] (as moe_router writes it) computes what
+ * moe_dispatch computes for the same selection: counts [E] (tokens per expert
+ * before drops), dropped [T, k] (1 = over the capacity floor(T cf / E)) and
+ * perm_row [T, k] (row in the expert-contiguous, token-ascending order of kept
+ * slots, -1 if dropped).  It does not compute the balance statistic and does not
+ * permute token rows.
+ *
+ * Scratch: a static device array of about 1 MB inside the library, one per device
+ * that loads the library, held until the process exits.  Limits: T * k <=
+ * MOE_NOALLOC_MAX_SLOTS and E <= MOE_MAX_EXPERTS; larger problems return
+ * MOE_ERR_INVALID_ARG and enqueue nothing.  The first call on a device looks up
+ * the array's device address (once, with that device current); make that first
+ * call before starting any stream capture.  All calls on a device share the array:
+ * calls whose work overlaps on the GPU (e.g. on two streams) race; calls ordered on
+ * one stream are safe.  Allocates nothing; all pointers are device pointers. */
+#define MOE_NOALLOC_MAX_SLOTS 131072
+moe_status_t moe_dispatch_positions_noalloc(const moe_params_t* params,
+                                            const int32_t* expert_idx, int32_t* counts,
+                                            uint8_t* dropped, int32_t* perm_row, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 

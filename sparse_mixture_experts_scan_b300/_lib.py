@@ -26,6 +26,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_FLAG_FFMA_EXPERTS = 1
 MOE_MAX_EXPERTS = 512
 MOE_MAX_TOPK = 32
+MOE_NOALLOC_MAX_SLOTS = 131072
 
 
 class moe_params_t(ctypes.Structure):
@@ -74,6 +75,8 @@ def load(build_if_stale: bool = True):
         f.argtypes = _STAGE_ARGS
     L.moe_last_device_status.restype = _i32
     L.moe_last_device_status.argtypes = [_vp, ctypes.c_size_t, _vp]
+    L.moe_dispatch_positions_noalloc.restype = _i32
+    L.moe_dispatch_positions_noalloc.argtypes = [_P(moe_params_t), _vp, _vp, _vp, _vp, _vp]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_status_string.argtypes = [_i32]
     _handle = L
@@ -120,6 +123,11 @@ def moe_grouped_gemm(params, inputs, outputs, workspace, workspace_bytes, stream
 
 def moe_combine(params, inputs, outputs, workspace, workspace_bytes, stream):
     return _stage("moe_combine", params, inputs, outputs, workspace, workspace_bytes, stream)
+
+
+def moe_dispatch_positions_noalloc(params, expert_idx, counts, dropped, perm_row, stream):
+    return load().moe_dispatch_positions_noalloc(ctypes.byref(params), _vp(expert_idx), _vp(counts),
+                                                 _vp(dropped), _vp(perm_row), _vp(stream))
 
 
 def moe_last_device_status(workspace, workspace_bytes, stream):

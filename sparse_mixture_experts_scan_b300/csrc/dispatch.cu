@@ -233,4 +233,17 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st)
     return cudaGetLastError();
 }
 
+cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st)
+{
+    const size_t smem = dispatch_scan_smem(a.E);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_dispatch_scan,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    k_dispatch_scan<<<a.nchunks, 1024, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

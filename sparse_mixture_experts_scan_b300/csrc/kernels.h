@@ -55,6 +55,8 @@ struct DispatchArgs {
 };
 size_t dispatch_scan_smem(int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st);
+// The scan kernel alone (no permute); used by the allocation-free entry point.
+cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st);
 
 // ---- stage 3: grouped GEMMs ------------------------------------------------
 // tcgen05 kernel: act is kActNone (plain GEMM), kActRelu, kActGeluTanh,

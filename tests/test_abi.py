@@ -11,7 +11,7 @@ def test_library_exports_every_header_function():
     names = _lib.header_functions()
     assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
-                          "moe_status_string"}
+                          "moe_status_string", "moe_dispatch_positions_noalloc"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
