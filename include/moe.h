@@ -64,6 +64,9 @@ typedef enum {
 /* moe_params_t.flags */
 #define MOE_FLAG_FFMA_EXPERTS 1u /* run bf16 experts on the CUDA-core FFMA grouped GEMM
                                     (cross-check kernel) instead of the tcgen05 one */
+#define MOE_FLAG_FFMA_ROUTER 2u  /* compute bf16 router logits with CUDA-core FFMA
+                                    (cross-check kernel) instead of the tensor-core
+                                    three-term split; fp32 layers always use FFMA */
 
 /* Limits of this build. */
 #define MOE_MAX_EXPERTS 512 /* E (routed) */

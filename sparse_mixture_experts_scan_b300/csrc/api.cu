@@ -27,6 +27,9 @@ struct Layout {
     int rows_cap;      // rows of the permuted buffers (multiple of 128)
     int t_pad;         // T rounded up to 128 (shared-expert buffers)
     size_t esz;        // element size of the activation dtype
+    bool tc_router;    // bf16 router logits on the tensor core
+    int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
+    size_t off_wsplit, off_logits;
     size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
         off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys, total;
 };
@@ -51,7 +54,7 @@ moe_status_t validate_params(const moe_params_t* p)
     if (p->residual_mode != 0 && p->residual_mode != 1) return MOE_ERR_INVALID_ARG;
     if (p->act < MOE_ACT_RELU || p->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-    if ((p->flags & ~MOE_FLAG_FFMA_EXPERTS) != 0u) return MOE_ERR_INVALID_ARG;
+    if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER)) != 0u) return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     // every index and row count below must fit in int32
@@ -83,6 +86,10 @@ Layout make_layout(const moe_params_t& p)
     L.rows_cap = (int)((cap + kSegRows - 1) / kSegRows * kSegRows);
     L.t_pad = (p.T + kSegRows - 1) / kSegRows * kSegRows;
     L.esz = (p.dtype == MOE_BF16) ? 2 : 4;
+    L.tc_router = p.dtype == MOE_BF16 && !(p.flags & MOE_FLAG_FFMA_ROUTER);
+    L.r_bn = router_tc_bn(p.E);
+    L.r_tiles = (p.E + L.r_bn - 1) / L.r_bn;
+    L.e_pad = L.r_tiles * L.r_bn;
 
     size_t o = kRegionAlign;  // header: [0] device error word, [1] scan arrival counter
     auto take = [&](size_t bytes) {
@@ -90,6 +97,8 @@ Layout make_layout(const moe_params_t& p)
         o = align_up(o + bytes, kRegionAlign);
         return at;
     };
+    L.off_wsplit = take(L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
+    L.off_logits = take(sizeof(float) * (size_t)L.T * L.E);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
     L.off_hist = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
     L.off_base = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
@@ -184,7 +193,7 @@ struct Ctx {
     int sms;
     bool bf16, use_tc;
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
-    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2;
+    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW;
     template <typename T>
     T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
     uint32_t* err() const { return reinterpret_cast<uint32_t*>(ws); }
@@ -212,6 +221,12 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.sms <= 0) return MOE_ERR_CUDA;
     c.bf16 = c.p.dtype == MOE_BF16;
     c.use_tc = c.bf16 && !(c.p.flags & MOE_FLAG_FFMA_EXPERTS);
+    if (c.L.tc_router) {
+        const Layout& L = c.L;
+        if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) ||
+            !encode_bf16_2d(&c.mW, c.at<void>(L.off_wsplit), 3ull * L.e_pad, L.d, L.r_bn))
+            return MOE_ERR_UNSUPPORTED;
+    }
     if (c.use_tc) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
@@ -252,7 +267,22 @@ moe_status_t stage_router(Ctx& c)
     a.probs = c.out->probs;
     a.psum_part = c.at<float>(c.L.off_psum);
     a.scan_done = c.scan_done();
-    return cuda_status(launch_router(a, c.bf16, c.st));
+    if (!c.L.tc_router) return cuda_status(launch_router(a, c.bf16, c.st));
+    // tensor-core logits into the caller's logits buffer (or the workspace), then top-k
+    if (a.logits == nullptr) a.logits = c.at<float>(c.L.off_logits);
+    RouterGemmArgs g{};
+    g.T = c.L.T;
+    g.d = c.L.d;
+    g.E = c.L.E;
+    g.E_pad = c.L.e_pad;
+    g.n_tiles = c.L.r_tiles;
+    g.bg = c.in->b_gate;
+    g.logits = a.logits;
+    g.err = c.err();
+    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st);
+    if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
+    if (e == cudaSuccess) e = launch_router_topk(a, c.st);
+    return cuda_status(e);
 }
 
 moe_status_t stage_dispatch(Ctx& c)

@@ -278,6 +278,23 @@ __device__ __forceinline__ float activate(float z)
     }
 }
 
+// Activations for epilogues whose result is rounded to bf16: the CUDA fast
+// intrinsics (__expf, __fdividef; about 2 ulp of fp32) are far below bf16's
+// rounding step and keep the unrolled epilogue small and branch-free.
+//   silu(z) = z / (1 + e^-z);  tanh(u) = 1 - 2 / (1 + e^{2u}).
+template <int ACT>
+__device__ __forceinline__ float activate_bf16out(float z)
+{
+    if constexpr (ACT == kActSwiglu) {
+        return __fdividef(z, 1.0f + __expf(-z));
+    } else if constexpr (ACT == kActGeluTanh) {
+        const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+        return 0.5f * z * (2.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * u)));
+    } else {
+        return activate<ACT>(z);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Grouped GEMM problem description (shared by the tcgen05 and FFMA kernels).
 //

@@ -110,7 +110,18 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     int my_count = 0, my_kept = 0;
     if (tid < E) {
         int run = 0;
-        for (int c = 0; c < a.nchunks; ++c) {
+        int c = 0;
+        for (; c + 8 <= a.nchunks; c += 8) {  // 8 independent loads in flight, summed in order
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(&a.chunk_hist[(size_t)(c + u) * E + tid]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                a.chunk_base[(size_t)(c + u) * E + tid] = run;
+                run += v[u];
+            }
+        }
+        for (; c < a.nchunks; ++c) {
             const int v = __ldcg(&a.chunk_hist[(size_t)c * E + tid]);
             a.chunk_base[(size_t)c * E + tid] = run;
             run += v;
@@ -140,8 +151,15 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     if (tid < P * E) {
         const int ee = tid % E, p = tid / E;
         float acc = 0.0f;
-        for (int b = p; b < a.n_router_blocks; b += P)
-            acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
+        int b = p;
+        for (; b + 7 * P < a.n_router_blocks; b += 8 * P) {  // 8 loads in flight, summed in order
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(&a.psum_part[(size_t)(b + u * P) * E + ee]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += v[u];
+        }
+        for (; b < a.n_router_blocks; b += P) acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
         s_part[p * E + ee] = acc;
     }
     __syncthreads();

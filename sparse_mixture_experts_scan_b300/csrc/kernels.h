@@ -24,7 +24,25 @@ struct RouterArgs {
     unsigned* scan_done;  // dispatch-scan arrival counter, reset here
 };
 int router_blocks(int T);
+// CUDA-core router: fp32 logits by FFMA, then softmax / top-k / gates.
 cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st);
+// Softmax / top-k / gates of logits already in a.logits.
+cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st);
+
+// Tensor-core router logits (bf16 x, W_gate split into three bf16 terms).
+struct RouterGemmArgs {
+    int T, d, E;
+    int E_pad;            // n_tiles * BN rows per split
+    int n_tiles;          // expert tiles of BN columns
+    const float* bg;      // [E] or nullptr
+    float* logits;        // [T, E] fp32
+    uint32_t* err;
+};
+int router_tc_bn(int E);  // MMA N of the router GEMM for E experts (16..128)
+cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms,
+                               cudaStream_t st);
+cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
+                                    int bn, int sms, cudaStream_t st);
 
 // ---- stage 2: dispatch -----------------------------------------------------
 struct DispatchArgs {

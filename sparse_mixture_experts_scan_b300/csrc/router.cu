@@ -22,6 +22,100 @@ namespace {
 constexpr int kRouterBK = 16;  // d-chunk staged in shared memory
 constexpr int kTokPerWarp = kRouterTokens / 8;
 
+// Softmax, top-k and gates of one token from its logit row l (lane owns experts
+// lane, lane+32, ...; -inf beyond E), executed by a whole warp.  Adds the token's
+// probabilities to the lane's running column sums.  write_logits = false when
+// the logits row already sits in a.logits.
+template <int EJ>
+__device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const RouterArgs& a,
+                                            bool write_logits, float (&psum)[EJ])
+{
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) m = fmaxf(m, l[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float p[EJ];
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) {
+        const int e = lane + 32 * j;
+        p[j] = (e < a.E) ? expf(l[j] - m) : 0.0f;
+        s += p[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) {
+        const int e = lane + 32 * j;
+        p[j] *= inv;
+        psum[j] += p[j];
+        if (e < a.E) {
+            if (write_logits && a.logits) a.logits[(size_t)t * a.E + e] = l[j];
+            if (a.probs) a.probs[(size_t)t * a.E + e] = p[j];
+        }
+    }
+
+    // top-k: k rounds of a warp argmax over (logit desc, expert asc)
+    uint32_t taken = 0;
+    int my_e = 0;
+    float my_p = 0.0f, gsum = 0.0f;
+    for (int r = 0; r < a.k; ++r) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+        float bp = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            if (e < a.E && !((taken >> j) & 1u) && (l[j] > bv || be == 0x7fffffff)) {
+                bv = l[j];
+                be = e;
+                bp = p[j];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+                bp = op;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == r) {
+            my_e = be;
+            my_p = bp;
+        }
+        gsum += bp;
+    }
+    if (lane < a.k) {
+        a.idx[(size_t)t * a.k + lane] = my_e;
+        a.gates[(size_t)t * a.k + lane] = a.renormalize ? my_p / gsum : my_p;
+    }
+}
+
+// Deterministic per-block column sums of p (warps in order, each warp's tokens in
+// order) into a.psum_part[blockIdx.x].  `scratch` holds 8 x 32*EJ floats.
+template <int EJ>
+__device__ __forceinline__ void block_psum(const float (&psum)[EJ], float* scratch, const RouterArgs& a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) scratch[warp * 32 * EJ + lane + 32 * j] = psum[j];
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += 256) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += scratch[w * 32 * EJ + e];
+        a.psum_part[(size_t)blockIdx.x * a.E + e] = s;
+    }
+}
+
 template <typename TX, int EJ>
 __global__ void __launch_bounds__(256) k_router(RouterArgs a)
 {
@@ -85,89 +179,43 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
         const int t = t0 + warp * kTokPerWarp + i;
         if (t >= a.T) break;  // warp-uniform
         float l[EJ];
-        float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < EJ; ++j) {
             const int e = lane + 32 * j;
             l[j] = (e < a.E) ? acc[i][j] + bias[j] : -INFINITY;
-            m = fmaxf(m, l[j]);
         }
+        route_token<EJ>(l, t, a, true, psum);
+    }
+
+    // the d-loop ended with a barrier: the weight tile is free for the column sums
+    block_psum<EJ>(psum, ws, a);
+}
+
+// Softmax / top-k / gates for logits already in a.logits (computed by the
+// tensor-core router GEMM); same block layout and column sums as k_router.
+template <int EJ>
+__global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
+{
+    __shared__ float scratch[8 * 32 * EJ];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRouterTokens;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
+    float psum[EJ];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float p[EJ];
-        float s = 0.0f;
+    for (int j = 0; j < EJ; ++j) psum[j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kTokPerWarp; ++i) {
+        const int t = t0 + warp * kTokPerWarp + i;
+        if (t >= a.T) break;  // warp-uniform
+        float l[EJ];
 #pragma unroll
         for (int j = 0; j < EJ; ++j) {
             const int e = lane + 32 * j;
-            p[j] = (e < a.E) ? expf(l[j] - m) : 0.0f;
-            s += p[j];
+            l[j] = (e < a.E) ? a.logits[(size_t)t * a.E + e] : -INFINITY;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        const float inv = 1.0f / s;
-#pragma unroll
-        for (int j = 0; j < EJ; ++j) {
-            const int e = lane + 32 * j;
-            p[j] *= inv;
-            psum[j] += p[j];
-            if (e < a.E) {
-                if (a.logits) a.logits[(size_t)t * a.E + e] = l[j];
-                if (a.probs) a.probs[(size_t)t * a.E + e] = p[j];
-            }
-        }
-
-        // top-k: k rounds of a warp argmax over (logit desc, expert asc)
-        uint32_t taken = 0;
-        int my_e = 0;
-        float my_p = 0.0f, gsum = 0.0f;
-        for (int r = 0; r < a.k; ++r) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-            float bp = 0.0f;
-#pragma unroll
-            for (int j = 0; j < EJ; ++j) {
-                const int e = lane + 32 * j;
-                if (e < a.E && !((taken >> j) & 1u) && (l[j] > bv || be == 0x7fffffff)) {
-                    bv = l[j];
-                    be = e;
-                    bp = p[j];
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                    bp = op;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == r) {
-                my_e = be;
-                my_p = bp;
-            }
-            gsum += bp;
-        }
-        if (lane < a.k) {
-            a.idx[(size_t)t * a.k + lane] = my_e;
-            a.gates[(size_t)t * a.k + lane] = a.renormalize ? my_p / gsum : my_p;
-        }
+        route_token<EJ>(l, t, a, false, psum);
     }
-
-    // deterministic block column sums of p: warps in order, tokens in order
-    float* psum_s = ws;  // 8 x 32*EJ floats; the d-loop ended with a barrier
-#pragma unroll
-    for (int j = 0; j < EJ; ++j) psum_s[warp * 32 * EJ + lane + 32 * j] = psum[j];
-    __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += 256) {
-        float s = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) s += psum_s[w * 32 * EJ + e];
-        a.psum_part[(size_t)blockIdx.x * a.E + e] = s;
-    }
+    block_psum<EJ>(psum, scratch, a);
 }
 
 template <typename TX>
@@ -182,9 +230,25 @@ cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+template <int EJ>
+cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
+{
+    k_router_topk<EJ><<<ceil_div(a.T, kRouterTokens), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int router_blocks(int T) { return ceil_div(T, kRouterTokens); }
+
+cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st)
+{
+    if (a.E <= 32) return launch_topk_ej<1>(a, st);
+    if (a.E <= 64) return launch_topk_ej<2>(a, st);
+    if (a.E <= 128) return launch_topk_ej<4>(a, st);
+    if (a.E <= 256) return launch_topk_ej<8>(a, st);
+    return launch_topk_ej<16>(a, st);
+}
 
 cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st)
 {

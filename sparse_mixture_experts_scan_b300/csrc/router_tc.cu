@@ -1,0 +1,335 @@
+// router_tc.cu -- stage 1 of bf16 layers on the tensor core: router logits.
+//
+// The router must run in fp32 ("MoE 混合专家模型串讲" §"选择性精度"), but the
+// logits x W_gate^T are a dense contraction.  x is bf16 already, so it is
+// exact; W_gate (fp32) is split exactly into three bf16 terms
+//     W = W_hi + W_mid + W_lo,  W_hi = bf16(W), W_mid = bf16(W - W_hi),
+//     W_lo = bf16(W - W_hi - W_mid)        (residual error <= 2^-24 |W|)
+// (the split-precision bfloat16 method of Henry, Tang and Heinecke, "Leveraging
+// the bfloat16 artificial intelligence datatype for higher-precision
+// computations", 2019).  Every bf16 x bf16 product is exact in fp32.
+//
+// The tensor core adds each MMA's partial products into the TMEM accumulator
+// with less than IEEE fp32 precision, so the error of one long accumulation
+// chain grows with its length (3 d / 16 MMAs).  The K loop is therefore cut
+// into chunks of kChunkKB K-blocks: each chunk accumulates in one of two TMEM
+// accumulators (alternating, so the MMAs of chunk c+1 overlap the drain of
+// chunk c), and the epilogue warps add every finished chunk into fp32
+// registers with round-to-nearest additions.  The error is then bounded by the
+// chunk length, independent of d, and comparable to an fp32 FFMA dot product.
+//
+// k_split_wgate writes [3, E_pad, d] bf16 (rows >= E zero) into the workspace.
+// k_router_logits_tc: persistent, one CTA per SM, warp-specialised like the
+// grouped GEMM: warp 0 TMA (x tile 128 x 64 + the three W tiles BN x 64 of one
+// K-block per stage), warp 1 tcgen05.mma (M = 128, N = BN, three splits, lo
+// first, one accumulator per chunk), warps 2-5 epilogue (chunk promotion into
+// fp32 registers, bias add, fp32 logits to global).  Softmax,
+// top-k and gates follow in k_router_topk (router.cu).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRBM = 128;
+constexpr int kRBK = 64;
+constexpr int kRThreads = 192;
+constexpr int kChunkKB = 2;  // K-blocks (of 64) per TMEM accumulation chunk
+
+template <int BN>
+struct RCfg {
+    static constexpr uint32_t A_BYTES = kRBM * kRBK * 2;
+    static constexpr uint32_t B_BYTES = BN * kRBK * 2;  // one split
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+    static constexpr int STAGES_FIT = 196608 / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+    static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 256;
+};
+
+__global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int d,
+                                                     __nv_bfloat16* __restrict__ out)
+{
+    const size_t n = (size_t)E_pad * d;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int e = (int)(i / d);
+        const float w = e < E ? Wg[i] : 0.0f;  // Wg is [E, d]: the same flat index for e < E
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);  // exact
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);  // exact
+        out[i] = hi;
+        out[n + i] = mid;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+}
+
+__device__ __forceinline__ bool wait_short(uint64_t* bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > 100000000ull) return false;  // 100 ms
+    return true;
+}
+
+// Each thread of the warp loads 16 consecutive fp32 columns of its TMEM lane.
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kRThreads, 1)
+    k_router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       const RouterGemmArgs a)
+{
+    using C = RCfg<BN>;
+    constexpr uint32_t IDESC = idesc_bf16_f32(kRBM, BN);
+    constexpr int CHUNK = BN < 32 ? BN : 32;  // TMEM columns per epilogue load
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sA = base;
+    uint8_t* sB = base + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * 3 * C::B_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&tfull[q], 1);
+            mbar_init(&tempty[q], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int m_tiles = ceil_div(a.T, kRBM);
+    const int total = m_tiles * a.n_tiles;
+    const int num_kb = ceil_div(a.d, kRBK);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();  // x and W are re-read by other CTAs
+            int stage = 0;
+            uint32_t phase = 0, filled = 0, fill_par = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const int m = tile / a.n_tiles, n = tile - m * a.n_tiles;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    tma_load_2d(sA + stage * C::A_BYTES, &tmX, &full[stage], kb * kRBK, m * kRBM, pol);
+                    uint8_t* dB = sB + stage * 3 * C::B_BYTES;
+#pragma unroll
+                    for (int s = 0; s < 3; ++s)
+                        tma_load_2d(dB + s * C::B_BYTES, &tmW, &full[stage], kb * kRBK,
+                                    s * a.E_pad + n * BN, pol);
+                    filled |= 1u << stage;
+                    fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(a.err, kErrTimeoutProducer);
+                *abort_flag = 1;
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (((filled >> s) & 1u) && !wait_short(&full[s], (fill_par >> s) & 1u))
+                        atomicOr(a.err, kErrTimeoutDrain);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, ci = 0;  // ci counts accumulation chunks over all tiles of this CTA
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kChunkKB, ++ci) {
+                    const int acc = ci & 1;
+                    if (!mbar_wait(&tempty[acc], ((ci >> 1) & 1) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    const int kb1 = kb0 + kChunkKB < num_kb ? kb0 + kChunkKB : num_kb;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+                        const uint32_t b0 = smem_u32(sB + stage * 3 * C::B_BYTES);
+#pragma unroll
+                        for (int s = 2; s >= 0; --s)  // smallest split first
+#pragma unroll
+                            for (int k = 0; k < kRBK / 16; ++k)
+                                mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32),
+                                            sdesc_kmajor_sw128(b0 + s * C::B_BYTES + k * 32), IDESC,
+                                            (kb == kb0 && s == 2 && k == 0) ? 0u : 1u);
+                        mma_commit(&empty[stage]);
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) mma_commit(&tfull[acc]);
+                }
+            }
+            if (!ok) {
+                atomicOr(a.err, kErrTimeoutMma);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);
+            if (!wait_short(drain, 0)) atomicOr(a.err, kErrTimeoutDrain);
+        }
+    } else {
+        const int q = warp & 3;
+        bool ok = true;
+        int ci = 0;
+        const bool vec = (a.E % 4) == 0;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const int m = tile / a.n_tiles, n = tile - m * a.n_tiles;
+            float sum[BN];
+#pragma unroll
+            for (int i = 0; i < BN; ++i) sum[i] = 0.0f;
+            for (int kb0 = 0; kb0 < num_kb; kb0 += kChunkKB, ++ci) {
+                const int acc = ci & 1;
+                if (!mbar_wait(&tfull[acc], (ci >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+                for (int c = 0; c < BN / CHUNK; ++c) {
+                    if constexpr (CHUNK == 32) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(t_lane + c * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(r[i]);
+                    } else {
+                        uint32_t r[16];
+                        tmem_ld_16cols(t_lane + c * 16, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) sum[c * 16 + i] += __uint_as_float(r[i]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            if (!ok) break;
+            const int row = m * kRBM + q * 32 + lane;
+            if (row < a.T) {
+                float* lrow = a.logits + (size_t)row * a.E;
+#pragma unroll
+                for (int i = 0; i < BN; i += 4) {
+                    const int col = n * BN + i;
+                    float o[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        o[u] = sum[i + u] + ((a.bg != nullptr && col + u < a.E) ? a.bg[col + u] : 0.0f);
+                    if (vec && col + 4 <= a.E) {
+                        *reinterpret_cast<float4*>(lrow + col) = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (col + u < a.E) lrow[col + u] = o[u];
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(a.err, kErrTimeoutEpilogue);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a, int sms,
+                      cudaStream_t st)
+{
+    auto kern = k_router_logits_tc<BN>;
+    const size_t smem = RCfg<BN>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int tiles = ceil_div(a.T, kRBM) * a.n_tiles;
+    kern<<<tiles < sms ? tiles : sms, kRThreads, smem, st>>>(x, w, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int router_tc_bn(int E)
+{
+    int bn = 16;
+    while (bn < E && bn < 128) bn *= 2;
+    return bn;
+}
+
+cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms, cudaStream_t st)
+{
+    const size_t n = (size_t)E_pad * d;
+    size_t grid = (n + 255) / 256;
+    if (grid > (size_t)sms * 8) grid = (size_t)sms * 8;
+    k_split_wgate<<<(int)grid, 256, 0, st>>>(Wg, E, E_pad, d, static_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
+                                    int bn, int sms, cudaStream_t st)
+{
+    switch (bn) {
+    case 16: return launch_bn<16>(x, w, a, sms, st);
+    case 32: return launch_bn<32>(x, w, a, sms, st);
+    case 64: return launch_bn<64>(x, w, a, sms, st);
+    default: return launch_bn<128>(x, w, a, sms, st);
+    }
+}
+
+}  // namespace moe

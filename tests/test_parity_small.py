@@ -162,3 +162,21 @@ def test_tcgen05_and_ffma_experts_agree():
     b = run_device(cfg, inp, flags=FFMA)
     ya, yb = a["y"].double(), b["y"].double()
     assert float((ya - yb).norm() / yb.norm()) < 1e-2
+
+
+@pytest.mark.parametrize("name", ["switch_like_k1", "max_experts", "ragged_dims", "many_experts_drops",
+                                  "gelu_erf_k_eq_E"])
+def test_ffma_router_matches_oracle_and_tensor_core_router(name):
+    # bf16 layers compute router logits on the tensor core (three-term bf16 split of
+    # W_gate); the CUDA-core FFMA router is the cross-check.  Both must route
+    # bit-exactly on their own logits and agree with the fp64 oracle.
+    cfg = SMALL[name]
+    inp = _inputs(cfg, random_bias=True)
+    cpu = to_cpu(inp)
+    tc = run_device(cfg, inp)
+    ff = run_device(cfg, inp, flags=_lib.MOE_FLAG_FFMA_ROUTER)
+    for out in (tc, ff):
+        check_routing_bitexact(cfg, out)
+        check_router_vs_fp64(cfg, cpu, out)
+    scale = max(1.0, float(ff["logits"].abs().max()))
+    assert float((tc["logits"] - ff["logits"]).abs().max()) <= 2e-5 * scale
