@@ -131,6 +131,62 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "power_w_max": top}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons via NVML every ~1 ms (a timed region of a
+    few milliseconds is shorter than nvidia-smi's sampling interval)."""
+
+    def __init__(self, index: int):
+        self.index, self.samples, self.ok = index, [], False
+
+    def __enter__(self):
+        import threading
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:  # NVML missing: fall back to nvidia-smi only
+            return self
+        self.stop = threading.Event()
+
+        def loop():
+            while not self.stop.is_set():
+                self._sample()
+                time.sleep(0.001)
+
+        self._sample()  # at least one sample at the start of the region
+        self.th = threading.Thread(target=loop, daemon=True)
+        self.th.start()
+        return self
+
+    def _sample(self):
+        nv, h = self.nv, self.h
+        try:
+            self.samples.append((nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM),
+                                 nv.nvmlDeviceGetCurrentClocksEventReasons(h)))
+        except Exception:
+            pass
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self.stop.set()
+            self.th.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        nv = self.nv
+        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+        reasons = sorted(n for n, bit in names.items() if any(r & bit for _, r in self.samples))
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml 1 ms"}
+
+
 # --------------------------------------------------------------------------- oracle (CPU)
 
 def oracle_step(cfg, cpu_inp, n_sample: int, seed: int = 7):
@@ -296,11 +352,14 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with clk:
+    nvml = NvmlSampler(dev.index)
+    with clk, nvml:
         t_wall0 = time.perf_counter()
         for i in range(K):
             flush.zero_()
             step(evs[i])
+        if nvml.ok:
+            nvml._sample()  # while the last steps are still running on the device
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -425,7 +484,8 @@ def run_gpu(args):
         "cpu_baseline": cpu_base,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
-        "clocks": clk.summary(),
+        "clocks": (nvml.summary() or clk.summary()),
+        "clocks_nvidia_smi": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
