@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch each stage directly instead of replaying a captured CUDA graph")
     return ap.parse_args()
 
 
@@ -345,6 +347,30 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
 
+    if not args.no_graph:
+        # one CUDA graph per stage (the library only enqueues kernels: capturable);
+        # replaying them removes per-launch host overhead, the kernels are unchanged
+        graphs = []
+        for s in stages:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer.run(s)
+            graphs.append(g)
+        torch.cuda.synchronize()
+
+        def step(evs=None):  # noqa: F811
+            for i, g in enumerate(graphs):
+                if evs is not None:
+                    evs[i].record(stream)
+                g.replay()
+            if evs is not None:
+                evs[-1].record(stream)
+
+        for _ in range(2):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     clk = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
@@ -474,6 +500,7 @@ def run_gpu(args):
         "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "direct" if args.no_graph else "CUDA graph per stage",
                    "stage_ms": stage_ms,
                    "memory_stages": mem_stages,
                    "router_dispatch_combine": {"bytes": rdc_bytes, "ms": rdc_ms,

@@ -87,7 +87,7 @@ Layout make_layout(const moe_params_t& p)
     L.t_pad = (p.T + kSegRows - 1) / kSegRows * kSegRows;
     L.esz = (p.dtype == MOE_BF16) ? 2 : 4;
     L.tc_router = p.dtype == MOE_BF16 && !(p.flags & MOE_FLAG_FFMA_ROUTER);
-    L.r_bn = router_tc_bn(p.E);
+    L.r_bn = router_tc_bn(p.T, p.E);
     L.r_tiles = (p.E + L.r_bn - 1) / L.r_bn;
     L.e_pad = L.r_tiles * L.r_bn;
 

@@ -11,6 +11,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 namespace moe {
 
 // Expert segments in the permuted buffers are padded to this many rows: the
@@ -36,6 +40,22 @@ enum : uint32_t {
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s
 
 __host__ __device__ constexpr inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device); later
+// launches (including ones recorded into CUDA graphs) make no attribute call.
+inline cudaError_t ensure_smem_limit(const void* kernel, size_t bytes)
+{
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.insert({kernel, dev});
+    return e;
+}
 __host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
 // ---------------------------------------------------------------------------

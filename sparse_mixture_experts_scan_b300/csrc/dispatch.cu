@@ -16,10 +16,10 @@
 //     the slot's rank inside its chunk;
 //   - the last block to arrive scans the chunk histograms per expert (counts,
 //     chunk bases), the per-expert kept counts over experts (segment offsets,
-//     M-tile offsets for the grouped GEMM), and reduces the router's per-block
-//     probability sums for the balance statistic.
+//     M-tile offsets for the grouped GEMM).
 // k_permute: one warp per slot; position = chunk base + rank; kept rows are
-// copied with 16-byte vector loads/stores.
+// copied with 16-byte vector loads/stores.  Its block 0 also reduces the
+// router's per-block probability sums into the balance statistic.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
 {
     extern __shared__ int32_t sm[];  // [32][E] warp histograms, reused by the last block
     __shared__ int wsum[32][3];
-    __shared__ double dsum[32];
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -144,10 +143,18 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     }
     if (tid == 0) a.mtile_off[E] = tot[2];
 
-    // balance statistic: P_e = mean_t p[t,e] from the router's per-block sums,
-    // reduced in a fixed order (partition p sums blocks p, p+P, ... ascending)
-    float* s_part = reinterpret_cast<float*>(sm);
-    const int P = 1024 / E;
+    if (tid == 0) *a.scan_done = 0u;  // re-arm for the next call
+}
+
+// Switch balance statistic E * sum_e (counts_e / (T k)) * P_e with P_e the mean router
+// probability, from the router's per-block column sums, reduced in a fixed order
+// (partition p sums blocks p, p+P, ... ascending; partitions in order; experts in a
+// fixed tree).  Run by the 256 threads of one block.
+__device__ void balance_statistic(const DispatchArgs& a, float* s_part, double* dsum)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E;
+    const int P = E >= 256 ? 1 : 256 / E;
     if (tid < P * E) {
         const int ee = tid % E, p = tid / E;
         float acc = 0.0f;
@@ -162,25 +169,28 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
         for (; b < a.n_router_blocks; b += P) acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
         s_part[p * E + ee] = acc;
     }
+    // E may exceed the block: the remaining experts are summed by the same threads
+    for (int ee = tid + 256; ee < E && P == 1; ee += 256) {
+        float acc = 0.0f;
+        for (int b = 0; b < a.n_router_blocks; ++b) acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
+        s_part[ee] = acc;
+    }
     __syncthreads();
     double term = 0.0;
-    if (tid < E) {
+    for (int ee = tid; ee < E; ee += 256) {
         float Pe = 0.0f;
-        for (int p = 0; p < P; ++p) Pe += s_part[p * E + tid];
-        term = ((double)my_count / ((double)a.T * (double)a.k)) * ((double)Pe / (double)a.T);
+        for (int p = 0; p < P; ++p) Pe += s_part[p * E + ee];
+        term += ((double)__ldcg(&a.counts[ee]) / ((double)a.T * (double)a.k)) * ((double)Pe / (double)a.T);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
     if (lane == 0) dsum[warp] = term;
     __syncthreads();
     if (warp == 0) {
-        double w = dsum[lane];
+        double w = lane < 8 ? dsum[lane] : 0.0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (lane == 0) {
-            *a.aux = (float)((double)E * w);
-            *a.scan_done = 0u;
-        }
+        if (lane == 0) *a.aux = (float)((double)E * w);
     }
 }
 
@@ -195,6 +205,11 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p)
 
 __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
 {
+    __shared__ float s_part[kMaxExperts > 256 ? kMaxExperts : 256];
+    __shared__ double dsum[8];
+    // block 0 also computes the balance statistic (it needs the scan's counts,
+    // complete at this kernel's start), off the scan's serial tail
+    if (blockIdx.x == 0 && a.aux != nullptr && a.n_router_blocks > 0) balance_statistic(a, s_part, dsum);
     const int lane = threadIdx.x & 31;
     const long long n_slots = (long long)a.T * a.k;
     const int nvec = a.row_bytes / 16;
@@ -236,9 +251,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st)
 {
     const size_t smem = dispatch_scan_smem(a.E);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_dispatch_scan,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_dispatch_scan), smem);
         if (e != cudaSuccess) return e;
     }
     k_dispatch_scan<<<a.nchunks, 1024, smem, st>>>(a);
@@ -255,9 +268,7 @@ cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st)
 {
     const size_t smem = dispatch_scan_smem(a.E);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_dispatch_scan,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_dispatch_scan), smem);
         if (e != cudaSuccess) return e;
     }
     k_dispatch_scan<<<a.nchunks, 1024, smem, st>>>(a);

@@ -335,7 +335,7 @@ cudaError_t launch_tc_t(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 {
     auto kern = k_grouped_gemm_tc<BN, ACT>;
     const size_t smem = TcCfg<BN>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(a, b, b3, args);
     return cudaGetLastError();

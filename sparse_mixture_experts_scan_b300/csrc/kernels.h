@@ -38,7 +38,7 @@ struct RouterGemmArgs {
     float* logits;        // [T, E] fp32
     uint32_t* err;
 };
-int router_tc_bn(int E);  // MMA N of the router GEMM for E experts (16..128)
+int router_tc_bn(int T, int E);  // MMA N of the router GEMM (16..128), ~128 CTAs
 cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms,
                                cudaStream_t st);
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,

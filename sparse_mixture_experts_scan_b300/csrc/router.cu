@@ -203,17 +203,22 @@ __global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
     float psum[EJ];
 #pragma unroll
     for (int j = 0; j < EJ; ++j) psum[j] = 0.0f;
+    // all loads of the warp's tokens first, then the dependent shuffle chains
+    float l[kTokPerWarp][EJ];
+#pragma unroll
+    for (int i = 0; i < kTokPerWarp; ++i) {
+        const int t = t0 + warp * kTokPerWarp + i;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            l[i][j] = (t < a.T && e < a.E) ? a.logits[(size_t)t * a.E + e] : -INFINITY;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < kTokPerWarp; ++i) {
         const int t = t0 + warp * kTokPerWarp + i;
         if (t >= a.T) break;  // warp-uniform
-        float l[EJ];
-#pragma unroll
-        for (int j = 0; j < EJ; ++j) {
-            const int e = lane + 32 * j;
-            l[j] = (e < a.E) ? a.logits[(size_t)t * a.E + e] : -INFINITY;
-        }
-        route_token<EJ>(l, t, a, false, psum);
+        route_token<EJ>(l[i], t, a, false, psum);
     }
     block_psum<EJ>(psum, scratch, a);
 }

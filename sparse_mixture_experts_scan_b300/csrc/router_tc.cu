@@ -296,7 +296,7 @@ cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGe
 {
     auto kern = k_router_logits_tc<BN>;
     const size_t smem = RCfg<BN>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int tiles = ceil_div(a.T, kRBM) * a.n_tiles;
     kern<<<tiles < sms ? tiles : sms, kRThreads, smem, st>>>(x, w, a);
@@ -305,10 +305,14 @@ cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGe
 
 }  // namespace
 
-int router_tc_bn(int E)
+int router_tc_bn(int T, int E)
 {
+    // Aim for about 128 CTAs (m-tiles x expert tiles), BN a power of two in [16, 128].
+    const int m_tiles = ceil_div(T, kRBM);
+    const int want_tiles = ceil_div(128, m_tiles);
+    const int per_tile = ceil_div(E, want_tiles);
     int bn = 16;
-    while (bn < E && bn < 128) bn *= 2;
+    while (bn < per_tile && bn < 128) bn *= 2;
     return bn;
 }
 
