@@ -134,22 +134,35 @@ class ClockSampler:
 
 
 class NvmlSampler:
-    """SM clock and clock-event reasons via NVML every ~1 ms (a timed region of a
-    few milliseconds is shorter than nvidia-smi's sampling interval)."""
+    """SM clock and clock-event reasons from the driver's NVML library (the library
+    nvidia-smi reads) every ~1 ms: a timed region of a few milliseconds is shorter
+    than nvidia-smi's sampling interval.  Loaded with ctypes (no Python binding needed)."""
+
+    CLOCK_SM = 1
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
 
     def __init__(self, index: int):
-        self.index, self.samples, self.ok = index, [], False
+        self.index, self.samples, self.ok, self.error = index, [], False, None
 
     def __enter__(self):
+        import ctypes
         import threading
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise OSError("nvmlDeviceGetHandleByIndex_v2 failed")
+            self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(self.CLOCK_SM), ctypes.byref(mx))
+            self.lib, self.h, self.max_mhz, self.ct = lib, h, mx.value, ctypes
             self.ok = True
-        except Exception:  # NVML missing: fall back to nvidia-smi only
+        except (OSError, AttributeError) as exc:
+            self.error = str(exc)
             return self
         self.stop = threading.Event()
 
@@ -164,12 +177,11 @@ class NvmlSampler:
         return self
 
     def _sample(self):
-        nv, h = self.nv, self.h
-        try:
-            self.samples.append((nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM),
-                                 nv.nvmlDeviceGetCurrentClocksEventReasons(h)))
-        except Exception:
-            pass
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, ct.c_int(self.CLOCK_SM), ct.byref(clk)) == 0 and \
+                self.get_reasons(self.h, ct.byref(rs)) == 0:
+            self.samples.append((clk.value, rs.value))
 
     def __exit__(self, *exc):
         if self.ok:
@@ -179,14 +191,9 @@ class NvmlSampler:
     def summary(self):
         if not self.ok or not self.samples:
             return None
-        nv = self.nv
-        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
-        reasons = sorted(n for n, bit in names.items() if any(r & bit for _, r in self.samples))
+        reasons = sorted(n for n, bit in self.REASONS.items() if any(r & bit for _, r in self.samples))
         return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(self.samples), "source": "nvml 1 ms"}
+                "reasons": reasons, "samples": len(self.samples), "source": "NVML every ~1 ms"}
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -439,31 +446,52 @@ def run_gpu(args):
     cap_zero = cfg.cf is not None and int(cfg.T * cfg.cf / cfg.E) == 0
     launches_per_step = 1 + 2 + (0 if cap_zero else 2) + (2 if cfg.S else 0) + 1
 
-    # ---- end to end: host x -> device, layer, y + aux -> host, every step
+    # ---- end to end through the public API with host buffers: every step copies its x
+    # from pinned host memory to the device, runs the layer, and copies y and aux back.
+    # Steps are pipelined over three streams (copy in / compute / copy out) with two
+    # layer instances, so step i+1's upload and step i-1's download overlap step i.
     e2e = None
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
-        y_host = torch.empty_like(out["y"], device="cpu").pin_memory()
-        aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
-        x_dev = torch.empty_like(inp["x"])
-        layer.set_x(x_dev)
-        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        for _ in range(max(args.warmup, 1)):
-            x_dev.copy_(x_host, non_blocking=True)
-            layer.run()
-            y_host.copy_(out["y"], non_blocking=True)
+        layers = [layer, MoELayer(cfg, dict(inp), device=dev)]
+        x_dev = [torch.empty_like(inp["x"]) for _ in layers]
+        for L, xd in zip(layers, x_dev):
+            L.set_x(xd)
+        y_host = [torch.empty_like(out["y"], device="cpu").pin_memory() for _ in range(K)]
+        aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(K)]
+        s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+        def run_e2e(nsteps, t0=None, t1=None):
+            up, comp, down = [None] * nsteps, [None] * nsteps, [None] * nsteps
+            if t0 is not None:
+                t0.record(s_in)
+            for i in range(nsteps):
+                b = i % 2
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(comp[i - 2])  # x buffer b is free again
+                    x_dev[b].copy_(x_host, non_blocking=True)
+                    up[i] = ev(); up[i].record(s_in)
+                with torch.cuda.stream(s_run):
+                    s_run.wait_event(up[i])
+                    if i >= 2:
+                        s_run.wait_event(down[i - 2])  # outputs of buffer b downloaded
+                    layers[b].run("moe_forward", s_run)
+                    comp[i] = ev(); comp[i].record(s_run)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp[i])
+                    y_host[i % K].copy_(layers[b].out["y"], non_blocking=True)
+                    aux_host[i % K].copy_(layers[b].out["aux"], non_blocking=True)
+                    down[i] = ev(); down[i].record(s_out)
+            if t1 is not None:
+                s_out.wait_event(down[nsteps - 1])
+                t1.record(s_out)
+        run_e2e(max(args.warmup, 2))
         torch.cuda.synchronize()
-        for i in range(K):
-            flush.zero_()
-            e_s[i].record(stream)
-            x_dev.copy_(x_host, non_blocking=True)
-            layer.run("moe_forward", stream)
-            y_host.copy_(out["y"], non_blocking=True)
-            aux_host.copy_(out["aux"], non_blocking=True)
-            e_e[i].record(stream)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        run_e2e(K, t0, t1)
         torch.cuda.synchronize()
-        e_ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K)) / K
+        e_ms = t0.elapsed_time(t1) / K
         if world > 1:
             t = torch.tensor([e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -471,8 +499,11 @@ def run_gpu(args):
         esz = x_host.element_size()
         e2e = {"value": world * cfg.T / (e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": x_host.numel() * esz,
-               "d2h_bytes_per_step": y_host.numel() * y_host.element_size() + 4,
-               "ms_per_step": e_ms}
+               "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size() + 4,
+               "ms_per_step": e_ms,
+               "method": "moe_forward per step on pinned host buffers; upload, compute and "
+                         "download of consecutive steps overlap on three streams"}
+        layer = layers[0]
 
     status = layer.device_status()
     if status != 0:

@@ -67,6 +67,9 @@ typedef enum {
 #define MOE_FLAG_FFMA_ROUTER 2u  /* compute bf16 router logits with CUDA-core FFMA
                                     (cross-check kernel) instead of the tensor-core
                                     three-term split; fp32 layers always use FFMA */
+#define MOE_FLAG_UNFUSED_EXPERTS 4u /* run the routed experts' two layers as two
+                                       grouped-GEMM launches instead of one fused
+                                       persistent launch (cross-check path) */
 
 /* Limits of this build. */
 #define MOE_MAX_EXPERTS 512 /* E (routed) */

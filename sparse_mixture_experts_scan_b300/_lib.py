@@ -25,6 +25,7 @@ MOE_ACT_RELU, MOE_ACT_GELU_TANH, MOE_ACT_GELU_ERF, MOE_ACT_SWIGLU = 0, 1, 2, 3
 MOE_F32, MOE_BF16 = 0, 1
 MOE_FLAG_FFMA_EXPERTS = 1
 MOE_FLAG_FFMA_ROUTER = 2
+MOE_FLAG_UNFUSED_EXPERTS = 4
 MOE_MAX_EXPERTS = 512
 MOE_MAX_TOPK = 32
 MOE_NOALLOC_MAX_SLOTS = 131072

@@ -30,6 +30,8 @@ struct Layout {
     bool tc_router;    // bf16 router logits on the tensor core
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
     size_t off_wsplit, off_logits;
+    size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
+    int ffn_sync_n;
     size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
         off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys, total;
 };
@@ -54,7 +56,8 @@ moe_status_t validate_params(const moe_params_t* p)
     if (p->residual_mode != 0 && p->residual_mode != 1) return MOE_ERR_INVALID_ARG;
     if (p->act < MOE_ACT_RELU || p->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-    if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER)) != 0u) return MOE_ERR_INVALID_ARG;
+    if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER | MOE_FLAG_UNFUSED_EXPERTS)) != 0u)
+        return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     // every index and row count below must fit in int32
@@ -99,6 +102,8 @@ Layout make_layout(const moe_params_t& p)
     };
     L.off_wsplit = take(L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
     L.off_logits = take(sizeof(float) * (size_t)L.T * L.E);
+    L.ffn_sync_n = 2 + L.rows_cap / kSegRows;
+    L.off_ffn_sync = take(sizeof(unsigned) * L.ffn_sync_n);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
     L.off_hist = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
     L.off_base = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
@@ -191,7 +196,7 @@ struct Ctx {
     Layout L;
     cudaStream_t st;
     int sms;
-    bool bf16, use_tc;
+    bool bf16, use_tc, fused;
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW;
     template <typename T>
@@ -221,6 +226,7 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.sms <= 0) return MOE_ERR_CUDA;
     c.bf16 = c.p.dtype == MOE_BF16;
     c.use_tc = c.bf16 && !(c.p.flags & MOE_FLAG_FFMA_EXPERTS);
+    c.fused = c.use_tc && !(c.p.flags & MOE_FLAG_UNFUSED_EXPERTS);
     if (c.L.tc_router) {
         const Layout& L = c.L;
         if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) ||
@@ -230,8 +236,8 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.use_tc) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
-        c.bn1 = gated ? 256 : pick_bn(L.F);
-        c.bn2 = pick_bn(L.d);
+        c.bn1 = c.fused || gated ? 256 : pick_bn(L.F);
+        c.bn2 = c.fused ? 256 : pick_bn(L.d);
         const int b1_rows = gated ? c.bn1 / 2 : c.bn1;
         const uint64_t ES = (uint64_t)(L.E + L.S);
         bool ok = encode_bf16_2d(&c.mB1, in->W1, ES * L.F, L.d, b1_rows) &&
@@ -313,6 +319,8 @@ moe_status_t stage_dispatch(Ctx& c)
     a.dropped = c.out->dropped;
     a.perm_row = c.out->perm_row;
     a.slot_row = c.at<int32_t>(c.L.off_slot_row);
+    a.ffn_sync = c.at<unsigned>(c.L.off_ffn_sync);
+    a.ffn_sync_n = c.L.ffn_sync_n;
     return cuda_status(launch_dispatch(a, c.sms, c.st));
 }
 
@@ -376,7 +384,35 @@ moe_status_t stage_gemm(Ctx& c)
         const int out1 = gated ? c.bn1 / 2 : c.bn1;
         g1.n_tiles = ceil_div(L.F, out1);
         g2.n_tiles = ceil_div(L.d, c.bn2);
-        if (mt_routed > 0) {
+        if (mt_routed > 0 && c.fused) {
+            FusedFfnArgs f{};
+            f.mtile_off = g1.mtile_off;
+            f.row_off = g1.row_off;
+            f.rows = g1.rows;
+            f.G = L.E;
+            f.N1 = L.F;
+            f.n_tiles1 = g1.n_tiles;
+            f.K1 = L.d;
+            f.N2 = L.d;
+            f.n_tiles2 = g2.n_tiles;
+            f.K2 = L.F;
+            f.b1_rows_per_group = L.F;
+            f.b2_rows_per_group = L.d;
+            f.h = g1.out;
+            f.ldh = L.F;
+            f.yp = g2.out;
+            f.ldy = L.d;
+            f.bias1 = c.in->b1;
+            f.bias2 = c.in->b2;
+            unsigned* sync = c.at<unsigned>(L.off_ffn_sync);
+            f.tile_ctr = sync;
+            f.ctas_done = sync + 1;
+            f.mt_done = sync + 2;
+            f.mt_max = L.ffn_sync_n - 2;
+            f.err = c.err();
+            const CUtensorMap maps[5] = {c.mA1, c.mB1, c.mB3, c.mA2, c.mB2};
+            e = launch_ffn_fused_tc(maps, f, act1, grid_for(mt_routed * (g1.n_tiles + g2.n_tiles), 1), c.st);
+        } else if (mt_routed > 0) {
             e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st);
             if (e == cudaSuccess)
                 e = launch_gemm_tc(c.mA2, c.mB2, c.mB2, g2, kActNone, c.bn2, grid_for(mt_routed * g2.n_tiles, 1),

@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     }
     if (tid == 0) a.mtile_off[E] = tot[2];
 
+    // the fused expert kernel that follows starts from zeroed scheduler counters
+    if (a.ffn_sync != nullptr)
+        for (int i = tid; i < a.ffn_sync_n; i += 1024) a.ffn_sync[i] = 0u;
     if (tid == 0) *a.scan_done = 0u;  // re-arm for the next call
 }
 

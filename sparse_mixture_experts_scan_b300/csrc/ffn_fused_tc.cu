@@ -1,0 +1,389 @@
+// ffn_fused_tc.cu -- both linear layers of the routed experts in one persistent
+// tcgen05 launch.
+//
+// Expert FFN ("混合专家模型MoE入门实战" §3.2): H = act(Xp W1^T (+b1)) or SwiGLU, then
+// Yp = H W2^T (+b2).  Running the two layers as two grouped-GEMM launches leaves
+// SMs idle in the tail of each launch (the second layer of a Switch-sized layer
+// has only 2.6 tiles per SM) and at the launch boundary.  Here the GEMM1 tiles and
+// then the GEMM2 tiles of all experts form one tile list that CTAs claim
+// dynamically (an atomic counter), so the tail of GEMM1 overlaps the start of
+// GEMM2 and every SM stays busy until the last tile.
+//
+// Dependencies: a GEMM2 tile reads the H rows of one M-tile, written by the
+// n_tiles1 GEMM1 tiles of that M-tile (possibly on other SMs).  After storing its
+// rows of a GEMM1 tile, each of the 4 epilogue warps fences (generic -> async
+// proxy, then GPU scope) and adds 1 to mt_done[M-tile] with release semantics;
+// the producer of a GEMM2 tile waits (bounded) until mt_done reaches
+// 4 * n_tiles1 with acquire loads, then fences the async proxy before its TMA
+// loads of H.  Tiles are
+// claimed in increasing order and GEMM1 tiles never wait, so every GEMM1 tile a
+// GEMM2 tile depends on was claimed earlier by a CTA that will finish it: no
+// deadlock, whatever the residency.
+//
+// Tile ids travel from the producer (which claims them) to the MMA issuer and the
+// epilogue through a 4-entry shared-memory ring guarded by mbarriers.  The last
+// CTA to finish resets the scheduler counters for the next launch.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_tile.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kRing = 4;
+
+template <int BN>
+struct FCfg {
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr size_t BAR_BYTES = 512;
+    static constexpr size_t TABLE_BYTES = sizeof(int) * (3 * kMaxExperts + 1);
+    static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + BAR_BYTES + TABLE_BYTES;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *p >= target (acquire), bounded like every wait of the kernel.
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, volatile int* abort)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        __nanosleep(64);
+    }
+}
+
+template <int BN, int ACT1>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_ffn_fused_tc(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB2, const FusedFfnArgs args)
+{
+    using C = FCfg<BN>;
+    constexpr bool GATED = (ACT1 == kActSwiglu);
+    constexpr int OUT1 = GATED ? BN / 2 : BN;  // GEMM1 output columns per tile
+    constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sA = base;
+    uint8_t* sB = base + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint64_t* ring_full = drain + 1;
+    uint64_t* ring_empty = ring_full + kRing;
+    volatile int* ring = reinterpret_cast<volatile int*>(ring_empty + kRing);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kRing);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_mt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + C::BAR_BYTES);
+    int* s_roff = s_mt + kMaxExperts + 1;
+    int* s_rows = s_roff + kMaxExperts;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = args.G;
+    for (int i = threadIdx.x; i <= G; i += kThreads) s_mt[i] = args.mtile_off[i];
+    for (int i = threadIdx.x; i < G; i += kThreads) {
+        s_roff[i] = args.row_off[i];
+        s_rows[i] = args.rows[i];
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&tfull[q], 1);
+            mbar_init(&tempty[q], 4);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(&ring_full[r], 1);
+            mbar_init(&ring_empty[r], 5);  // the MMA thread + the 4 epilogue warps
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB1);
+        if (GATED) tma_prefetch_desc(&tmB3);
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total1 = s_mt[G] * args.n_tiles1;
+    const int total = total1 + s_mt[G] * args.n_tiles2;
+    const int nkb1 = ceil_div(args.K1, kBK);
+    const int nkb2 = ceil_div(args.K2, kBK);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_act = policy_evict_last();
+            const uint64_t pol_w = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, filled = 0, fill_par = 0;
+            bool ok = true;
+            TileMap tm1, tm2;
+            for (int j = 0; ok; ++j) {
+                const int slot = j % kRing;
+                if (!mbar_wait(&ring_empty[slot], ((j / kRing) & 1) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                int t = (int)atomicAdd(args.tile_ctr, 1u);
+                if (t >= total) t = -1;
+                ring[slot] = t;
+                mbar_arrive(&ring_full[slot]);
+                if (t < 0) break;
+                int m, n;
+                const bool second = t >= total1;
+                int g;
+                if (second) {
+                    tm2.locate(t - total1, s_mt, args.n_tiles2, m, n);
+                    g = tm2.g;
+                    // H rows of this M-tile must be complete (all n_tiles1 GEMM1 tiles)
+                    if (!wait_counter(&args.mt_done[s_mt[g] + m], 4u * (unsigned)args.n_tiles1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                } else {
+                    tm1.locate(t, s_mt, args.n_tiles1, m, n);
+                    g = tm1.g;
+                }
+                const int a_row = s_roff[g] + m * kBM;
+                const int b_row = second ? g * args.b2_rows_per_group + n * BN
+                                         : g * args.b1_rows_per_group + n * OUT1;
+                const int nkb = second ? nkb2 : nkb1;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    uint8_t* dA = sA + stage * C::A_BYTES;
+                    uint8_t* dB = sB + stage * C::B_BYTES;
+                    // each TMA names its kernel-parameter tensor map directly
+                    if (second) {
+                        tma_load_2d(dA, &tmA2, &full[stage], kb * kBK, a_row, pol_act);
+                        tma_load_2d(dB, &tmB2, &full[stage], kb * kBK, b_row, pol_w);
+                    } else if (GATED) {
+                        tma_load_2d(dA, &tmA1, &full[stage], kb * kBK, a_row, pol_act);
+                        tma_load_2d(dB, &tmB1, &full[stage], kb * kBK, b_row, pol_w);
+                        tma_load_2d(dB + C::B_BYTES / 2, &tmB3, &full[stage], kb * kBK, b_row, pol_w);
+                    } else {
+                        tma_load_2d(dA, &tmA1, &full[stage], kb * kBK, a_row, pol_act);
+                        tma_load_2d(dB, &tmB1, &full[stage], kb * kBK, b_row, pol_w);
+                    }
+                    filled |= 1u << stage;
+                    fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(args.err, kErrTimeoutProducer);
+                *abort_flag = 1;
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (((filled >> s) & 1u) && !mbar_wait_short(&full[s], (fill_par >> s) & 1u))
+                        atomicOr(args.err, kErrTimeoutDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                const int slot = j % kRing;
+                if (!mbar_wait(&ring_full[slot], (j / kRing) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int t = ring[slot];
+                if (t < 0) break;
+                const int nkb = t >= total1 ? nkb2 : nkb1;
+                const int acc = it & 1;
+                if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32),
+                                    IDESC, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                mbar_arrive(&ring_empty[slot]);
+                ++it;
+            }
+            if (!ok) {
+                atomicOr(args.err, kErrTimeoutMma);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);
+            if (!mbar_wait_short(drain, 0)) atomicOr(args.err, kErrTimeoutDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        const __nv_bfloat16* bias1 = static_cast<const __nv_bfloat16*>(args.bias1);
+        const __nv_bfloat16* bias2 = static_cast<const __nv_bfloat16*>(args.bias2);
+        bool ok = true;
+        int it = 0;
+        TileMap tm1, tm2;
+        for (int j = 0; ok; ++j) {
+            const int slot = j % kRing;
+            if (!mbar_wait(&ring_full[slot], (j / kRing) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const int t = ring[slot];
+            if (t < 0) break;
+            const bool second = t >= total1;
+            int m, n, g;
+            if (second) {
+                tm2.locate(t - total1, s_mt, args.n_tiles2, m, n);
+                g = tm2.g;
+            } else {
+                tm1.locate(t, s_mt, args.n_tiles1, m, n);
+                g = tm1.g;
+            }
+            const int acc = it & 1;
+            if (!mbar_wait(&tfull[acc], (it >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const int row = m * kBM + r_in_tile;
+            const bool row_ok = row < s_rows[g];
+            const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            if (second) {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.yp) + (size_t)(s_roff[g] + row) * args.ldy;
+                epilogue_tile<BN, kActNone>(t_lane, orow, row_ok, n * BN, args.N2, bias2,
+                                            (size_t)g * args.b2_rows_per_group, 1, args.b2_rows_per_group);
+            } else {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.h) + (size_t)(s_roff[g] + row) * args.ldh;
+                epilogue_tile<BN, ACT1>(t_lane, orow, row_ok, n * OUT1, args.N1, bias1,
+                                        (size_t)g * args.b1_rows_per_group, 1, args.b1_rows_per_group);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (!second) {
+                // publish this warp's 32 H rows to the GEMM2 tiles that read them: each
+                // of the 4 epilogue warps adds 1, so an M-tile is complete at 4 * n_tiles1
+                fence_proxy_async_global();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) red_release_gpu_add(&args.mt_done[s_mt[g] + m], 1u);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ring_empty[slot]);
+            ++it;
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(args.err, kErrTimeoutEpilogue);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (threadIdx.x == 0) {
+        // the last CTA to finish re-arms the scheduler for the next launch
+        __threadfence();
+        if (atomicAdd(args.ctas_done, 1u) == gridDim.x - 1) {
+            __threadfence();
+            for (int i = 0; i < args.mt_max; ++i) args.mt_done[i] = 0u;
+            *args.tile_ctr = 0u;
+            __threadfence();
+            *args.ctas_done = 0u;
+        }
+    }
+}
+
+template <int BN, int ACT1>
+cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st)
+{
+    auto kern = k_ffn_fused_tc<BN, ACT1>;
+    const size_t smem = FCfg<BN>::SMEM;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
+                                cudaStream_t st)
+{
+    switch (act1) {
+    case kActRelu: return launch_t<256, kActRelu>(maps, a, grid, st);
+    case kActGeluTanh: return launch_t<256, kActGeluTanh>(maps, a, grid, st);
+    case kActGeluErf: return launch_t<256, kActGeluErf>(maps, a, grid, st);
+    default: return launch_t<256, kActSwiglu>(maps, a, grid, st);
+    }
+}
+
+}  // namespace moe

@@ -22,6 +22,7 @@
 // error bit, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_tile.cuh"
 
 namespace moe {
 
@@ -42,46 +43,6 @@ struct TcCfg {
     static constexpr size_t TABLE_BYTES = sizeof(int) * (3 * kMaxExperts + 1);
     static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + BAR_BYTES + TABLE_BYTES;
 };
-
-struct TileMap {
-    int g = 0;
-    // Advance to the group holding `tile` (tiles are visited in increasing order).
-    __device__ __forceinline__ void locate(int tile, const int* mt, int n_tiles, int& m, int& n)
-    {
-        while (tile >= mt[g + 1] * n_tiles) ++g;
-        const int local = tile - mt[g] * n_tiles;
-        const int mtg = mt[g + 1] - mt[g];
-        n = local / mtg;  // M fastest: consecutive tiles share the B (weight) tile
-        m = local - n * mtg;
-    }
-};
-
-// Round 32 consecutive outputs of one row to bf16 and store the 16-byte groups
-// that lie inside the N valid columns (N is a multiple of 8).
-__device__ __forceinline__ void store_row32(__nv_bfloat16* orow, int col0, int N, const float (&o)[32])
-{
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        const int col = col0 + v * 8;
-        if (col + 8 <= N) {
-            uint4 u;
-            u.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
-            u.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
-            u.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
-            u.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
-            *reinterpret_cast<uint4*>(orow + col) = u;
-        }
-    }
-}
-
-// Bounded wait used only while draining after an abort.
-__device__ __forceinline__ bool mbar_wait_short(uint64_t* bar, uint32_t parity)
-{
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > 100000000ull) return false;  // 100 ms
-    return true;
-}
 
 template <int BN, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -267,52 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = row < s_rows[tm.g];
             __nv_bfloat16* orow = out + (size_t)(s_roff[tm.g] + row) * args.ldo;
             const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const int n0 = n * OUT_COLS;
-            if constexpr (GATED) {
-                // accumulator columns [0, BN/2) hold x.W1^T, [BN/2, BN) hold x.W3^T
-#pragma unroll 1
-                for (int c = 0; c < OUT_COLS / 32; ++c) {
-                    uint32_t va[32], vb[32];
-                    tmem_ld_32cols(t_lane + c * 32, va);
-                    tmem_ld_32cols(t_lane + BN / 2 + c * 32, vb);
-                    tmem_ld_wait();
-                    float o[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = activate_bf16out<kActSwiglu>(__uint_as_float(va[i])) * __uint_as_float(vb[i]);
-                    if (row_ok) store_row32(orow, n0 + c * 32, args.N, o);
-                }
-            } else if (bias == nullptr) {
-#pragma unroll 1
-                for (int c = 0; c < OUT_COLS / 32; ++c) {
-                    uint32_t va[32];
-                    tmem_ld_32cols(t_lane + c * 32, va);
-                    tmem_ld_wait();
-                    float o[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = activate_bf16out<ACT>(__uint_as_float(va[i]));
-                    if (row_ok) store_row32(orow, n0 + c * 32, args.N, o);
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < OUT_COLS / 32; ++c) {
-                    uint32_t va[32];
-                    tmem_ld_32cols(t_lane + c * 32, va);
-                    tmem_ld_wait();
-                    float o[32];
-#pragma unroll 4
-                    for (int i = 0; i < 32; ++i) {
-                        float z = __uint_as_float(va[i]);
-                        const int col = n0 + c * 32 + i;
-                        if (col < args.N)
-                            for (int sg = 0; sg < args.k_segments; ++sg)
-                                z += __bfloat162float(
-                                    bias[(size_t)(args.b_group0 + tm.g + sg) * args.b_rows_per_group + col]);
-                        o[i] = activate_bf16out<ACT>(z);
-                    }
-                    if (row_ok) store_row32(orow, n0 + c * 32, args.N, o);
-                }
-            }
+            epilogue_tile<BN, ACT>(t_lane, orow, row_ok, n * OUT_COLS, args.N, bias,
+                                   (size_t)(args.b_group0 + tm.g) * args.b_rows_per_group, args.k_segments,
+                                   args.b_rows_per_group);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);

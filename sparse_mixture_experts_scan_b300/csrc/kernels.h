@@ -70,6 +70,8 @@ struct DispatchArgs {
     uint8_t* dropped;     // [T, k]
     int32_t* perm_row;    // [T, k] or nullptr
     int32_t* slot_row;    // [T, k] padded row of the slot or -1
+    unsigned* ffn_sync;   // fused-FFN scheduler words cleared by the scan, or nullptr
+    int ffn_sync_n;
 };
 size_t dispatch_scan_smem(int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st);
@@ -83,6 +85,33 @@ cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& b, const CUt
                            const GroupedGemmArgs& args, int act, int bn, int grid,
                            cudaStream_t st);
 size_t gemm_tc_smem(int bn);
+// Both expert layers of the routed experts in one persistent launch (dynamic tile
+// scheduler, GEMM2 tiles wait for the GEMM1 tiles of their M-tile).
+struct FusedFfnArgs {
+    const int* mtile_off;  // [G+1]
+    const int* row_off;    // [G]
+    const int* rows;       // [G]
+    int G;
+    int N1, n_tiles1, K1;  // GEMM1: output columns (d_ff), tiles, reduction (d_model)
+    int N2, n_tiles2, K2;  // GEMM2: output columns (d_model), tiles, reduction (d_ff)
+    int b1_rows_per_group; // d_ff
+    int b2_rows_per_group; // d_model
+    void* h;
+    int ldh;
+    void* yp;
+    int ldy;
+    const void* bias1;
+    const void* bias2;
+    unsigned* tile_ctr;    // tiles claimed so far (0 at launch)
+    unsigned* ctas_done;   // CTAs finished (0 at launch)
+    unsigned* mt_done;     // [mt_max] epilogue-warp arrivals per M-tile (0 at launch)
+    int mt_max;
+    uint32_t* err;
+};
+// maps: A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2); MMA N = 256.
+cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
+                                cudaStream_t st);
+
 // FFMA kernel over fp32 or bf16 operands (A [a_rows_alloc, lda], B [*, ldb]).
 cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
                              const GroupedGemmArgs& args, int act, bool bf16, int grid,
