@@ -341,32 +341,42 @@ def run_gpu(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
 
-    def step(evs=None):
-        for i, s in enumerate(stages):
+    def stage_step(evs=None):
+        for i, st_name in enumerate(stages):
             if evs is not None:
                 evs[i].record(stream)
-            layer.run(s, stream)
+            layer.run(st_name, stream)
         if evs is not None:
             evs[-1].record(stream)
 
+    def full_step():
+        layer.run("moe_forward", stream)
+
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
-        step()
+        full_step()
     torch.cuda.synchronize()
 
     if not args.no_graph:
-        # one CUDA graph per stage (the library only enqueues kernels: capturable);
-        # replaying them removes per-launch host overhead, the kernels are unchanged
-        graphs = []
-        for s in stages:
+        # CUDA graphs of the library's calls (it only enqueues kernels, so it is
+        # capturable): one of the whole forward (kernels chained by programmatic
+        # dependent launch) and one per stage for the stage breakdown
+        g_full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_full):
+            layer.run("moe_forward")
+        g_stage = []
+        for st_name in stages:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                layer.run(s)
-            graphs.append(g)
+                layer.run(st_name)
+            g_stage.append(g)
         torch.cuda.synchronize()
 
-        def step(evs=None):  # noqa: F811
-            for i, g in enumerate(graphs):
+        def full_step():  # noqa: F811
+            g_full.replay()
+
+        def stage_step(evs=None):  # noqa: F811
+            for i, g in enumerate(g_stage):
                 if evs is not None:
                     evs[i].record(stream)
                 g.replay()
@@ -375,36 +385,44 @@ def run_gpu(args):
 
         for _ in range(2):
             flush.zero_()
-            step()
+            full_step()
+            stage_step()
         torch.cuda.synchronize()
 
     K = args.steps
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     clk = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    nvml = NvmlSampler(dev.index)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    nvml = NvmlSampler(dev.index)
     with clk, nvml:
         t_wall0 = time.perf_counter()
+        # timed region: K whole-layer steps, events only at step boundaries
         for i in range(K):
             flush.zero_()
-            step(evs[i])
+            ev_step[i][0].record(stream)
+            full_step()
+            ev_step[i][1].record(stream)
         if nvml.ok:
             nvml._sample()  # while the last steps are still running on the device
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall0
-    stage_ms = {s: 0.0 for s in stages}
-    total_ms = 0.0
+        # second timed pass: the same K steps with events between the four stages
+        for i in range(K):
+            flush.zero_()
+            stage_step(evs[i])
+        torch.cuda.synchronize()
+    stage_ms = {st_name: 0.0 for st_name in stages}
     for i in range(K):
-        for j, s in enumerate(stages):
-            stage_ms[s] += evs[i][j].elapsed_time(evs[i][j + 1])
-        total_ms += evs[i][0].elapsed_time(evs[i][-1])
-    stage_ms = {s: v / K for s, v in stage_ms.items()}
-    ms_step = total_ms / K
+        for j, st_name in enumerate(stages):
+            stage_ms[st_name] += evs[i][j].elapsed_time(evs[i][j + 1])
+    stage_ms = {k_: v / K for k_, v in stage_ms.items()}
+    ms_step = sum(a.elapsed_time(b) for a, b in ev_step) / K
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -416,8 +434,13 @@ def run_gpu(args):
     sbytes = stage_bytes(cfg, out, gemm)
     pk = peaks()
     g_ms = stage_ms["moe_grouped_gemm"]
-    hbm_bound = gemm["flops"] / gemm["bytes"] < pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if hbm_bound:
+    hbm_bound = gemm["bytes"] == 0 or \
+        gemm["flops"] / gemm["bytes"] < pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if gemm["bytes"] == 0 or g_ms <= 0:
+        # capacity 0: every slot is dropped, the expert stage has no work
+        roof = {"bound": "hbm", "achieved": 0.0, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": 0.0,
+                "note": "no kept rows: the expert stage does no work"}
+    elif hbm_bound:
         achieved = gemm["bytes"] / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"]}
@@ -431,10 +454,10 @@ def run_gpu(args):
                  "algorithmic_bytes": gemm["bytes"], "algorithmic_flops": gemm["flops"],
                  "touched_experts": gemm["touched_experts"], "kept_rows": gemm["kept_rows"],
                  "peak_source": pk["source"] + " (burst)",
-                 "tensor_tflops": gemm["flops"] / (g_ms * 1e-3) / 1e12,
-                 "tensor_frac": gemm["flops"] / (g_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
-                 "hbm_gbs": gemm["bytes"] / (g_ms * 1e-3) / 1e9,
-                 "hbm_frac": gemm["bytes"] / (g_ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+                 "tensor_tflops": gemm["flops"] / max(g_ms * 1e-3, 1e-12) / 1e12,
+                 "tensor_frac": gemm["flops"] / max(g_ms * 1e-3, 1e-12) / 1e12 / pk["bf16_tflops"],
+                 "hbm_gbs": gemm["bytes"] / max(g_ms * 1e-3, 1e-12) / 1e9,
+                 "hbm_frac": gemm["bytes"] / max(g_ms * 1e-3, 1e-12) / 1e9 / pk["hbm_gbs"]})
     mem_stages = {}
     for s in ("moe_router", "moe_dispatch", "moe_combine"):
         gbs = sbytes[s] / (stage_ms[s] * 1e-3) / 1e9
@@ -454,9 +477,18 @@ def run_gpu(args):
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
         layers = [layer, MoELayer(cfg, dict(inp), device=dev)]
-        x_dev = [torch.empty_like(inp["x"]) for _ in layers]
+        x_dev = [inp["x"].clone() for _ in layers]  # valid data before the first forward
         for L, xd in zip(layers, x_dev):
             L.set_x(xd)
+        fwd = [(lambda L=L: L.run("moe_forward")) for L in layers]
+        if not args.no_graph:
+            for b_, L in enumerate(layers):
+                L.run("moe_forward")
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    L.run("moe_forward")
+                fwd[b_] = g.replay
         y_host = [torch.empty_like(out["y"], device="cpu").pin_memory() for _ in range(K)]
         aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(K)]
         s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -476,7 +508,7 @@ def run_gpu(args):
                     s_run.wait_event(up[i])
                     if i >= 2:
                         s_run.wait_event(down[i - 2])  # outputs of buffer b downloaded
-                    layers[b].run("moe_forward", s_run)
+                    fwd[b]()
                     comp[i] = ev(); comp[i].record(s_run)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp[i])
@@ -501,8 +533,8 @@ def run_gpu(args):
                "h2d_bytes_per_step": x_host.numel() * esz,
                "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size() + 4,
                "ms_per_step": e_ms,
-               "method": "moe_forward per step on pinned host buffers; upload, compute and "
-                         "download of consecutive steps overlap on three streams"}
+               "method": "moe_forward per step (its CUDA graph) on pinned host buffers; upload, "
+                         "compute and download of consecutive steps overlap on three streams"}
         layer = layers[0]
 
     status = layer.device_status()
@@ -531,7 +563,12 @@ def run_gpu(args):
         "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "direct" if args.no_graph else "CUDA graph per stage",
+                   "launch": ("direct C-ABI calls" if args.no_graph else
+                              "one CUDA graph of moe_forward per step (kernels chained by programmatic "
+                              "dependent launch)"),
+                   "stage_timing": "second timed pass of the same K steps, CUDA events between the "
+                                   "four stage calls (events break the launch overlap, so the stage "
+                                   "times add up to slightly more than ms_per_step)",
                    "stage_ms": stage_ms,
                    "memory_stages": mem_stages,
                    "router_dispatch_combine": {"bytes": rdc_bytes, "ms": rdc_ms,

@@ -186,7 +186,8 @@ moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, voi
  * before drops), dropped [T, k] (1 = over the capacity floor(T cf / E)) and
  * perm_row [T, k] (row in the expert-contiguous, token-ascending order of kept
  * slots, -1 if dropped).  It does not compute the balance statistic and does not
- * permute token rows.
+ * permute token rows.  Indices outside [0, E) are not counted and their slots are
+ * reported as dropped.
  *
  * Scratch: a static device array of about 1 MB inside the library, one per device
  * that loads the library, held until the process exits.  Limits: T * k <=

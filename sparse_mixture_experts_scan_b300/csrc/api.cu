@@ -197,6 +197,7 @@ struct Ctx {
     cudaStream_t st;
     int sms;
     bool bf16, use_tc, fused;
+    bool pdl = false;  // false until this call has launched its first kernel
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW;
     template <typename T>
@@ -206,6 +207,15 @@ struct Ctx {
 };
 
 int pick_bn(int N) { return N >= 256 ? 256 : 128; }
+
+// PDL for every launch of a C-ABI call except its first one (whose predecessor in
+// the stream may be the caller's own work).
+bool take_pdl(Ctx& c)
+{
+    const bool p = c.pdl;
+    c.pdl = true;
+    return p;
+}
 
 moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_outputs_t* out, void* ws,
                      size_t ws_bytes, void* stream, Ctx& c)
@@ -273,7 +283,7 @@ moe_status_t stage_router(Ctx& c)
     a.probs = c.out->probs;
     a.psum_part = c.at<float>(c.L.off_psum);
     a.scan_done = c.scan_done();
-    if (!c.L.tc_router) return cuda_status(launch_router(a, c.bf16, c.st));
+    if (!c.L.tc_router) return cuda_status(launch_router(a, c.bf16, c.st, take_pdl(c)));
     // tensor-core logits into the caller's logits buffer (or the workspace), then top-k
     if (a.logits == nullptr) a.logits = c.at<float>(c.L.off_logits);
     RouterGemmArgs g{};
@@ -285,7 +295,8 @@ moe_status_t stage_router(Ctx& c)
     g.bg = c.in->b_gate;
     g.logits = a.logits;
     g.err = c.err();
-    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st);
+    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
+                                       take_pdl(c));
     if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
     if (e == cudaSuccess) e = launch_router_topk(a, c.st);
     return cuda_status(e);
@@ -321,7 +332,7 @@ moe_status_t stage_dispatch(Ctx& c)
     a.slot_row = c.at<int32_t>(c.L.off_slot_row);
     a.ffn_sync = c.at<unsigned>(c.L.off_ffn_sync);
     a.ffn_sync_n = c.L.ffn_sync_n;
-    return cuda_status(launch_dispatch(a, c.sms, c.st));
+    return cuda_status(launch_dispatch(a, c.sms, c.st, take_pdl(c)));
 }
 
 moe_status_t stage_gemm(Ctx& c)
@@ -411,39 +422,42 @@ moe_status_t stage_gemm(Ctx& c)
             f.mt_max = L.ffn_sync_n - 2;
             f.err = c.err();
             const CUtensorMap maps[5] = {c.mA1, c.mB1, c.mB3, c.mA2, c.mB2};
-            e = launch_ffn_fused_tc(maps, f, act1, grid_for(mt_routed * (g1.n_tiles + g2.n_tiles), 1), c.st);
+            e = launch_ffn_fused_tc(maps, f, act1, grid_for(mt_routed * (g1.n_tiles + g2.n_tiles), 1), c.st,
+                                    take_pdl(c));
         } else if (mt_routed > 0) {
-            e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st);
+            e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st,
+                               take_pdl(c));
             if (e == cudaSuccess)
                 e = launch_gemm_tc(c.mA2, c.mB2, c.mB2, g2, kActNone, c.bn2, grid_for(mt_routed * g2.n_tiles, 1),
-                                   c.st);
+                                   c.st, take_pdl(c));
         }
         if (e == cudaSuccess && L.S > 0) {
             s1.n_tiles = ceil_div(s1.N, out1);
             s2.n_tiles = ceil_div(L.d, c.bn2);
-            e = launch_gemm_tc(c.mAs1, c.mB1, c.mB3, s1, act1, c.bn1, grid_for(mt_shared * s1.n_tiles, 1), c.st);
+            e = launch_gemm_tc(c.mAs1, c.mB1, c.mB3, s1, act1, c.bn1, grid_for(mt_shared * s1.n_tiles, 1), c.st,
+                               take_pdl(c));
             if (e == cudaSuccess)
                 e = launch_gemm_tc(c.mAs2, c.mB2, c.mB2, s2, kActNone, c.bn2, grid_for(mt_shared * s2.n_tiles, 1),
-                                   c.st);
+                                   c.st, take_pdl(c));
         }
     } else {
         g1.n_tiles = ceil_div(L.F, kFfmaTileN);
         g2.n_tiles = ceil_div(L.d, kFfmaTileN);
         if (mt_routed > 0) {
             e = launch_gemm_ffma(c.at<void>(L.off_xp), L.d, c.in->W1, c.in->W3, L.d, g1, act1, c.bf16,
-                                 grid_for(mt_routed * g1.n_tiles, 4), c.st);
+                                 grid_for(mt_routed * g1.n_tiles, 4), c.st, take_pdl(c));
             if (e == cudaSuccess)
                 e = launch_gemm_ffma(c.at<void>(L.off_h), L.F, c.in->W2, nullptr, L.F, g2, kActNone, c.bf16,
-                                     grid_for(mt_routed * g2.n_tiles, 4), c.st);
+                                     grid_for(mt_routed * g2.n_tiles, 4), c.st, take_pdl(c));
         }
         if (e == cudaSuccess && L.S > 0) {
             s1.n_tiles = ceil_div(s1.N, kFfmaTileN);
             s2.n_tiles = ceil_div(L.d, kFfmaTileN);
             e = launch_gemm_ffma(c.in->x, L.d, c.in->W1, c.in->W3, L.d, s1, act1, c.bf16,
-                                 grid_for(mt_shared * s1.n_tiles, 4), c.st);
+                                 grid_for(mt_shared * s1.n_tiles, 4), c.st, take_pdl(c));
             if (e == cudaSuccess)
                 e = launch_gemm_ffma(c.at<void>(L.off_hs), L.S * L.F, c.in->W2, nullptr, L.F, s2, kActNone,
-                                     c.bf16, grid_for(mt_shared * s2.n_tiles, 4), c.st);
+                                     c.bf16, grid_for(mt_shared * s2.n_tiles, 4), c.st, take_pdl(c));
         }
     }
     return cuda_status(e);
@@ -462,7 +476,7 @@ moe_status_t stage_combine(Ctx& c)
     a.k = c.L.k;
     a.d = c.L.d;
     a.residual_mode = c.p.residual_mode;
-    return cuda_status(launch_combine(a, c.bf16, c.sms, c.st));
+    return cuda_status(launch_combine(a, c.bf16, c.sms, c.st, take_pdl(c)));
 }
 
 using StageFn = moe_status_t (*)(Ctx&);

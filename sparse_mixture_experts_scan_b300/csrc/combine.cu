@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
     constexpr int V = Vec<T>::N;
     __shared__ int s_row[8][kMaxTopK];
     __shared__ float s_gate[8][kMaxTopK];
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = a.d / V;
     const size_t row_bytes = (size_t)a.d * sizeof(T);
@@ -118,13 +120,12 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st)
+cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st, bool pdl)
 {
     long long grid = ((long long)a.T + 7) / 8;
     if (grid > (long long)num_sms * 32) grid = (long long)num_sms * 32;
-    if (bf16) k_combine<__nv_bfloat16><<<(int)grid, 256, 0, st>>>(a);
-    else k_combine<float><<<(int)grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    if (bf16) return launch_kernel(k_combine<__nv_bfloat16>, dim3((int)grid), dim3(256), 0, st, pdl, a);
+    return launch_kernel(k_combine<float>, dim3((int)grid), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace moe

@@ -41,6 +41,36 @@ constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s
 
 __host__ __device__ constexpr inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch.  A kernel launched with pdl = true may start while
+// the previous kernel of its stream is still running; it must call griddep_wait()
+// before reading anything earlier kernels wrote, and every such kernel calls it
+// before exiting, so the completion of a grid implies that of all its predecessors.
+// griddep_launch_dependents() lets the next kernel begin launching: it launches once
+// every CTA of this grid has called it (or exited), so all of this grid's CTAs are
+// resident by then and the early CTAs of the next kernel cannot starve them.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 bool pdl, Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device); later
 // launches (including ones recorded into CUDA graphs) make no attribute call.
 inline cudaError_t ensure_smem_limit(const void* kernel, size_t bytes)

@@ -72,12 +72,17 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     __shared__ int wsum[32][3];
     __shared__ int s_last;
 
+    griddep_launch_dependents();
+    griddep_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E;
     const long long n_slots = (long long)a.T * a.k;
     const long long s = (long long)blockIdx.x * kScanChunk + tid;
-    const bool valid = s < n_slots;
-    const int e = valid ? a.idx[s] : -1;
+    // an index outside [0, E) (never produced by the router; possible in caller-provided
+    // indices) is not counted and its slot ends up dropped
+    int e = s < n_slots ? a.idx[s] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const bool valid = e >= 0;
 
     for (int i = tid; i < 32 * E; i += 1024) sm[i] = 0;
     __syncthreads();
@@ -210,6 +215,8 @@ __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
 {
     __shared__ float s_part[kMaxExperts > 256 ? kMaxExperts : 256];
     __shared__ double dsum[8];
+    griddep_launch_dependents();
+    griddep_wait();
     // block 0 also computes the balance statistic (it needs the scan's counts,
     // complete at this kernel's start), off the scan's serial tail
     if (blockIdx.x == 0 && a.aux != nullptr && a.n_router_blocks > 0) balance_statistic(a, s_part, dsum);
@@ -220,9 +227,10 @@ __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
          s += (long long)gridDim.x * 8) {
         const int t = (int)(s / a.k);
         const int e = a.idx[s];
+        const bool e_ok = e >= 0 && e < a.E;
         const int c = (int)(s / kScanChunk);
-        const int pos = a.chunk_base[(size_t)c * a.E + e] + a.local_rank[s];
-        const bool keep = a.C < 0 || pos < a.C;
+        const int pos = e_ok ? a.chunk_base[(size_t)c * a.E + e] + a.local_rank[s] : 0;
+        const bool keep = e_ok && (a.C < 0 || pos < a.C);
         const int row = keep ? a.row_off[e] + pos : -1;
         if (lane == 0) {
             a.dropped[s] = keep ? 0 : 1;
@@ -250,21 +258,19 @@ __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
 
 size_t dispatch_scan_smem(int E) { return sizeof(int32_t) * 32 * (size_t)(E < 64 ? 64 : E); }
 
-cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st)
+cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st, bool pdl)
 {
     const size_t smem = dispatch_scan_smem(a.E);
     if (smem > 48 * 1024) {
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_dispatch_scan), smem);
         if (e != cudaSuccess) return e;
     }
-    k_dispatch_scan<<<a.nchunks, 1024, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(k_dispatch_scan, dim3(a.nchunks), dim3(1024), smem, st, pdl, a);
     if (e != cudaSuccess) return e;
     const long long n_slots = (long long)a.T * a.k;
     long long grid = (n_slots + 7) / 8;
     if (grid > (long long)num_sms * 32) grid = (long long)num_sms * 32;
-    k_permute<<<(int)grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_permute, dim3((int)grid), dim3(256), 0, st, true, a);
 }
 
 cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st)

@@ -75,9 +75,10 @@ __global__ void __launch_bounds__(256) k_positions_noalloc(DispatchArgs a)
     for (long long s = (long long)blockIdx.x * 256 + threadIdx.x; s < n_slots;
          s += (long long)gridDim.x * 256) {
         const int e = a.idx[s];
+        const bool e_ok = e >= 0 && e < a.E;  // out-of-range indices are dropped
         const int c = (int)(s / kScanChunk);
-        const int pos = a.chunk_base[(size_t)c * a.E + e] + a.local_rank[s];
-        const bool keep = a.C < 0 || pos < a.C;
+        const int pos = e_ok ? a.chunk_base[(size_t)c * a.E + e] + a.local_rank[s] : 0;
+        const bool keep = e_ok && (a.C < 0 || pos < a.C);
         a.dropped[s] = keep ? 0 : 1;
         a.perm_row[s] = keep ? a.kept_off[e] + pos : -1;
     }

@@ -107,13 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_roff = s_mt + kMaxExperts + 1;
     int* s_rows = s_roff + kMaxExperts;
 
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = args.G;
-    for (int i = threadIdx.x; i <= G; i += kThreads) s_mt[i] = args.mtile_off[i];
-    for (int i = threadIdx.x; i < G; i += kThreads) {
-        s_roff[i] = args.row_off[i];
-        s_rows[i] = args.rows[i];
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -146,6 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+
+    griddep_wait();  // tile tables, counters and Xp come from earlier kernels
+    for (int i = threadIdx.x; i <= G; i += kThreads) s_mt[i] = args.mtile_off[i];
+    for (int i = threadIdx.x; i < G; i += kThreads) {
+        s_roff[i] = args.row_off[i];
+        s_rows[i] = args.rows[i];
+    }
+    __syncthreads();
 
     const int total1 = s_mt[G] * args.n_tiles1;
     const int total = total1 + s_mt[G] * args.n_tiles2;
@@ -363,26 +367,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, int ACT1>
-cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st)
+cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st, bool pdl)
 {
     auto kern = k_ffn_fused_tc<BN, ACT1>;
     const size_t smem = FCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, pdl, maps[0], maps[1], maps[2], maps[3],
+                         maps[4], a);
 }
 
 }  // namespace
 
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
-                                cudaStream_t st)
+                                cudaStream_t st, bool pdl)
 {
     switch (act1) {
-    case kActRelu: return launch_t<256, kActRelu>(maps, a, grid, st);
-    case kActGeluTanh: return launch_t<256, kActGeluTanh>(maps, a, grid, st);
-    case kActGeluErf: return launch_t<256, kActGeluErf>(maps, a, grid, st);
-    default: return launch_t<256, kActSwiglu>(maps, a, grid, st);
+    case kActRelu: return launch_t<256, kActRelu>(maps, a, grid, st, pdl);
+    case kActGeluTanh: return launch_t<256, kActGeluTanh>(maps, a, grid, st, pdl);
+    case kActGeluErf: return launch_t<256, kActGeluErf>(maps, a, grid, st, pdl);
+    default: return launch_t<256, kActSwiglu>(maps, a, grid, st, pdl);
     }
 }
 

@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(256) k_grouped_gemm_ffma(const T* __restrict__
     __shared__ float B3s[GATED ? kTK : 1][kTN + 4];
     __shared__ int s_mt[kMaxExperts + 1];
 
+    griddep_launch_dependents();
+    griddep_wait();
     const bool fixed = args.mtile_off == nullptr;
     const int G = fixed ? 1 : args.G;
     for (int i = threadIdx.x; i <= G; i += 256)
@@ -137,28 +139,27 @@ __global__ void __launch_bounds__(256) k_grouped_gemm_ffma(const T* __restrict__
 
 template <typename T>
 cudaError_t launch_ffma_t(const void* A, int lda, const void* B, const void* B3, int ldb,
-                          const GroupedGemmArgs& args, int act, int grid, cudaStream_t st)
+                          const GroupedGemmArgs& args, int act, int grid, cudaStream_t st, bool pdl)
 {
     const T* a = static_cast<const T*>(A);
     const T* b = static_cast<const T*>(B);
     const T* b3 = static_cast<const T*>(B3);
     switch (act) {
-    case kActNone: k_grouped_gemm_ffma<T, kActNone><<<grid, 256, 0, st>>>(a, lda, b, b3, ldb, args); break;
-    case kActRelu: k_grouped_gemm_ffma<T, kActRelu><<<grid, 256, 0, st>>>(a, lda, b, b3, ldb, args); break;
-    case kActGeluTanh: k_grouped_gemm_ffma<T, kActGeluTanh><<<grid, 256, 0, st>>>(a, lda, b, b3, ldb, args); break;
-    case kActGeluErf: k_grouped_gemm_ffma<T, kActGeluErf><<<grid, 256, 0, st>>>(a, lda, b, b3, ldb, args); break;
-    default: k_grouped_gemm_ffma<T, kActSwiglu><<<grid, 256, 0, st>>>(a, lda, b, b3, ldb, args); break;
+    case kActNone: return launch_kernel(k_grouped_gemm_ffma<T, kActNone>, dim3(grid), dim3(256), 0, st, pdl, a, lda, b, b3, ldb, args);
+    case kActRelu: return launch_kernel(k_grouped_gemm_ffma<T, kActRelu>, dim3(grid), dim3(256), 0, st, pdl, a, lda, b, b3, ldb, args);
+    case kActGeluTanh: return launch_kernel(k_grouped_gemm_ffma<T, kActGeluTanh>, dim3(grid), dim3(256), 0, st, pdl, a, lda, b, b3, ldb, args);
+    case kActGeluErf: return launch_kernel(k_grouped_gemm_ffma<T, kActGeluErf>, dim3(grid), dim3(256), 0, st, pdl, a, lda, b, b3, ldb, args);
+    default: return launch_kernel(k_grouped_gemm_ffma<T, kActSwiglu>, dim3(grid), dim3(256), 0, st, pdl, a, lda, b, b3, ldb, args);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
-                             const GroupedGemmArgs& args, int act, bool bf16, int grid, cudaStream_t st)
+                             const GroupedGemmArgs& args, int act, bool bf16, int grid, cudaStream_t st, bool pdl)
 {
-    if (bf16) return launch_ffma_t<__nv_bfloat16>(A, lda, B, B3, ldb, args, act, grid, st);
-    return launch_ffma_t<float>(A, lda, B, B3, ldb, args, act, grid, st);
+    if (bf16) return launch_ffma_t<__nv_bfloat16>(A, lda, B, B3, ldb, args, act, grid, st, pdl);
+    return launch_ffma_t<float>(A, lda, B, B3, ldb, args, act, grid, st, pdl);
 }
 
 }  // namespace moe

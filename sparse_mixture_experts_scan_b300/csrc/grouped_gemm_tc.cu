@@ -69,16 +69,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_roff = s_mt + kMaxExperts + 1;
     int* s_rows = s_roff + kMaxExperts;
 
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool fixed = args.mtile_off == nullptr;
     const int G = fixed ? 1 : args.G;
 
-    for (int i = threadIdx.x; i <= G; i += kThreads)
-        s_mt[i] = fixed ? (i == 0 ? 0 : ceil_div(args.fixed_rows, kBM)) : args.mtile_off[i];
-    for (int i = threadIdx.x; i < G; i += kThreads) {
-        s_roff[i] = fixed ? 0 : args.row_off[i];
-        s_rows[i] = fixed ? args.fixed_rows : args.rows[i];
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -105,6 +100,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+
+    griddep_wait();  // the tile tables and the A operand come from earlier kernels
+    for (int i = threadIdx.x; i <= G; i += kThreads)
+        s_mt[i] = fixed ? (i == 0 ? 0 : ceil_div(args.fixed_rows, kBM)) : args.mtile_off[i];
+    for (int i = threadIdx.x; i < G; i += kThreads) {
+        s_roff[i] = fixed ? 0 : args.row_off[i];
+        s_rows[i] = fixed ? args.fixed_rows : args.rows[i];
+    }
+    __syncthreads();
 
     const int n_tiles = args.n_tiles;
     const int total = s_mt[G] * n_tiles;
@@ -249,26 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int ACT>
 cudaError_t launch_tc_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
-                        const GroupedGemmArgs& args, int grid, cudaStream_t st)
+                        const GroupedGemmArgs& args, int grid, cudaStream_t st, bool pdl)
 {
     auto kern = k_grouped_gemm_tc<BN, ACT>;
     const size_t smem = TcCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(a, b, b3, args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, pdl, a, b, b3, args);
 }
 
 template <int BN>
 cudaError_t launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
-                         const GroupedGemmArgs& args, int act, int grid, cudaStream_t st)
+                         const GroupedGemmArgs& args, int act, int grid, cudaStream_t st, bool pdl)
 {
     switch (act) {
-    case kActNone: return launch_tc_t<BN, kActNone>(a, b, b3, args, grid, st);
-    case kActRelu: return launch_tc_t<BN, kActRelu>(a, b, b3, args, grid, st);
-    case kActGeluTanh: return launch_tc_t<BN, kActGeluTanh>(a, b, b3, args, grid, st);
-    case kActGeluErf: return launch_tc_t<BN, kActGeluErf>(a, b, b3, args, grid, st);
-    default: return launch_tc_t<BN, kActSwiglu>(a, b, b3, args, grid, st);
+    case kActNone: return launch_tc_t<BN, kActNone>(a, b, b3, args, grid, st, pdl);
+    case kActRelu: return launch_tc_t<BN, kActRelu>(a, b, b3, args, grid, st, pdl);
+    case kActGeluTanh: return launch_tc_t<BN, kActGeluTanh>(a, b, b3, args, grid, st, pdl);
+    case kActGeluErf: return launch_tc_t<BN, kActGeluErf>(a, b, b3, args, grid, st, pdl);
+    default: return launch_tc_t<BN, kActSwiglu>(a, b, b3, args, grid, st, pdl);
     }
 }
 
@@ -277,10 +280,10 @@ cudaError_t launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUten
 size_t gemm_tc_smem(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
-                           const GroupedGemmArgs& args, int act, int bn, int grid, cudaStream_t st)
+                           const GroupedGemmArgs& args, int act, int bn, int grid, cudaStream_t st, bool pdl)
 {
-    if (bn == 256) return launch_tc_bn<256>(a, b, b3, args, act, grid, st);
-    return launch_tc_bn<128>(a, b, b3, args, act, grid, st);
+    if (bn == 256) return launch_tc_bn<256>(a, b, b3, args, act, grid, st, pdl);
+    return launch_tc_bn<128>(a, b, b3, args, act, grid, st, pdl);
 }
 
 }  // namespace moe

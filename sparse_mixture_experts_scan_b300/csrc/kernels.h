@@ -10,6 +10,10 @@
 
 namespace moe {
 
+// Every launch function takes `pdl`: true lets the launch overlap the tail of the
+// previous kernel of the stream (programmatic dependent launch; see common.cuh).
+// It is false for the first kernel of each C-ABI call.
+
 // ---- stage 1: router -------------------------------------------------------
 struct RouterArgs {
     const void* x;        // [T, d] fp32 or bf16
@@ -25,7 +29,7 @@ struct RouterArgs {
 };
 int router_blocks(int T);
 // CUDA-core router: fp32 logits by FFMA, then softmax / top-k / gates.
-cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st, bool pdl);
 // Softmax / top-k / gates of logits already in a.logits.
 cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st);
 
@@ -40,7 +44,7 @@ struct RouterGemmArgs {
 };
 int router_tc_bn(int T, int E);  // MMA N of the router GEMM (16..128), ~128 CTAs
 cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms,
-                               cudaStream_t st);
+                               cudaStream_t st, bool pdl);
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
                                     int bn, int sms, cudaStream_t st);
 
@@ -74,7 +78,7 @@ struct DispatchArgs {
     int ffn_sync_n;
 };
 size_t dispatch_scan_smem(int E);
-cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st, bool pdl);
 // The scan kernel alone (no permute); used by the allocation-free entry point.
 cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st);
 
@@ -83,7 +87,7 @@ cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st);
 // kActGeluErf (bias allowed) or kActSwiglu (gated: B rows from W1 and W3).
 cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                            const GroupedGemmArgs& args, int act, int bn, int grid,
-                           cudaStream_t st);
+                           cudaStream_t st, bool pdl);
 size_t gemm_tc_smem(int bn);
 // Both expert layers of the routed experts in one persistent launch (dynamic tile
 // scheduler, GEMM2 tiles wait for the GEMM1 tiles of their M-tile).
@@ -110,12 +114,12 @@ struct FusedFfnArgs {
 };
 // maps: A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2); MMA N = 256.
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
-                                cudaStream_t st);
+                                cudaStream_t st, bool pdl);
 
 // FFMA kernel over fp32 or bf16 operands (A [a_rows_alloc, lda], B [*, ldb]).
 cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
                              const GroupedGemmArgs& args, int act, bool bf16, int grid,
-                             cudaStream_t st);
+                             cudaStream_t st, bool pdl);
 constexpr int kFfmaTileN = 64;
 
 // ---- stage 4: combine ------------------------------------------------------
@@ -128,6 +132,6 @@ struct CombineArgs {
     void* y;              // [T, d]
     int T, k, d, residual_mode;
 };
-cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st, bool pdl);
 
 }  // namespace moe

@@ -58,7 +58,12 @@ __device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const R
         }
     }
 
-    // top-k: k rounds of a warp argmax over (logit desc, expert asc)
+    // top-k: k rounds of a warp argmax over (logit desc, expert asc).  A NaN logit
+    // competes as -inf, so every comparison is ordered and the winner of each round
+    // is always one of the E experts (k <= E), whatever the inputs hold.
+    float ls[EJ];
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) ls[j] = (l[j] != l[j]) ? -INFINITY : l[j];
     uint32_t taken = 0;
     int my_e = 0;
     float my_p = 0.0f, gsum = 0.0f;
@@ -69,8 +74,8 @@ __device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const R
 #pragma unroll
         for (int j = 0; j < EJ; ++j) {
             const int e = lane + 32 * j;
-            if (e < a.E && !((taken >> j) & 1u) && (l[j] > bv || be == 0x7fffffff)) {
-                bv = l[j];
+            if (e < a.E && !((taken >> j) & 1u) && (ls[j] > bv || be == 0x7fffffff)) {
+                bv = ls[j];
                 be = e;
                 bp = p[j];
             }
@@ -123,6 +128,8 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
     __shared__ float xs[kRouterTokens][kRouterBK];
     __shared__ float ws[32 * EJ * kWsStride];  // reused for the column sums afterwards
 
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kRouterTokens;
     const TX* x = static_cast<const TX*>(a.x);
@@ -197,6 +204,8 @@ template <int EJ>
 __global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
 {
     __shared__ float scratch[8 * 32 * EJ];
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kRouterTokens;
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
@@ -224,22 +233,20 @@ __global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
 }
 
 template <typename TX>
-cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st)
+cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st, bool pdl)
 {
-    const int grid = ceil_div(a.T, kRouterTokens);
-    if (a.E <= 32) k_router<TX, 1><<<grid, 256, 0, st>>>(a);
-    else if (a.E <= 64) k_router<TX, 2><<<grid, 256, 0, st>>>(a);
-    else if (a.E <= 128) k_router<TX, 4><<<grid, 256, 0, st>>>(a);
-    else if (a.E <= 256) k_router<TX, 8><<<grid, 256, 0, st>>>(a);
-    else k_router<TX, 16><<<grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    const dim3 grid(ceil_div(a.T, kRouterTokens)), block(256);
+    if (a.E <= 32) return launch_kernel(k_router<TX, 1>, grid, block, 0, st, pdl, a);
+    if (a.E <= 64) return launch_kernel(k_router<TX, 2>, grid, block, 0, st, pdl, a);
+    if (a.E <= 128) return launch_kernel(k_router<TX, 4>, grid, block, 0, st, pdl, a);
+    if (a.E <= 256) return launch_kernel(k_router<TX, 8>, grid, block, 0, st, pdl, a);
+    return launch_kernel(k_router<TX, 16>, grid, block, 0, st, pdl, a);
 }
 
 template <int EJ>
 cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
 {
-    k_router_topk<EJ><<<ceil_div(a.T, kRouterTokens), 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_router_topk<EJ>, dim3(ceil_div(a.T, kRouterTokens)), dim3(256), 0, st, true, a);
 }
 
 }  // namespace
@@ -255,9 +262,9 @@ cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st)
     return launch_topk_ej<16>(a, st);
 }
 
-cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st)
+cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st, bool pdl)
 {
-    return bf16 ? launch_router_t<__nv_bfloat16>(a, st) : launch_router_t<float>(a, st);
+    return bf16 ? launch_router_t<__nv_bfloat16>(a, st, pdl) : launch_router_t<float>(a, st, pdl);
 }
 
 }  // namespace moe

@@ -51,6 +51,8 @@ struct RCfg {
 __global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int d,
                                                      __nv_bfloat16* __restrict__ out)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const size_t n = (size_t)E_pad * d;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int e = (int)(i / d);
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();  // the W_gate splits come from the previous kernel
 
     const int m_tiles = ceil_div(a.T, kRBM);
     const int total = m_tiles * a.n_tiles;
@@ -299,8 +303,7 @@ cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGe
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int tiles = ceil_div(a.T, kRBM) * a.n_tiles;
-    kern<<<tiles < sms ? tiles : sms, kRThreads, smem, st>>>(x, w, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(tiles < sms ? tiles : sms), dim3(kRThreads), smem, st, true, x, w, a);
 }
 
 }  // namespace
@@ -316,13 +319,14 @@ int router_tc_bn(int T, int E)
     return bn;
 }
 
-cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms, cudaStream_t st)
+cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms, cudaStream_t st,
+                               bool pdl)
 {
     const size_t n = (size_t)E_pad * d;
     size_t grid = (n + 255) / 256;
     if (grid > (size_t)sms * 8) grid = (size_t)sms * 8;
-    k_split_wgate<<<(int)grid, 256, 0, st>>>(Wg, E, E_pad, d, static_cast<__nv_bfloat16*>(out));
-    return cudaGetLastError();
+    return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, d,
+                         static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,

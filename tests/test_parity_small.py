@@ -197,3 +197,24 @@ def test_fused_and_two_launch_experts_agree_bitwise(name):
     for _ in range(3):  # the scheduler counters re-arm themselves between launches
         c = run_device(cfg, inp)
         assert torch.equal(a["y"], c["y"])
+
+
+def test_nan_tokens_route_to_valid_experts():
+    # Non-finite inputs must never produce an expert index outside [0, E): NaN logits
+    # compete as -inf in the selection (so an all-NaN row takes experts 0, 1, ...,
+    # as the oracle's selection on the same logits does), and the finite tokens are
+    # unaffected.
+    cfg = _case("mixtral", T=300, d=128, E=8, k=2, F=128, cf=1.0)
+    inp = _inputs(cfg)
+    x = inp["x"].clone()
+    bad = torch.tensor([0, 7, 150, 299], device="cuda")
+    x[bad] = float("nan")
+    inp["x"] = x
+    out = run_device(cfg, inp)
+    idx = out["expert_idx"]
+    assert int(idx.min()) >= 0 and int(idx.max()) < cfg.E
+    check_routing_bitexact(cfg, out)
+    good = np.setdiff1d(np.arange(cfg.T), bad.cpu().numpy())
+    r = orc.route_from_logits(out["logits"].numpy(), k=cfg.k, renormalize=cfg.renormalize, cf=cfg.cf)
+    from parity_utils import check_output
+    check_output(cfg, to_cpu(inp), out, r, tokens=good)
