@@ -449,8 +449,12 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16_tflops"]}
     wl_key = args.config
-    tr = traffic_from_profiles("grouped_gemm_tc.cu", wl_key)
-    roof.update({"traffic": tr, "kernel": "moe_grouped_gemm (tcgen05 grouped GEMM, GEMM1+GEMM2)",
+    fused = cfg.dtype == "bf16"
+    tr = traffic_from_profiles("ffn_fused_tc.cu" if fused else "grouped_gemm_ffma.cu", wl_key)
+    kname = ("moe_grouped_gemm stage: k_ffn_fused_tc (both expert layers, one persistent tcgen05 launch)"
+             + (" + shared-expert k_grouped_gemm_tc launches" if cfg.S else "")) if fused else \
+        "moe_grouped_gemm stage: k_grouped_gemm_ffma (fp32)"
+    roof.update({"traffic": tr, "kernel": kname,
                  "algorithmic_bytes": gemm["bytes"], "algorithmic_flops": gemm["flops"],
                  "touched_experts": gemm["touched_experts"], "kept_rows": gemm["kept_rows"],
                  "peak_source": pk["source"] + " (burst)",

@@ -30,6 +30,7 @@ struct Layout {
     bool tc_router;    // bf16 router logits on the tensor core
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
     size_t off_wsplit, off_logits;
+    size_t off_psum_chunk;
     size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
     int ffn_sync_n;
     size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
@@ -105,6 +106,7 @@ Layout make_layout(const moe_params_t& p)
     L.ffn_sync_n = 2 + L.rows_cap / kSegRows;
     L.off_ffn_sync = take(sizeof(unsigned) * L.ffn_sync_n);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
+    L.off_psum_chunk = take(sizeof(float) * (size_t)L.nchunks * L.E);
     L.off_hist = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
     L.off_base = take(sizeof(int32_t) * (size_t)L.nchunks * L.E);
     L.off_rank = take(sizeof(int32_t) * (size_t)slots);
@@ -314,6 +316,7 @@ moe_status_t stage_dispatch(Ctx& c)
     a.nchunks = c.L.nchunks;
     a.n_router_blocks = c.L.n_rblk;
     a.psum_part = c.at<float>(c.L.off_psum);
+    a.psum_chunk = c.at<float>(c.L.off_psum_chunk);
     a.local_rank = c.at<int32_t>(c.L.off_rank);
     a.chunk_hist = c.at<int32_t>(c.L.off_hist);
     a.chunk_base = c.at<int32_t>(c.L.off_base);

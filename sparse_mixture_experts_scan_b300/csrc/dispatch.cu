@@ -17,9 +17,10 @@
 //   - the last block to arrive scans the chunk histograms per expert (counts,
 //     chunk bases), the per-expert kept counts over experts (segment offsets,
 //     M-tile offsets for the grouped GEMM).
+// The balance statistic is reduced in two levels: every scan block sums a slice
+// of the router's per-block probability sums, the last block adds those partials.
 // k_permute: one warp per slot; position = chunk base + rank; kept rows are
-// copied with 16-byte vector loads/stores.  Its block 0 also reduces the
-// router's per-block probability sums into the balance statistic.
+// copied with 16-byte vector loads/stores.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
 {
     extern __shared__ int32_t sm[];  // [32][E] warp histograms, reused by the last block
     __shared__ int wsum[32][3];
+    __shared__ double dsum[32];
     __shared__ int s_last;
 
     griddep_launch_dependents();
@@ -101,6 +103,38 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     }
     __syncthreads();
     if (valid) a.local_rank[s] = sm[warp * E + e] + wrank;
+
+    // balance statistic, first level: this block sums a contiguous slice of the
+    // router's per-block column sums (fixed order: partition p takes rows r0+p,
+    // r0+p+P, ...; partitions added in order)
+    const int P = 1024 / E;
+    if (a.n_router_blocks > 0) {
+        __syncthreads();  // sm is reused below
+        float* s_part = reinterpret_cast<float*>(sm);
+        const int R = a.n_router_blocks, nb = gridDim.x;
+        const int r0 = (int)((long long)blockIdx.x * R / nb);
+        const int r1 = (int)((long long)(blockIdx.x + 1) * R / nb);
+        if (tid < P * E) {
+            const int ee = tid % E, p = tid / E;
+            float acc = 0.0f;
+            int r = r0 + p;
+            for (; r + 3 * P < r1; r += 4 * P) {
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldcg(&a.psum_part[(size_t)(r + u * P) * E + ee]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc += v[u];
+            }
+            for (; r < r1; r += P) acc += __ldcg(&a.psum_part[(size_t)r * E + ee]);
+            s_part[p * E + ee] = acc;
+        }
+        __syncthreads();
+        if (tid < E) {
+            float acc = 0.0f;
+            for (int p = 0; p < P; ++p) acc += s_part[p * E + tid];
+            a.psum_chunk[(size_t)blockIdx.x * E + tid] = acc;
+        }
+    }
 
     // the last block to arrive finishes the device-wide part
     __threadfence();
@@ -148,58 +182,48 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     }
     if (tid == 0) a.mtile_off[E] = tot[2];
 
+    // balance statistic, second level: E * sum_e (counts_e / (T k)) * P_e, P_e the mean
+    // router probability, from the scan blocks' partial sums (fixed order)
+    if (a.n_router_blocks > 0 && a.aux != nullptr) {
+        float* s_part = reinterpret_cast<float*>(sm);
+        const int nb = gridDim.x;
+        if (tid < P * E) {
+            const int ee = tid % E, p = tid / E;
+            float acc = 0.0f;
+            int q = p;
+            for (; q + 3 * P < nb; q += 4 * P) {
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldcg(&a.psum_chunk[(size_t)(q + u * P) * E + ee]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc += v[u];
+            }
+            for (; q < nb; q += P) acc += __ldcg(&a.psum_chunk[(size_t)q * E + ee]);
+            s_part[p * E + ee] = acc;
+        }
+        __syncthreads();
+        double term = 0.0;
+        if (tid < E) {
+            float Pe = 0.0f;
+            for (int p = 0; p < P; ++p) Pe += s_part[p * E + tid];
+            term = ((double)my_count / ((double)a.T * (double)a.k)) * ((double)Pe / (double)a.T);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+        if (lane == 0) dsum[warp] = term;
+        __syncthreads();
+        if (warp == 0) {
+            double w = dsum[lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if (lane == 0) *a.aux = (float)((double)E * w);
+        }
+    }
+
     // the fused expert kernel that follows starts from zeroed scheduler counters
     if (a.ffn_sync != nullptr)
         for (int i = tid; i < a.ffn_sync_n; i += 1024) a.ffn_sync[i] = 0u;
     if (tid == 0) *a.scan_done = 0u;  // re-arm for the next call
-}
-
-// Switch balance statistic E * sum_e (counts_e / (T k)) * P_e with P_e the mean router
-// probability, from the router's per-block column sums, reduced in a fixed order
-// (partition p sums blocks p, p+P, ... ascending; partitions in order; experts in a
-// fixed tree).  Run by the 256 threads of one block.
-__device__ void balance_statistic(const DispatchArgs& a, float* s_part, double* dsum)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int E = a.E;
-    const int P = E >= 256 ? 1 : 256 / E;
-    if (tid < P * E) {
-        const int ee = tid % E, p = tid / E;
-        float acc = 0.0f;
-        int b = p;
-        for (; b + 7 * P < a.n_router_blocks; b += 8 * P) {  // 8 loads in flight, summed in order
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(&a.psum_part[(size_t)(b + u * P) * E + ee]);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) acc += v[u];
-        }
-        for (; b < a.n_router_blocks; b += P) acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
-        s_part[p * E + ee] = acc;
-    }
-    // E may exceed the block: the remaining experts are summed by the same threads
-    for (int ee = tid + 256; ee < E && P == 1; ee += 256) {
-        float acc = 0.0f;
-        for (int b = 0; b < a.n_router_blocks; ++b) acc += __ldcg(&a.psum_part[(size_t)b * E + ee]);
-        s_part[ee] = acc;
-    }
-    __syncthreads();
-    double term = 0.0;
-    for (int ee = tid; ee < E; ee += 256) {
-        float Pe = 0.0f;
-        for (int p = 0; p < P; ++p) Pe += s_part[p * E + ee];
-        term += ((double)__ldcg(&a.counts[ee]) / ((double)a.T * (double)a.k)) * ((double)Pe / (double)a.T);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-    if (lane == 0) dsum[warp] = term;
-    __syncthreads();
-    if (warp == 0) {
-        double w = lane < 8 ? dsum[lane] : 0.0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (lane == 0) *a.aux = (float)((double)E * w);
-    }
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p)
@@ -213,13 +237,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p)
 
 __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
 {
-    __shared__ float s_part[kMaxExperts > 256 ? kMaxExperts : 256];
-    __shared__ double dsum[8];
     griddep_launch_dependents();
     griddep_wait();
-    // block 0 also computes the balance statistic (it needs the scan's counts,
-    // complete at this kernel's start), off the scan's serial tail
-    if (blockIdx.x == 0 && a.aux != nullptr && a.n_router_blocks > 0) balance_statistic(a, s_part, dsum);
     const int lane = threadIdx.x & 31;
     const long long n_slots = (long long)a.T * a.k;
     const int nvec = a.row_bytes / 16;

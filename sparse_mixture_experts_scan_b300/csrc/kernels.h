@@ -57,6 +57,7 @@ struct DispatchArgs {
     int nchunks;          // ceil(T*k / kScanChunk)
     int n_router_blocks;
     const float* psum_part;
+    float* psum_chunk;    // [nchunks, E] partial sums of psum_part, one row per scan block
     int32_t* local_rank;  // [T*k] rank of the slot among its chunk's slots of the same expert
     int32_t* chunk_hist;  // [nchunks, E]
     int32_t* chunk_base;  // [nchunks, E] exclusive prefix over chunks
