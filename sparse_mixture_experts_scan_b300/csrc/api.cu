@@ -29,6 +29,7 @@ struct Layout {
     size_t esz;        // element size of the activation dtype
     bool tc_router;    // bf16 router logits on the tensor core
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
+    int r_ksplits;             // router GEMM K splits
     size_t off_wsplit, off_logits;
     size_t off_psum_chunk;
     size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
@@ -94,6 +95,7 @@ Layout make_layout(const moe_params_t& p)
     L.r_bn = router_tc_bn(p.T, p.E);
     L.r_tiles = (p.E + L.r_bn - 1) / L.r_bn;
     L.e_pad = L.r_tiles * L.r_bn;
+    L.r_ksplits = L.tc_router ? router_tc_ksplits(p.T, p.E, p.d_model) : 1;
 
     size_t o = kRegionAlign;  // header: [0] device error word, [1] scan arrival counter
     auto take = [&](size_t bytes) {
@@ -102,7 +104,7 @@ Layout make_layout(const moe_params_t& p)
         return at;
     };
     L.off_wsplit = take(L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
-    L.off_logits = take(sizeof(float) * (size_t)L.T * L.E);
+    L.off_logits = take(sizeof(float) * (size_t)L.T * L.E * (L.r_ksplits > 1 ? L.r_ksplits + 1 : 1));
     L.ffn_sync_n = 2 + L.rows_cap / kSegRows;
     L.off_ffn_sync = take(sizeof(unsigned) * L.ffn_sync_n);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
@@ -286,16 +288,22 @@ moe_status_t stage_router(Ctx& c)
     a.psum_part = c.at<float>(c.L.off_psum);
     a.scan_done = c.scan_done();
     if (!c.L.tc_router) return cuda_status(launch_router(a, c.bf16, c.st, take_pdl(c)));
-    // tensor-core logits into the caller's logits buffer (or the workspace), then top-k
+    // tensor-core logits into the caller's logits buffer (or the workspace), then top-k;
+    // with split K, partial sums go to the workspace and the top-k kernel adds them
     if (a.logits == nullptr) a.logits = c.at<float>(c.L.off_logits);
+    const bool split = c.L.r_ksplits > 1;
+    float* parts = c.at<float>(c.L.off_logits) + (size_t)c.L.T * c.L.E;
+    a.logit_parts = split ? parts : nullptr;
+    a.k_splits = c.L.r_ksplits;
     RouterGemmArgs g{};
     g.T = c.L.T;
     g.d = c.L.d;
     g.E = c.L.E;
     g.E_pad = c.L.e_pad;
     g.n_tiles = c.L.r_tiles;
+    g.k_splits = c.L.r_ksplits;
     g.bg = c.in->b_gate;
-    g.logits = a.logits;
+    g.logits = split ? parts : a.logits;
     g.err = c.err();
     cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
                                        take_pdl(c));

@@ -8,8 +8,8 @@
 // pass(t) is 1 for every token when residual_mode == 1; with residual_mode 0 it
 // is 1 only when all k routed slots of t were dropped.
 //
-// One warp per token; each lane handles 16-byte vectors of the row; no atomics,
-// so the result is deterministic.
+// One warp per (token, row segment); each lane handles 16-byte vectors of the
+// row; no atomics, so the result is deterministic.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -69,10 +69,18 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = a.d / V;
+    const int seg = a.seg_vec;  // 16-byte vectors per work item
+    const int nseg = ceil_div(nvec, seg);
+    const int items = a.T * nseg;  // < 2^31: nseg > 1 only for T < 8192
     const size_t row_bytes = (size_t)a.d * sizeof(T);
     const unsigned all_k = (a.k >= 32) ? 0xffffffffu : ((1u << a.k) - 1u);
 
-    for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
+    // work item = (token, segment of the row): whole rows for large batches, several
+    // independent warps per token when the batch is small
+    for (int item = blockIdx.x * 8 + warp; item < items; item += gridDim.x * 8) {
+        const int t = item / nseg;
+        const int v0 = (item - t * nseg) * seg;
+        const int v1 = min(nvec, v0 + seg);
         int r = -1;
         float g = 0.0f;
         if (lane < a.k) {
@@ -87,7 +95,7 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
         const char* xrow = static_cast<const char*>(a.x) + (size_t)t * row_bytes;
         const char* ysrow = a.ys ? static_cast<const char*>(a.ys) + (size_t)t * row_bytes : nullptr;
         char* yrow = static_cast<char*>(a.y) + (size_t)t * row_bytes;
-        for (int v = lane; v < nvec; v += 32) {
+        for (int v = v0 + lane; v < v1; v += 32) {
             float acc[V];
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] = 0.0f;
@@ -122,10 +130,19 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
 
 cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st, bool pdl)
 {
-    long long grid = ((long long)a.T + 7) / 8;
+    // one warp per token keeps the GPU full from about 8192 tokens on; smaller batches
+    // split each row into segments (multiples of 32 vectors) to raise the warp count
+    const int nvec = a.d / (bf16 ? 8 : 4);
+    int nseg = a.T >= 8192 ? 1 : ceil_div(16384, a.T);
+    const int max_seg = ceil_div(nvec, 32);
+    if (nseg > max_seg) nseg = max_seg;
+    CombineArgs b = a;
+    b.seg_vec = ceil_div(ceil_div(nvec, nseg), 32) * 32;
+    const long long items = (long long)a.T * ceil_div(nvec, b.seg_vec);
+    long long grid = (items + 7) / 8;
     if (grid > (long long)num_sms * 32) grid = (long long)num_sms * 32;
-    if (bf16) return launch_kernel(k_combine<__nv_bfloat16>, dim3((int)grid), dim3(256), 0, st, pdl, a);
-    return launch_kernel(k_combine<float>, dim3((int)grid), dim3(256), 0, st, pdl, a);
+    if (bf16) return launch_kernel(k_combine<__nv_bfloat16>, dim3((int)grid), dim3(256), 0, st, pdl, b);
+    return launch_kernel(k_combine<float>, dim3((int)grid), dim3(256), 0, st, pdl, b);
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@ struct RouterArgs {
     float* probs;         // [T, E] or nullptr
     float* psum_part;     // [router_blocks(T), E] per-block column sums of p
     unsigned* scan_done;  // dispatch-scan arrival counter, reset here
+    const float* logit_parts;  // k_router_topk with split-K logits: [k_splits, T, E], else nullptr
+    int k_splits;
 };
 int router_blocks(int T);
 // CUDA-core router: fp32 logits by FFMA, then softmax / top-k / gates.
@@ -38,11 +40,13 @@ struct RouterGemmArgs {
     int T, d, E;
     int E_pad;            // n_tiles * BN rows per split
     int n_tiles;          // expert tiles of BN columns
-    const float* bg;      // [E] or nullptr
-    float* logits;        // [T, E] fp32
+    int k_splits;         // K split into this many ranges (1: logits + bias written directly)
+    const float* bg;      // [E] or nullptr (added here only when k_splits == 1)
+    float* logits;        // [T, E] fp32 when k_splits == 1, else [k_splits, T, E] partial sums
     uint32_t* err;
 };
 int router_tc_bn(int T, int E);  // MMA N of the router GEMM (16..128), ~128 CTAs
+int router_tc_ksplits(int T, int E, int d);  // K splits so that small batches still fill ~128 CTAs
 cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms,
                                cudaStream_t st, bool pdl);
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
@@ -132,6 +136,7 @@ struct CombineArgs {
     const float* gates;
     void* y;              // [T, d]
     int T, k, d, residual_mode;
+    int seg_vec;          // 16-byte vectors per work item (set by launch_combine)
 };
 cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStream_t st, bool pdl);
 

@@ -105,18 +105,18 @@ __device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const R
 }
 
 // Deterministic per-block column sums of p (warps in order, each warp's tokens in
-// order) into a.psum_part[blockIdx.x].  `scratch` holds 8 x 32*EJ floats.
-template <int EJ>
+// order) into a.psum_part[blockIdx.x].  `scratch` holds WARPS x 32*EJ floats.
+template <int EJ, int WARPS = 8>
 __device__ __forceinline__ void block_psum(const float (&psum)[EJ], float* scratch, const RouterArgs& a)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int j = 0; j < EJ; ++j) scratch[warp * 32 * EJ + lane + 32 * j] = psum[j];
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += 256) {
+    for (int e = threadIdx.x; e < a.E; e += WARPS * 32) {
         float s = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) s += scratch[w * 32 * EJ + e];
+        for (int w = 0; w < WARPS; ++w) s += scratch[w * 32 * EJ + e];
         a.psum_part[(size_t)blockIdx.x * a.E + e] = s;
     }
 }
@@ -199,11 +199,15 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
 }
 
 // Softmax / top-k / gates for logits already in a.logits (computed by the
-// tensor-core router GEMM); same block layout and column sums as k_router.
-template <int EJ>
-__global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
+// tensor-core router GEMM), or for the sum of split-K partial logits plus the bias.
+// A block covers 32 tokens (the column-sum layout of k_router), WARPS warps with
+// 32 / WARPS tokens each: one token per warp when the registers allow it (E <= 256),
+// so a small batch still runs many independent warps.
+template <int EJ, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
 {
-    __shared__ float scratch[8 * 32 * EJ];
+    constexpr int TPW = kRouterTokens / WARPS;  // tokens per warp
+    __shared__ float scratch[WARPS * 32 * EJ];
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -213,23 +217,42 @@ __global__ void __launch_bounds__(256) k_router_topk(RouterArgs a)
 #pragma unroll
     for (int j = 0; j < EJ; ++j) psum[j] = 0.0f;
     // all loads of the warp's tokens first, then the dependent shuffle chains
-    float l[kTokPerWarp][EJ];
+    float l[TPW][EJ];
 #pragma unroll
-    for (int i = 0; i < kTokPerWarp; ++i) {
-        const int t = t0 + warp * kTokPerWarp + i;
+    for (int i = 0; i < TPW; ++i)
 #pragma unroll
         for (int j = 0; j < EJ; ++j) {
-            const int e = lane + 32 * j;
-            l[i][j] = (t < a.T && e < a.E) ? a.logits[(size_t)t * a.E + e] : -INFINITY;
+            const int t = t0 + warp * TPW + i, e = lane + 32 * j;
+            const bool in = t < a.T && e < a.E;
+            l[i][j] = in ? (a.logit_parts == nullptr ? a.logits[(size_t)t * a.E + e] : 0.0f) : -INFINITY;
         }
+    if (a.logit_parts != nullptr) {
+        // split-K: add the partial sums in K order (each round's loads are independent)
+        for (int ks = 0; ks < a.k_splits; ++ks) {
+            const float* part = a.logit_parts + (size_t)ks * a.T * a.E;
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                for (int j = 0; j < EJ; ++j) {
+                    const int t = t0 + warp * TPW + i, e = lane + 32 * j;
+                    if (t < a.T && e < a.E) l[i][j] += part[(size_t)t * a.E + e];
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) {
+                const int e = lane + 32 * j;
+                if (a.bg != nullptr && e < a.E) l[i][j] += a.bg[e];
+            }
     }
 #pragma unroll
-    for (int i = 0; i < kTokPerWarp; ++i) {
-        const int t = t0 + warp * kTokPerWarp + i;
+    for (int i = 0; i < TPW; ++i) {
+        const int t = t0 + warp * TPW + i;
         if (t >= a.T) break;  // warp-uniform
-        route_token<EJ>(l[i], t, a, false, psum);
+        route_token<EJ>(l[i], t, a, a.logit_parts != nullptr, psum);
     }
-    block_psum<EJ>(psum, scratch, a);
+    block_psum<EJ, WARPS>(psum, scratch, a);
 }
 
 template <typename TX>
@@ -246,7 +269,9 @@ cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st, bool pdl)
 template <int EJ>
 cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
 {
-    return launch_kernel(k_router_topk<EJ>, dim3(ceil_div(a.T, kRouterTokens)), dim3(256), 0, st, true, a);
+    constexpr int WARPS = EJ <= 8 ? 32 : 8;
+    return launch_kernel(k_router_topk<EJ, WARPS>, dim3(ceil_div(a.T, kRouterTokens)), dim3(WARPS * 32), 0, st,
+                         true, a);
 }
 
 }  // namespace

@@ -138,8 +138,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
     griddep_wait();  // the W_gate splits come from the previous kernel
 
     const int m_tiles = ceil_div(a.T, kRBM);
-    const int total = m_tiles * a.n_tiles;
-    const int num_kb = ceil_div(a.d, kRBK);
+    const int total = m_tiles * a.n_tiles * a.k_splits;
+    const int num_kb_all = ceil_div(a.d, kRBK);
+    const int kb_per_split = ceil_div(num_kb_all, a.k_splits);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -148,8 +149,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
             uint32_t phase = 0, filled = 0, fill_par = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const int m = tile / a.n_tiles, n = tile - m * a.n_tiles;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int mn = tile % (m_tiles * a.n_tiles), ks = tile / (m_tiles * a.n_tiles);
+                const int m = mn / a.n_tiles, n = mn - m * a.n_tiles;
+                const int kbeg = ks * kb_per_split;
+                const int kend = min(kbeg + kb_per_split, num_kb_all);
+                for (int kb = kbeg; kb < kend; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -183,7 +187,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kChunkKB, ++ci) {
+                const int ks = tile / (m_tiles * a.n_tiles);
+                const int kbeg = ks * kb_per_split;
+                const int num_kb = min(kbeg + kb_per_split, num_kb_all);
+                for (int kb0 = kbeg; kb0 < num_kb && ok; kb0 += kChunkKB, ++ci) {
                     const int acc = ci & 1;
                     if (!mbar_wait(&tempty[acc], ((ci >> 1) & 1) ^ 1u, abort_flag)) {
                         ok = false;
@@ -229,11 +236,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
         int ci = 0;
         const bool vec = (a.E % 4) == 0;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const int m = tile / a.n_tiles, n = tile - m * a.n_tiles;
+            const int mn = tile % (m_tiles * a.n_tiles), ks = tile / (m_tiles * a.n_tiles);
+            const int m = mn / a.n_tiles, n = mn - m * a.n_tiles;
+            const int kbeg = ks * kb_per_split;
+            const int num_kb = min(kbeg + kb_per_split, num_kb_all);
             float sum[BN];
 #pragma unroll
             for (int i = 0; i < BN; ++i) sum[i] = 0.0f;
-            for (int kb0 = 0; kb0 < num_kb; kb0 += kChunkKB, ++ci) {
+            for (int kb0 = kbeg; kb0 < num_kb; kb0 += kChunkKB, ++ci) {
                 const int acc = ci & 1;
                 if (!mbar_wait(&tfull[acc], (ci >> 1) & 1, abort_flag)) {
                     ok = false;
@@ -264,14 +274,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
             if (!ok) break;
             const int row = m * kRBM + q * 32 + lane;
             if (row < a.T) {
-                float* lrow = a.logits + (size_t)row * a.E;
+                // one K range: partial sums without bias, summed by the top-k kernel
+                const bool split = a.k_splits > 1;
+                float* lrow = a.logits + ((size_t)ks * a.T + row) * a.E;
 #pragma unroll
                 for (int i = 0; i < BN; i += 4) {
                     const int col = n * BN + i;
                     float o[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        o[u] = sum[i + u] + ((a.bg != nullptr && col + u < a.E) ? a.bg[col + u] : 0.0f);
+                        o[u] = sum[i + u] + ((!split && a.bg != nullptr && col + u < a.E) ? a.bg[col + u] : 0.0f);
                     if (vec && col + 4 <= a.E) {
                         *reinterpret_cast<float4*>(lrow + col) = make_float4(o[0], o[1], o[2], o[3]);
                     } else {
@@ -302,7 +314,7 @@ cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGe
     const size_t smem = RCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    const int tiles = ceil_div(a.T, kRBM) * a.n_tiles;
+    const int tiles = ceil_div(a.T, kRBM) * a.n_tiles * a.k_splits;
     return launch_kernel(kern, dim3(tiles < sms ? tiles : sms), dim3(kRThreads), smem, st, true, x, w, a);
 }
 
@@ -317,6 +329,16 @@ int router_tc_bn(int T, int E)
     int bn = 16;
     while (bn < per_tile && bn < 128) bn *= 2;
     return bn;
+}
+
+int router_tc_ksplits(int T, int E, int d)
+{
+    // split K only when the (M-tile, expert-tile) grid is far below ~128 CTAs, keeping
+    // at least 8 K-blocks per split
+    const int tiles = ceil_div(T, kRBM) * ceil_div(E, router_tc_bn(T, E));
+    int ks = 1;
+    while (ks < 8 && tiles * ks * 2 <= 128 && ceil_div(d, kRBK) >= 16 * ks) ks *= 2;
+    return ks;
 }
 
 cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms, cudaStream_t st,

@@ -33,6 +33,7 @@ SMALL = {
     "many_experts_drops": _case("skewed", T=512, d=128, E=256, k=8, F=128),
     "max_experts": _case("mixtral", T=256, d=64, E=512, k=4, F=64),
     "one_token": _case("mixtral", T=1, d=64, E=8, k=2, F=64),
+    "router_split_k": _case("skewed", T=64, d=2048, E=64, k=4, F=128, cf=None),  # few tokens, long K
     "tiny_fp32": config("tiny"),
     "fp32_swiglu_shared": _case("deepseek", T=100, d=64, E=8, k=2, F=48, dtype="f32"),
 }
@@ -165,7 +166,7 @@ def test_tcgen05_and_ffma_experts_agree():
 
 
 @pytest.mark.parametrize("name", ["switch_like_k1", "max_experts", "ragged_dims", "many_experts_drops",
-                                  "gelu_erf_k_eq_E"])
+                                  "gelu_erf_k_eq_E", "router_split_k"])
 def test_ffma_router_matches_oracle_and_tensor_core_router(name):
     # bf16 layers compute router logits on the tensor core (three-term bf16 split of
     # W_gate); the CUDA-core FFMA router is the cross-check.  Both must route
