@@ -25,7 +25,9 @@
  *   - f_i counts the router's selection before capacity drops, normalised by T*k;
  *   - residual mode 0 adds x only to tokens whose routed slots were all dropped,
  *     mode 1 adds x to every token;
- *   - SwiGLU (absent from the pages) is W2 (silu(W1 x) * (W3 x)), silu(z) = z/(1+e^-z).
+ *   - SwiGLU (absent from the pages) is W2 (silu(W1 x) * (W3 x)), silu(z) = z/(1+e^-z);
+ *   - noisy gating: the noisy logits replace the clean ones in every later step
+ *     (softmax, top-k, gates, balance statistic); the normal draws are an input.
  *
  * Every function here is pinned by CPU tests against values the pages print,
  * closed forms, invariants and brute force (tests/test_oracle_pins.py).
@@ -83,6 +85,30 @@ void orc_router_logits(int T, int d, int E,
             logits[(size_t)t * E + e] = s;
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1' -- noisy top-k gating (training mode).  [Arch] §2.1
+ * noisy_top_k_gating: a second linear map of the token, x W_noise, passed
+ * through softplus, scales a standard normal draw that is added to the clean
+ * logits; the noisy logits then go through the same top-k gating.  [Switch]
+ * §"代码实战" NoisyTop1Gate gives the same step with a bias on the noise
+ * projection and a floor of 1e-2 added to the softplus (min_std below; 0 for
+ * the [Arch] form), and feeds the noisy logits to softmax, argmax and the
+ * balance statistic alike.  The normal draws are an input (eps, [T,E]).
+ *   noisy[t,e] = clean[t,e] + eps[t,e] * (softplus(noise_logits[t,e]) + min_std)
+ * softplus(z) = log(1 + e^z), evaluated as max(z,0) + log1p(e^-|z|), which is
+ * the same number without overflow. */
+double orc_softplus(double z)
+{
+    return (z > 0.0 ? z : 0.0) + log1p(exp(-fabs(z)));
+}
+
+void orc_noisy_logits(int T, int E, const double* clean, const double* noise_logits,
+                      const void* eps, int eps_code, double min_std, double* noisy)
+{
+    for (size_t i = 0; i < (size_t)T * E; ++i)
+        noisy[i] = clean[i] + rd(eps, eps_code, i) * (orc_softplus(noise_logits[i]) + min_std);
 }
 
 /* ------------------------------------------------------------------------ */

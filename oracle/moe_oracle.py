@@ -61,6 +61,10 @@ def _lib():
         L.orc_capacity.argtypes = [ctypes.c_longlong, ctypes.c_longlong, dbl]
         L.orc_router_logits.restype = None
         L.orc_router_logits.argtypes = [i32, i32, i32, vp, i32, vp, i32, vp, i32, vp]
+        L.orc_softplus.restype = dbl
+        L.orc_softplus.argtypes = [dbl]
+        L.orc_noisy_logits.restype = None
+        L.orc_noisy_logits.argtypes = [i32, i32, vp, vp, vp, i32, dbl, vp]
         L.orc_softmax.restype = None
         L.orc_softmax.argtypes = [i32, i32, vp, vp]
         L.orc_topk.restype = None
@@ -137,6 +141,23 @@ def router_logits(x, Wg, bg=None) -> np.ndarray:
     E = wa.shape[0]
     out = np.empty((T, E), dtype=np.float64)
     _lib().orc_router_logits(T, d, E, _ptr(xa), xc, _ptr(wa), wc, _ptr(ba), bc, _ptr(out))
+    return out
+
+
+def softplus(z: float) -> float:
+    return float(_lib().orc_softplus(float(z)))
+
+
+def noisy_logits(clean, noise_logits, eps, min_std: float = 0.0) -> np.ndarray:
+    """clean + eps * (softplus(noise_logits) + min_std), elementwise, in fp64."""
+    ca = np.ascontiguousarray(np.asarray(clean, dtype=np.float64))
+    na = np.ascontiguousarray(np.asarray(noise_logits, dtype=np.float64))
+    ea, ec = _as_array(eps)
+    if ca.shape != na.shape or ea.shape != ca.shape:
+        raise ValueError("clean, noise_logits and eps must have the same [T,E] shape")
+    T, E = ca.shape
+    out = np.empty_like(ca)
+    _lib().orc_noisy_logits(T, E, _ptr(ca), _ptr(na), _ptr(ea), ec, float(min_std), _ptr(out))
     return out
 
 
@@ -272,15 +293,23 @@ def route_from_logits(logits, *, k: int, renormalize: bool, cf) -> Routing:
     return Routing(la, probs, idx, g, dsp.counts, dsp.pos, dsp.dropped, dsp.perm_row, a, C)
 
 
-def route(x, Wg, bg=None, *, k: int, renormalize: bool, cf) -> Routing:
-    """Steps 1-6 and the aux statistic in fp64."""
-    return route_from_logits(router_logits(x, Wg, bg), k=k, renormalize=renormalize, cf=cf)
+def route(x, Wg, bg=None, *, k: int, renormalize: bool, cf, noise=None) -> Routing:
+    """Steps 1-6 and the aux statistic in fp64.
+
+    ``noise`` = (W_noise, b_noise or None, eps, min_std) selects noisy top-k
+    gating: every later step sees the noisy logits.
+    """
+    logits = router_logits(x, Wg, bg)
+    if noise is not None:
+        Wn, bn, eps, min_std = noise
+        logits = noisy_logits(logits, router_logits(x, Wn, bn), eps, min_std)
+    return route_from_logits(logits, k=k, renormalize=renormalize, cf=cf)
 
 
 def forward(x, Wg, bg, W1, W3, W2, b1, b2, *, E: int, S: int, k: int, act_name: str,
-            renormalize: bool, cf, residual_mode: int = 0, tokens=None):
+            renormalize: bool, cf, residual_mode: int = 0, tokens=None, noise=None):
     """Whole layer in fp64: returns (y rows for ``tokens``, Routing)."""
-    r = route(x, Wg, bg, k=k, renormalize=renormalize, cf=cf)
+    r = route(x, Wg, bg, k=k, renormalize=renormalize, cf=cf, noise=noise)
     y = output_rows(x, W1, W3, W2, b1, b2, r.idx, r.gates, r.dropped, E=E, S=S,
                     act_name=act_name, residual_mode=residual_mode, tokens=tokens)
     return y, r

@@ -446,3 +446,92 @@ def test_route_from_fp32_logits_is_selection_on_those_values():
     r = orc.route_from_logits(l32, k=2, renormalize=True, cf=None)
     for t in range(50):
         assert r.idx[t].tolist() == _brute_topk(l32[t].astype(np.float64).tolist(), 2)
+
+
+# ---------------------------------------------------------------- noisy top-k gating
+
+@pytest.mark.parametrize("z", [-700.0, -50.0, -3.5, -1e-3, 0.0, 0.7, 5.0, 40.0, 700.0])
+def test_softplus_closed_form(z):
+    # softplus(z) = ln(1 + e^z), evaluated at 40 digits
+    ref = float(mp.log(1 + mp.e ** mp.mpf(z)))
+    got = orc.softplus(z)
+    if ref == 0.0:
+        assert got == 0.0 or abs(got) < 1e-300
+    else:
+        assert abs(got - ref) <= 2e-16 * abs(ref)
+
+
+def test_softplus_identities():
+    assert orc.softplus(0.0) == pytest.approx(float(mp.log(2)), rel=1e-16, abs=0)
+    for z in (-9.25, -0.5, 0.125, 3.0, 31.0):
+        # softplus(z) - softplus(-z) = z;  softplus'(z) = sigmoid(z) via a central difference
+        assert orc.softplus(z) - orc.softplus(-z) == pytest.approx(z, rel=1e-14, abs=1e-14)
+        h = 1e-6
+        deriv = (orc.softplus(z + h) - orc.softplus(z - h)) / (2 * h)
+        assert deriv == pytest.approx(1.0 / (1.0 + np.exp(-z)), rel=1e-7)
+
+
+def test_noisy_logits_zero_draws_is_clean():
+    rng = np.random.default_rng(11)
+    clean = rng.standard_normal((5, 7))
+    nl = rng.standard_normal((5, 7)) * 4
+    out = orc.noisy_logits(clean, nl, np.zeros((5, 7)), 0.01)
+    np.testing.assert_array_equal(out, clean)
+
+
+def test_noisy_logits_constant_noise_map_closed_form():
+    # W_noise = 0 and a bias b: the noise scale of expert e is softplus(b_e) + min_std,
+    # the same for every token; distinct eps values catch a transposed index
+    T, E, d = 3, 5, 4
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, d))
+    b = np.array([-2.0, -0.5, 0.0, 1.5, 6.0])
+    eps = (np.arange(T * E, dtype=np.float64).reshape(T, E) - 7.0) / 3.0
+    min_std = 0.01
+    clean = orc.router_logits(x, Wg)
+    noise_logits = orc.router_logits(x, np.zeros((E, d)), b)
+    out = orc.noisy_logits(clean, noise_logits, eps, min_std)
+    for t in range(T):
+        for e in range(E):
+            scale = float(mp.log(1 + mp.e ** mp.mpf(b[e]))) + min_std
+            assert out[t, e] == pytest.approx(clean[t, e] + eps[t, e] * scale, rel=1e-14, abs=1e-14)
+
+
+def test_noisy_route_row_constant_shift_leaves_softmax_and_choice():
+    # W_noise = 0, b_noise = 0, min_std = 0: the shift of token t is eps[t] * ln 2 on every
+    # expert; softmax is invariant to a per-row constant, so probs, top-k and aux equal the
+    # clean routing's, while the logits move by exactly eps[t] * ln 2
+    T, E, d, k = 9, 6, 5, 2
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, d))
+    c = np.linspace(-3.0, 4.0, T)
+    eps = np.repeat(c[:, None], E, axis=1)
+    base = orc.route(x, Wg, None, k=k, renormalize=True, cf=1.0)
+    noisy = orc.route(x, Wg, None, k=k, renormalize=True, cf=1.0,
+                      noise=(np.zeros((E, d)), None, eps, 0.0))
+    np.testing.assert_allclose(noisy.logits - base.logits,
+                               np.repeat((c * float(mp.log(2)))[:, None], E, axis=1), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(noisy.probs, base.probs, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(noisy.idx, base.idx)
+    np.testing.assert_array_equal(noisy.dropped, base.dropped)
+    assert noisy.aux == pytest.approx(base.aux, rel=1e-13)
+
+
+def test_noisy_route_flips_choice_by_hand():
+    # one token, logits [1, 0, -1]; noise scale softplus(-40) + 0.01 ~= 0.01 on every expert.
+    # eps = [0, 0, 250] lifts expert 2 to -1 + 2.5 = 1.5 > 1: it wins and expert 0 is second;
+    # eps = [0, 0, 150] gives 0.5 < 1: the clean order [0, 1] stays
+    x = np.array([[1.0]])
+    Wg = np.array([[1.0], [0.0], [-1.0]])
+    Wn = np.zeros((3, 1))
+    bn = np.full(3, -40.0)
+    r = orc.route(x, Wg, None, k=2, renormalize=False, cf=None,
+                  noise=(Wn, bn, np.array([[0.0, 0.0, 250.0]]), 0.01))
+    assert r.idx.tolist() == [[2, 0]]
+    assert r.logits[0, 2] == pytest.approx(-1.0 + 250.0 * (0.01 + float(mp.log(1 + mp.e ** -40))), rel=1e-14)
+    r = orc.route(x, Wg, None, k=2, renormalize=False, cf=None,
+                  noise=(Wn, bn, np.array([[0.0, 0.0, 150.0]]), 0.01))
+    assert r.idx.tolist() == [[0, 2]]
+    # the second slot is expert 2 (0.5) ahead of expert 1 (0.0)
