@@ -89,7 +89,21 @@ typedef struct {
     int32_t act;        /* moe_act_t */
     int32_t dtype;      /* moe_dtype_t */
     uint32_t flags;     /* MOE_FLAG_* */
+    int32_t noisy_gating;  /* 1: noisy top-k gating (training mode, see below); 0: off */
+    float noise_min_std;   /* floor added to the noise scale; >= 0, finite */
 } moe_params_t;
+
+/* Noisy top-k gating ([Arch] §2.1 noisy_top_k_gating; [Switch] §"代码实战"
+ * NoisyTop1Gate).  With noisy_gating = 1 the router also computes
+ *     noise_logits[t,e] = sum_i x[t,i] W_noise[e,i] + b_noise[e]     (fp32)
+ * and replaces the logits by
+ *     logits[t,e] + noise_eps[t,e] * (softplus(noise_logits[t,e]) + noise_min_std)
+ * before softmax, top-k, gates and the balance statistic, which therefore all
+ * see the noisy logits (outputs.logits holds them too).  noise_eps is a [T,E]
+ * array of standard normal draws supplied by the caller: the library draws no
+ * random numbers, so a forward is a deterministic function of its inputs.
+ * noise_min_std = 0 is the [Arch] form, 1e-2 the [Switch] one.  With
+ * noisy_gating = 0, W_noise, b_noise and noise_eps must be NULL. */
 
 typedef struct {
     const void* x;       /* [T, d] dtype */
@@ -100,6 +114,9 @@ typedef struct {
     const void* W2;      /* [E+S, d, F] dtype */
     const void* b1;      /* [E+S, F] dtype or NULL (must be NULL for SwiGLU) */
     const void* b2;      /* [E+S, d] dtype or NULL (must be NULL for SwiGLU) */
+    const float* W_noise;   /* [E, d] fp32 noise projection; required iff noisy_gating */
+    const float* b_noise;   /* [E] fp32 noise projection bias, or NULL */
+    const float* noise_eps; /* [T, E] fp32 standard normal draws; required iff noisy_gating */
 } moe_inputs_t;
 
 typedef struct {
@@ -110,7 +127,8 @@ typedef struct {
     int32_t* counts;     /* [E] tokens routed to each expert before capacity drops */
     uint8_t* dropped;    /* [T, k] 1 = slot dropped by the capacity limit */
     float* aux;          /* [1] E * sum_e (counts_e / (T k)) * (mean_t p[t,e]) */
-    float* logits;       /* [T, E] fp32 router logits, or NULL (not written) */
+    float* logits;       /* [T, E] fp32 router logits (the noisy ones under noisy gating),
+                            or NULL (not written) */
     float* probs;        /* [T, E] fp32 router probabilities, or NULL */
     int32_t* perm_row;   /* [T, k] row of the slot in the expert-contiguous, token-ascending,
                             unpadded order of kept slots; -1 if dropped; or NULL */

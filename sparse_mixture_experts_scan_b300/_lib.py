@@ -34,12 +34,14 @@ MOE_NOALLOC_MAX_SLOTS = 131072
 class moe_params_t(ctypes.Structure):
     _fields_ = [("T", _i32), ("d_model", _i32), ("d_ff", _i32), ("E", _i32), ("k", _i32),
                 ("n_shared", _i32), ("capacity_factor", _f32), ("renormalize", _i32),
-                ("residual_mode", _i32), ("act", _i32), ("dtype", _i32), ("flags", _u32)]
+                ("residual_mode", _i32), ("act", _i32), ("dtype", _i32), ("flags", _u32),
+                ("noisy_gating", _i32), ("noise_min_std", _f32)]
 
 
 class moe_inputs_t(ctypes.Structure):
     _fields_ = [("x", _vp), ("W_gate", _vp), ("b_gate", _vp), ("W1", _vp), ("W3", _vp),
-                ("W2", _vp), ("b1", _vp), ("b2", _vp)]
+                ("W2", _vp), ("b1", _vp), ("b2", _vp), ("W_noise", _vp), ("b_noise", _vp),
+                ("noise_eps", _vp)]
 
 
 class moe_outputs_t(ctypes.Structure):

@@ -31,6 +31,7 @@ struct Layout {
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
     int r_ksplits;             // router GEMM K splits
     size_t off_wsplit, off_logits;
+    size_t off_nsplit, off_nlogits;  // noisy gating: W_noise splits, noise logits [ks, T, E]
     size_t off_psum_chunk;
     size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
     int ffn_sync_n;
@@ -61,6 +62,8 @@ moe_status_t validate_params(const moe_params_t* p)
     if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER | MOE_FLAG_UNFUSED_EXPERTS)) != 0u)
         return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (p->noisy_gating != 0 && p->noisy_gating != 1) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(p->noise_min_std) || p->noise_min_std < 0.0f) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     // every index and row count below must fit in int32
     const long long slots = (long long)p->T * p->k;
@@ -105,6 +108,9 @@ Layout make_layout(const moe_params_t& p)
     };
     L.off_wsplit = take(L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
     L.off_logits = take(sizeof(float) * (size_t)L.T * L.E * (L.r_ksplits > 1 ? L.r_ksplits + 1 : 1));
+    const bool noisy = p.noisy_gating == 1;
+    L.off_nsplit = take(noisy && L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
+    L.off_nlogits = take(noisy ? sizeof(float) * (size_t)L.T * L.E * L.r_ksplits : 0);
     L.ffn_sync_n = 2 + L.rows_cap / kSegRows;
     L.off_ffn_sync = take(sizeof(unsigned) * L.ffn_sync_n);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
@@ -137,9 +143,11 @@ moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const mo
     if (swiglu && (in->b1 || in->b2)) return MOE_ERR_INVALID_ARG;
     if (!out->y || !out->expert_idx || !out->gates || !out->counts || !out->dropped || !out->aux)
         return MOE_ERR_INVALID_ARG;
+    if (p.noisy_gating == 1 ? (!in->W_noise || !in->noise_eps) : (in->W_noise || in->b_noise || in->noise_eps))
+        return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
                           out->y, out->expert_idx, out->gates, out->counts, out->dropped, out->aux,
-                          out->logits, out->probs, out->perm_row};
+                          out->logits, out->probs, out->perm_row, in->W_noise, in->b_noise, in->noise_eps};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -203,7 +211,7 @@ struct Ctx {
     bool bf16, use_tc, fused;
     bool pdl = false;  // false until this call has launched its first kernel
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
-    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW;
+    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW, mWn;
     template <typename T>
     T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
     uint32_t* err() const { return reinterpret_cast<uint32_t*>(ws); }
@@ -246,6 +254,8 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
         if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) ||
             !encode_bf16_2d(&c.mW, c.at<void>(L.off_wsplit), 3ull * L.e_pad, L.d, L.r_bn))
             return MOE_ERR_UNSUPPORTED;
+        if (c.p.noisy_gating == 1 && !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, L.r_bn))
+            return MOE_ERR_UNSUPPORTED;
     }
     if (c.use_tc) {
         const Layout& L = c.L;
@@ -287,7 +297,25 @@ moe_status_t stage_router(Ctx& c)
     a.probs = c.out->probs;
     a.psum_part = c.at<float>(c.L.off_psum);
     a.scan_done = c.scan_done();
-    if (!c.L.tc_router) return cuda_status(launch_router(a, c.bf16, c.st, take_pdl(c)));
+    const bool noisy = c.p.noisy_gating == 1;
+    if (noisy) {
+        a.noise_parts = c.at<float>(c.L.off_nlogits);
+        a.bn = c.in->b_noise;
+        a.eps = c.in->noise_eps;
+        a.min_std = c.p.noise_min_std;
+    }
+    if (!c.L.tc_router) {
+        cudaError_t e = cudaSuccess;
+        if (noisy) {  // noise projection x W_noise^T first, then the routing pass adds the noise
+            RouterArgs r = a;
+            r.Wg = c.in->W_noise;
+            r.bg = nullptr;
+            r.raw_out = c.at<float>(c.L.off_nlogits);
+            e = launch_router(r, c.bf16, c.st, take_pdl(c));
+        }
+        if (e == cudaSuccess) e = launch_router(a, c.bf16, c.st, take_pdl(c));
+        return cuda_status(e);
+    }
     // tensor-core logits into the caller's logits buffer (or the workspace), then top-k;
     // with split K, partial sums go to the workspace and the top-k kernel adds them
     if (a.logits == nullptr) a.logits = c.at<float>(c.L.off_logits);
@@ -308,6 +336,15 @@ moe_status_t stage_router(Ctx& c)
     cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
                                        take_pdl(c));
     if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
+    if (noisy) {  // the same GEMM on W_noise, without bias, into the noise-logit partials
+        RouterGemmArgs gn = g;
+        gn.bg = nullptr;
+        gn.logits = c.at<float>(c.L.off_nlogits);
+        if (e == cudaSuccess)
+            e = launch_split_wgate(c.in->W_noise, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_nsplit), c.sms, c.st,
+                                   take_pdl(c));
+        if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mWn, gn, c.L.r_bn, c.sms, c.st);
+    }
     if (e == cudaSuccess) e = launch_router_topk(a, c.st);
     return cuda_status(e);
 }

@@ -59,7 +59,7 @@ struct Vec<float> {
     }
 };
 
-template <typename T>
+template <typename T, bool SEG>
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
 {
     constexpr int V = Vec<T>::N;
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = a.d / V;
-    const int seg = a.seg_vec;  // 16-byte vectors per work item
-    const int nseg = ceil_div(nvec, seg);
+    const int seg = SEG ? a.seg_vec : nvec;  // 16-byte vectors per work item
+    const int nseg = SEG ? ceil_div(nvec, seg) : 1;
     const int items = a.T * nseg;  // < 2^31: nseg > 1 only for T < 8192
     const size_t row_bytes = (size_t)a.d * sizeof(T);
     const unsigned all_k = (a.k >= 32) ? 0xffffffffu : ((1u << a.k) - 1u);
@@ -141,8 +141,13 @@ cudaError_t launch_combine(const CombineArgs& a, bool bf16, int num_sms, cudaStr
     const long long items = (long long)a.T * ceil_div(nvec, b.seg_vec);
     long long grid = (items + 7) / 8;
     if (grid > (long long)num_sms * 32) grid = (long long)num_sms * 32;
-    if (bf16) return launch_kernel(k_combine<__nv_bfloat16>, dim3((int)grid), dim3(256), 0, st, pdl, b);
-    return launch_kernel(k_combine<float>, dim3((int)grid), dim3(256), 0, st, pdl, b);
+    const dim3 g((int)grid), blk(256);
+    if (ceil_div(nvec, b.seg_vec) > 1) {
+        if (bf16) return launch_kernel(k_combine<__nv_bfloat16, true>, g, blk, 0, st, pdl, b);
+        return launch_kernel(k_combine<float, true>, g, blk, 0, st, pdl, b);
+    }
+    if (bf16) return launch_kernel(k_combine<__nv_bfloat16, false>, g, blk, 0, st, pdl, b);
+    return launch_kernel(k_combine<float, false>, g, blk, 0, st, pdl, b);
 }
 
 }  // namespace moe

@@ -91,6 +91,9 @@ __host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { retur
 // ---------------------------------------------------------------------------
 // Scalar helpers
 
+// softplus(z) = ln(1 + e^z) as max(z, 0) + ln(1 + e^-|z|): no overflow for large z
+__device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z))); }
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

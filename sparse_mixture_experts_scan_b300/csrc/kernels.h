@@ -28,6 +28,13 @@ struct RouterArgs {
     unsigned* scan_done;  // dispatch-scan arrival counter, reset here
     const float* logit_parts;  // k_router_topk with split-K logits: [k_splits, T, E], else nullptr
     int k_splits;
+    // noisy top-k gating (eps == nullptr: off): logits += eps * (softplus(noise + bn) + min_std),
+    // noise = the sum of noise_parts[0..k_splits) ([k_splits, T, E], without bn)
+    const float* noise_parts;
+    const float* bn;      // [E] or nullptr
+    const float* eps;     // [T, E] standard normal draws
+    float min_std;
+    float* raw_out;       // k_router only: write x W^T (no bias, no routing) here and stop
 };
 int router_blocks(int T);
 // CUDA-core router: fp32 logits by FFMA, then softmax / top-k / gates.

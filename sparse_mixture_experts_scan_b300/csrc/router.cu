@@ -170,11 +170,26 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
         __syncthreads();
     }
 
-    float bias[EJ];
+    if (a.raw_out != nullptr) {  // projection only (the noise logits of noisy gating)
+#pragma unroll
+        for (int i = 0; i < kTokPerWarp; ++i) {
+            const int t = t0 + warp * kTokPerWarp + i;
+            if (t >= a.T) break;
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) {
+                const int e = lane + 32 * j;
+                if (e < a.E) a.raw_out[(size_t)t * a.E + e] = acc[i][j];
+            }
+        }
+        return;
+    }
+
+    float bias[EJ], nbias[EJ];
 #pragma unroll
     for (int j = 0; j < EJ; ++j) {
         const int e = lane + 32 * j;
         bias[j] = (a.bg != nullptr && e < a.E) ? a.bg[e] : 0.0f;
+        nbias[j] = (a.bn != nullptr && e < a.E) ? a.bn[e] : 0.0f;
     }
 
     float psum[EJ];
@@ -190,6 +205,10 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
         for (int j = 0; j < EJ; ++j) {
             const int e = lane + 32 * j;
             l[j] = (e < a.E) ? acc[i][j] + bias[j] : -INFINITY;
+            if (a.eps != nullptr && e < a.E) {
+                const size_t o = (size_t)t * a.E + e;
+                l[j] += a.eps[o] * (softplus_f32(a.noise_parts[o] + nbias[j]) + a.min_std);
+            }
         }
         route_token<EJ>(l, t, a, true, psum);
     }
@@ -200,10 +219,13 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
 
 // Softmax / top-k / gates for logits already in a.logits (computed by the
 // tensor-core router GEMM), or for the sum of split-K partial logits plus the bias.
+// NOISY: the noise of noisy top-k gating is added first ("MoE架构解析" §2.1
+// noisy_top_k_gating; "MoE 混合专家模型串讲" §"代码实战" NoisyTop1Gate), so softmax,
+// top-k, gates and the column sums all see the noisy logits, which are written out.
 // A block covers 32 tokens (the column-sum layout of k_router), WARPS warps with
 // 32 / WARPS tokens each: one token per warp when the registers allow it (E <= 256),
 // so a small batch still runs many independent warps.
-template <int EJ, int WARPS>
+template <int EJ, int WARPS, bool NOISY>
 __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
 {
     constexpr int TPW = kRouterTokens / WARPS;  // tokens per warp
@@ -246,11 +268,39 @@ __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
                 if (a.bg != nullptr && e < a.E) l[i][j] += a.bg[e];
             }
     }
+    if constexpr (NOISY) {
+        // noise logits: split-K partials in K order, then the bias; then the noisy logits
+        float nz[TPW][EJ];
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) nz[i][j] = 0.0f;
+        for (int ks = 0; ks < a.k_splits; ++ks) {
+            const float* part = a.noise_parts + (size_t)ks * a.T * a.E;
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                for (int j = 0; j < EJ; ++j) {
+                    const int t = t0 + warp * TPW + i, e = lane + 32 * j;
+                    if (t < a.T && e < a.E) nz[i][j] += part[(size_t)t * a.E + e];
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < EJ; ++j) {
+                const int t = t0 + warp * TPW + i, e = lane + 32 * j;
+                if (t < a.T && e < a.E) {
+                    const float z = nz[i][j] + (a.bn != nullptr ? a.bn[e] : 0.0f);
+                    l[i][j] += a.eps[(size_t)t * a.E + e] * (softplus_f32(z) + a.min_std);
+                }
+            }
+    }
 #pragma unroll
     for (int i = 0; i < TPW; ++i) {
         const int t = t0 + warp * TPW + i;
         if (t >= a.T) break;  // warp-uniform
-        route_token<EJ>(l[i], t, a, a.logit_parts != nullptr, psum);
+        route_token<EJ>(l[i], t, a, NOISY || a.logit_parts != nullptr, psum);
     }
     block_psum<EJ, WARPS>(psum, scratch, a);
 }
@@ -270,8 +320,9 @@ template <int EJ>
 cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
 {
     constexpr int WARPS = EJ <= 8 ? 32 : 8;
-    return launch_kernel(k_router_topk<EJ, WARPS>, dim3(ceil_div(a.T, kRouterTokens)), dim3(WARPS * 32), 0, st,
-                         true, a);
+    const dim3 grid(ceil_div(a.T, kRouterTokens)), block(WARPS * 32);
+    if (a.eps != nullptr) return launch_kernel(k_router_topk<EJ, WARPS, true>, grid, block, 0, st, true, a);
+    return launch_kernel(k_router_topk<EJ, WARPS, false>, grid, block, 0, st, true, a);
 }
 
 }  // namespace

@@ -19,6 +19,11 @@ Configurations (shapes and distributions of the workloads the pages discuss):
             permutation), so the bias alone gives Zipf(1.2) expert popularity
   decode    the first 64 tokens of skewed with the same weights (capacity 1.0 -> C = 0)
   decode_nocap  the same without a capacity limit
+
+Noisy top-k gating (any config with noisy=True): after the tensors above, W_noise
+is drawn like W_gate, b_noise ~ N(0,1) (noise scales softplus(b) from about 0.1 to
+2.1) and noise_eps ~ N(0,1) of shape [T, E] (the standard normal draws the gate
+scales); for a config with a parent, the first T rows of the parent's draws.
 """
 from __future__ import annotations
 
@@ -46,6 +51,8 @@ class LayerConfig:
     init: str = "fan_in"         # small | trunc | fan_in
     zipf: float | None = None    # router-bias Zipf exponent
     parent: str | None = None    # take the first T tokens of this config's inputs
+    noisy: bool = False          # noisy top-k gating (training mode)
+    noise_min_std: float = 0.0   # floor added to the softplus noise scale
 
     @property
     def torch_dtype(self):
@@ -92,9 +99,11 @@ def _trunc(shape, std, g, device):
 def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> dict:
     """Seeded tensors for `cfg` on `device` (weights of all E + S experts)."""
     if cfg.parent is not None:
-        base = make_inputs(replace(CONFIGS[cfg.parent], d=cfg.d, E=cfg.E, k=cfg.k, F=cfg.F),
-                           seed, device)
+        base = make_inputs(replace(CONFIGS[cfg.parent], d=cfg.d, E=cfg.E, k=cfg.k, F=cfg.F,
+                                   noisy=cfg.noisy), seed, device)
         base["x"] = base["x"][: cfg.T].contiguous()
+        if cfg.noisy:
+            base["noise_eps"] = base["noise_eps"][: cfg.T].contiguous()
         return base
     g = torch.Generator(device=device).manual_seed(seed)
     T, d, E, F, S = cfg.T, cfg.d, cfg.E, cfg.F, cfg.S
@@ -128,4 +137,11 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> dict:
     out["W2"] = w((ES, d, F), F).to(dt)
     out["b1"] = torch.zeros(ES, F, device=device, dtype=dt) if cfg.bias else None
     out["b2"] = torch.zeros(ES, d, device=device, dtype=dt) if cfg.bias else None
+    if cfg.noisy:
+        out["W_noise"] = (_trunc((E, d), math.sqrt(0.1 / d), g, device) if wg_std is None
+                          else _normal((E, d), wg_std, g, device))
+        out["b_noise"] = _normal((E,), 1.0, g, device)
+        out["noise_eps"] = _normal((T, E), 1.0, g, device)
+    else:
+        out["W_noise"] = out["b_noise"] = out["noise_eps"] = None
     return out

@@ -33,7 +33,7 @@ def make_params(cfg: LayerConfig, *, flags: int = 0, residual_mode: int | None =
         renormalize=int(cfg.renormalize),
         residual_mode=cfg.residual_mode if residual_mode is None else residual_mode,
         act=ACT_CODES[cfg.act], dtype=_lib.MOE_BF16 if cfg.dtype == "bf16" else _lib.MOE_F32,
-        flags=flags)
+        flags=flags, noisy_gating=int(cfg.noisy), noise_min_std=float(cfg.noise_min_std))
 
 
 def _ptr(t):
@@ -79,7 +79,9 @@ class MoELayer:
         w = self.weights
         self.inputs = _lib.moe_inputs_t(
             x=_ptr(w["x"]), W_gate=_ptr(w["W_gate"]), b_gate=_ptr(w.get("b_gate")), W1=_ptr(w["W1"]),
-            W3=_ptr(w.get("W3")), W2=_ptr(w["W2"]), b1=_ptr(w.get("b1")), b2=_ptr(w.get("b2")))
+            W3=_ptr(w.get("W3")), W2=_ptr(w["W2"]), b1=_ptr(w.get("b1")), b2=_ptr(w.get("b2")),
+            W_noise=_ptr(w.get("W_noise")), b_noise=_ptr(w.get("b_noise")),
+            noise_eps=_ptr(w.get("noise_eps")))
         o = self.out
         self.outputs = _lib.moe_outputs_t(
             y=_ptr(o["y"]), expert_idx=_ptr(o["expert_idx"]), gates=_ptr(o["gates"]),

@@ -4,6 +4,8 @@ compare it with the fp64 CPU oracle on the same seeded inputs.
 Bars (per the layer's specification):
   - expert indices, counts, capacity drops and permutation rows: bit-exact
     against the oracle's selection re-run on the device's fp32 logits;
+  - noisy top-k gating: the noisy logits within 1e-5 * max(1, max |eps|) absolute
+    of the fp64 oracle's (fp32 accumulation of two d-long projections);
   - router probabilities and gates: <= 1e-5 absolute against the fp64 oracle
     (tokens whose k-th and (k+1)-th fp64 probabilities are within 1e-6 are
     excluded from the index comparison against the oracle's own selection, and
@@ -20,6 +22,7 @@ from oracle import moe_oracle as orc
 from sparse_mixture_experts_scan_b300 import MoELayer, _lib
 
 PROB_TOL = 1e-5
+LOGIT_TOL = 1e-5
 NEAR_TIE = 1e-6
 Y_TOL = {"bf16": 2e-2, "f32": 1e-4}
 
@@ -56,7 +59,12 @@ def check_routing_bitexact(cfg, out: dict):
 def check_router_vs_fp64(cfg, inp: dict, out: dict) -> int:
     """Probabilities, gates, selection and aux against the fp64 oracle; returns near-tie count."""
     r64 = orc.route(inp["x"], inp["W_gate"], inp["b_gate"], k=cfg.k, renormalize=cfg.renormalize,
-                    cf=cfg.cf)
+                    cf=cfg.cf, noise=oracle_noise(cfg, inp))
+    if cfg.noisy:
+        # noisy logits: fp32 accumulation of the two projections; the noise term scales the
+        # projection error by |eps| (a few units for normal draws)
+        tol = LOGIT_TOL * max(1.0, float(np.abs(inp["noise_eps"].double().numpy()).max()))
+        assert np.abs(out["logits"].double().numpy() - r64.logits).max() <= tol
     p_dev = out["probs"].double().numpy()
     assert np.abs(p_dev - r64.probs).max() <= PROB_TOL
     E = cfg.E
@@ -70,6 +78,13 @@ def check_router_vs_fp64(cfg, inp: dict, out: dict) -> int:
     aux_dev = float(out["aux"][0])
     assert abs(aux_dev - r64.aux) <= 1e-5 * max(1.0, abs(r64.aux)), (aux_dev, r64.aux)
     return int(near.sum())
+
+
+def oracle_noise(cfg, inp: dict):
+    """The oracle's noise argument for noisy top-k gating, or None."""
+    if not cfg.noisy:
+        return None
+    return (inp["W_noise"], inp["b_noise"], inp["noise_eps"], cfg.noise_min_std)
 
 
 def oracle_rows(cfg, inp: dict, r, tokens, residual_mode=None):

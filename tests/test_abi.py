@@ -24,9 +24,9 @@ def test_status_strings():
 
 
 def test_struct_layouts_match_header():
-    # moe_params_t: 11 int32/float fields + uint32 flags
-    assert ctypes.sizeof(_lib.moe_params_t) == 12 * 4
-    assert ctypes.sizeof(_lib.moe_inputs_t) == 8 * 8
+    # moe_params_t: 11 int32/float fields, uint32 flags, noisy_gating, noise_min_std
+    assert ctypes.sizeof(_lib.moe_params_t) == 14 * 4
+    assert ctypes.sizeof(_lib.moe_inputs_t) == 11 * 8
     assert ctypes.sizeof(_lib.moe_outputs_t) == 9 * 8
 
 
@@ -125,3 +125,47 @@ def test_relu_layer_rejects_w3_and_swiglu_rejects_biases():
     ins2.b1 = ins2.W1
     _, need2 = _lib.moe_workspace_size(p2)
     assert _lib.moe_forward(p2, ins2, outs2, 1 << 44, need2, None) == _lib.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value", [("noisy_gating", 2), ("noisy_gating", -1),
+                                         ("noise_min_std", -0.5), ("noise_min_std", float("nan")),
+                                         ("noise_min_std", float("inf"))])
+def test_invalid_noise_params_rejected(field, value):
+    p = make_params(config("switch", noisy=True))
+    setattr(p, field, value)
+    assert _lib.moe_workspace_size(p)[0] == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_noisy_gating_needs_more_workspace():
+    for name in ("switch", "tiny", "router_split"):
+        cfg = config("skewed", T=64, d=2048, E=64, k=4, cf=None) if name == "router_split" else config(name)
+        st0, n0 = _lib.moe_workspace_size(make_params(cfg))
+        st1, n1 = _lib.moe_workspace_size(make_params(cfg.__class__(**{**cfg.__dict__, "noisy": True})))
+        assert st0 == st1 == _lib.MOE_OK
+        assert n1 >= n0 + 4 * cfg.T * cfg.E  # at least the [T, E] noise logits
+
+
+def test_noise_pointers_must_match_the_mode():
+    base = 1 << 40
+    for noisy in (False, True):
+        cfg = config("switch", noisy=noisy)
+        p = make_params(cfg)
+        _, need = _lib.moe_workspace_size(p)
+        cases = []
+        if noisy:
+            for missing in ("W_noise", "noise_eps"):
+                ins, outs = _fake_io(cfg)
+                ins.W_noise, ins.noise_eps = base + 20 * (1 << 30), base + 21 * (1 << 30)
+                setattr(ins, missing, None)
+                cases.append((ins, outs))
+            ins, outs = _fake_io(cfg)
+            ins.W_noise, ins.noise_eps = base + 20 * (1 << 30) + 4, base + 21 * (1 << 30)  # unaligned
+            cases.append((ins, outs))
+        else:
+            for extra in ("W_noise", "b_noise", "noise_eps"):
+                ins, outs = _fake_io(cfg)
+                setattr(ins, extra, base + 22 * (1 << 30))
+                cases.append((ins, outs))
+        for ins, outs in cases:
+            for stage in ("moe_forward", "moe_router"):
+                assert getattr(_lib, stage)(p, ins, outs, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG

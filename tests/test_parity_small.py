@@ -2,6 +2,8 @@
 output element, for each kernel path (tcgen05 and FFMA experts), plus the edge
 cases of the method (ragged sizes, k = E, one expert, capacity 0, exact ties,
 all tokens on one expert, shared experts, biases, residual modes)."""
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -219,3 +221,55 @@ def test_nan_tokens_route_to_valid_experts():
     r = orc.route_from_logits(out["logits"].numpy(), k=cfg.k, renormalize=cfg.renormalize, cf=cfg.cf)
     from parity_utils import check_output
     check_output(cfg, to_cpu(inp), out, r, tokens=good)
+
+
+# ---------------------------------------------------------------- noisy top-k gating
+
+NOISY = {
+    "noisy_switch_k1": _case("switch", T=1000, d=256, E=32, k=1, F=384, cf=1.25, noisy=True,
+                             noise_min_std=0.01),
+    "noisy_top2_renorm": _case("mixtral", T=300, d=256, E=8, k=2, F=512, noisy=True),
+    "noisy_router_split_k": _case("skewed", T=64, d=2048, E=64, k=4, F=128, cf=None, noisy=True),
+    "noisy_many_experts_drops": _case("skewed", T=512, d=128, E=256, k=8, F=128, noisy=True),
+    "noisy_max_experts": _case("mixtral", T=256, d=64, E=512, k=4, F=64, noisy=True),
+    "noisy_fp32": config("tiny", noisy=True, noise_min_std=0.01),
+}
+_NOISE_KEYS = ("W_noise", "b_noise", "noise_eps")
+
+
+@pytest.mark.parametrize("name", sorted(NOISY))
+def test_noisy_gating_matches_oracle(name):
+    cfg = NOISY[name]
+    _full_check(cfg, _inputs(cfg, random_bias=True))
+
+
+@pytest.mark.parametrize("name", ["noisy_switch_k1", "noisy_router_split_k", "noisy_max_experts"])
+def test_noisy_gating_ffma_router_matches_oracle(name):
+    cfg = NOISY[name]
+    _full_check(cfg, _inputs(cfg), flags=_lib.MOE_FLAG_FFMA_ROUTER)
+
+
+@pytest.mark.parametrize("name", ["noisy_switch_k1", "noisy_router_split_k", "noisy_fp32"])
+def test_noisy_gating_with_zero_draws_equals_clean_bitwise(name):
+    # eps = 0: the noisy logits are the clean ones exactly (x + 0 * s = x), so every
+    # output equals the run without noisy gating bit for bit
+    cfg = NOISY[name]
+    inp = _inputs(cfg)
+    inp["noise_eps"] = torch.zeros_like(inp["noise_eps"])
+    noisy = run_device(cfg, inp)
+    clean_cfg = replace(cfg, noisy=False)
+    clean = run_device(clean_cfg, {k: v for k, v in inp.items() if k not in _NOISE_KEYS})
+    for key in ("logits", "probs", "expert_idx", "gates", "counts", "dropped", "aux", "perm_row", "y"):
+        assert torch.equal(noisy[key], clean[key]), key
+
+
+def test_noisy_gating_moves_the_selection():
+    # with unit normal draws a sizeable share of top-1 choices moves, and only where the
+    # oracle's noisy logits say so (checked in full by the parity test above)
+    cfg = NOISY["noisy_switch_k1"]
+    inp = _inputs(cfg)
+    noisy = run_device(cfg, inp)
+    clean_cfg = replace(cfg, noisy=False)
+    clean = run_device(clean_cfg, {k: v for k, v in inp.items() if k not in _NOISE_KEYS})
+    moved = (noisy["expert_idx"] != clean["expert_idx"]).any(dim=1).float().mean().item()
+    assert 0.05 < moved < 1.0, moved
