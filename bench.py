@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--noisy", action="store_true",
+                    help="noisy top-k gating (training-mode router; noise floor 0.01)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each stage directly instead of replaying a captured CUDA graph")
     return ap.parse_args()
@@ -54,8 +56,16 @@ def parse_args():
 def workload_name(cfg) -> str:
     cap = "none" if cfg.cf is None else f"{cfg.cf:g}"
     shared = f"+{cfg.S}shared" if cfg.S else ""
+    noisy = f", noisy top-k gating (noise floor {cfg.noise_min_std:g})" if cfg.noisy else ""
     return (f"{cfg.name} MoE FFN layer: T={cfg.T} d_model={cfg.d} E={cfg.E}{shared} k={cfg.k} "
-            f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts, fp32 router")
+            f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts, fp32 router{noisy}")
+
+
+def bench_config(args):
+    from sparse_mixture_experts_scan_b300 import config
+    if args.noisy:
+        return config(args.config, noisy=True, noise_min_std=0.01)
+    return config(args.config)
 
 
 def peaks():
@@ -206,8 +216,10 @@ def oracle_step(cfg, cpu_inp, n_sample: int, seed: int = 7):
     from oracle import moe_oracle as orc
 
     t0 = time.perf_counter()
+    noise = ((cpu_inp["W_noise"], cpu_inp["b_noise"], cpu_inp["noise_eps"], cfg.noise_min_std)
+             if cfg.noisy else None)
     r = orc.route(cpu_inp["x"], cpu_inp["W_gate"], cpu_inp["b_gate"], k=cfg.k,
-                  renormalize=cfg.renormalize, cf=cfg.cf)
+                  renormalize=cfg.renormalize, cf=cfg.cf, noise=noise)
     t_route = time.perf_counter() - t0
     rng = np.random.default_rng(seed)
     tok = np.sort(rng.choice(cfg.T, size=min(n_sample, cfg.T), replace=False))
@@ -230,9 +242,9 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    from sparse_mixture_experts_scan_b300 import config, make_inputs
+    from sparse_mixture_experts_scan_b300 import make_inputs
 
-    cfg = config(args.config)
+    cfg = bench_config(args)
     inp = make_inputs(cfg, 0, device="cpu")
     # size the per-step token sample so that warm-up + timed steps take ~2 minutes
     t0 = time.perf_counter()
@@ -297,6 +309,8 @@ def stage_bytes(cfg, out, gemm):
     T, d, k, E = cfg.T, cfg.d, cfg.k, cfg.E
     rows = gemm["kept_rows"]
     router = T * d * esz + E * d * 4 + T * k * 8
+    if cfg.noisy:
+        router += E * d * 4 + T * E * 4  # W_noise and the normal draws
     dispatch = T * k * 4 + rows * d * esz * 2 + T * k * (1 + 4 + 4)
     pass_tok = int((out["dropped"].bool().all(dim=1)).sum()) if cfg.residual_mode == 0 else T
     combine = rows * d * esz + T * d * esz + pass_tok * d * esz + T * k * 8 + \
@@ -325,14 +339,14 @@ def run_gpu(args):
     import torch
     import torch.distributed as dist
 
-    from sparse_mixture_experts_scan_b300 import MoELayer, config, make_inputs
+    from sparse_mixture_experts_scan_b300 import MoELayer, _lib, make_inputs
 
     world, rank, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    cfg = config(args.config)
+    cfg = bench_config(args)
     inp = make_inputs(cfg, seed=rank, device=dev)
     layer = MoELayer(cfg, inp, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -352,18 +366,23 @@ def run_gpu(args):
     def full_step():
         layer.run("moe_forward", stream)
 
+    n_launch0 = _lib.moe_kernel_launches()
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
         full_step()
     torch.cuda.synchronize()
+    # kernels one moe_forward enqueues, from the library's own launch counter
+    launches_per_step = (_lib.moe_kernel_launches() - n_launch0) // max(args.warmup, 1)
 
     if not args.no_graph:
         # CUDA graphs of the library's calls (it only enqueues kernels, so it is
         # capturable): one of the whole forward (kernels chained by programmatic
         # dependent launch) and one per stage for the stage breakdown
         g_full = torch.cuda.CUDAGraph()
+        n_launch0 = _lib.moe_kernel_launches()
         with torch.cuda.graph(g_full):
             layer.run("moe_forward")
+        launches_per_step = _lib.moe_kernel_launches() - n_launch0  # kernels in the replayed graph
         g_stage = []
         for st_name in stages:
             g = torch.cuda.CUDAGraph()
@@ -448,7 +467,7 @@ def run_gpu(args):
         achieved = gemm["flops"] / (g_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16_tflops"]}
-    wl_key = args.config
+    wl_key = args.config + ("_noisy" if cfg.noisy else "")
     fused = cfg.dtype == "bf16"
     tr = traffic_from_profiles("ffn_fused_tc.cu" if fused else "grouped_gemm_ffma.cu", wl_key)
     kname = ("moe_grouped_gemm stage: k_ffn_fused_tc (both expert layers, one persistent tcgen05 launch)"
@@ -468,10 +487,6 @@ def run_gpu(args):
         mem_stages[s] = {"ms": stage_ms[s], "bytes": sbytes[s], "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]}
     rdc_bytes = sum(sbytes.values())
     rdc_ms = sum(stage_ms[s] for s in ("moe_router", "moe_dispatch", "moe_combine"))
-
-    # router 1, dispatch 2 (scan, permute), GEMM1+GEMM2 unless capacity is 0, shared 2, combine 1
-    cap_zero = cfg.cf is not None and int(cfg.T * cfg.cf / cfg.E) == 0
-    launches_per_step = 1 + 2 + (0 if cap_zero else 2) + (2 if cfg.S else 0) + 1
 
     # ---- end to end through the public API with host buffers: every step copies its x
     # from pinned host memory to the device, runs the layer, and copies y and aux back.

@@ -220,6 +220,13 @@ moe_status_t moe_dispatch_positions_noalloc(const moe_params_t* params,
                                             const int32_t* expert_idx, int32_t* counts,
                                             uint8_t* dropped, int32_t* perm_row, void* stream);
 
+/* Number of kernels this library has launched in this process since it was
+ * loaded, counting launches recorded into a CUDA graph under stream capture
+ * (a graph replay launches no kernel through the library and counts nothing).
+ * The difference across one call is the number of kernels that call enqueues.
+ * Host-side counter; needs no device. */
+uint64_t moe_kernel_launches(void);
+
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 

@@ -81,6 +81,8 @@ def load(build_if_stale: bool = True):
     L.moe_last_device_status.argtypes = [_vp, ctypes.c_size_t, _vp]
     L.moe_dispatch_positions_noalloc.restype = _i32
     L.moe_dispatch_positions_noalloc.argtypes = [_P(moe_params_t), _vp, _vp, _vp, _vp, _vp]
+    L.moe_kernel_launches.restype = ctypes.c_uint64
+    L.moe_kernel_launches.argtypes = []
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_status_string.argtypes = [_i32]
     _handle = L
@@ -92,7 +94,7 @@ def header_functions() -> list[str]:
     path = os.path.join(_build.INCLUDE, "moe.h")
     with open(path) as f:
         text = f.read()
-    return re.findall(r"^\s*(?:const\s+char\s*\*|moe_status_t)\s+(moe_\w+)\s*\(", text, re.M)
+    return re.findall(r"^\s*(?:const\s+char\s*\*|moe_status_t|uint64_t)\s+(moe_\w+)\s*\(", text, re.M)
 
 
 # ---- the C entry points, same names ---------------------------------------
@@ -136,6 +138,10 @@ def moe_dispatch_positions_noalloc(params, expert_idx, counts, dropped, perm_row
 
 def moe_last_device_status(workspace, workspace_bytes, stream):
     return load().moe_last_device_status(_vp(workspace), ctypes.c_size_t(workspace_bytes), _vp(stream))
+
+
+def moe_kernel_launches() -> int:
+    return int(load().moe_kernel_launches())
 
 
 def moe_status_string(status: int) -> str:

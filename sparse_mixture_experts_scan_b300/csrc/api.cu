@@ -15,6 +15,13 @@
 #include "moe.h"
 
 namespace moe {
+
+std::atomic<unsigned long long>& launch_counter()
+{
+    static std::atomic<unsigned long long> n{0};
+    return n;
+}
+
 namespace {
 
 constexpr size_t kRegionAlign = 1024;
@@ -602,6 +609,8 @@ moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, voi
     }
     return MOE_OK;
 }
+
+uint64_t moe_kernel_launches(void) { return moe::launch_counter().load(std::memory_order_relaxed); }
 
 const char* moe_status_string(moe_status_t status)
 {

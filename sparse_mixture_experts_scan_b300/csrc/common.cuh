@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -54,6 +55,10 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Kernels launched (or recorded into a CUDA graph under stream capture) by this
+// library since it was loaded; read through moe_kernel_launches().
+std::atomic<unsigned long long>& launch_counter();
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                                  bool pdl, Args&&... args)
@@ -68,7 +73,9 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+    return e;
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device); later

@@ -299,8 +299,7 @@ cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st)
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k_dispatch_scan), smem);
         if (e != cudaSuccess) return e;
     }
-    k_dispatch_scan<<<a.nchunks, 1024, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_dispatch_scan, dim3(a.nchunks), dim3(1024), smem, st, false, a);
 }
 
 }  // namespace moe

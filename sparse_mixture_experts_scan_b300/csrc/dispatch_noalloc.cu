@@ -140,6 +140,6 @@ extern "C" moe_status_t moe_dispatch_positions_noalloc(const moe_params_t* param
     if (launch_dispatch_scan_only(a, st) != cudaSuccess) return MOE_ERR_CUDA;
     const long long n_slots = (long long)p.T * p.k;
     const int grid = (int)((n_slots + 255) / 256 < 4096 ? (n_slots + 255) / 256 : 4096);
-    k_positions_noalloc<<<grid, 256, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_kernel(k_positions_noalloc, dim3(grid), dim3(256), 0, st, false, a) == cudaSuccess ? MOE_OK
+                                                                                          : MOE_ERR_CUDA;
 }

@@ -11,7 +11,8 @@ def test_library_exports_every_header_function():
     names = _lib.header_functions()
     assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
-                          "moe_status_string", "moe_dispatch_positions_noalloc"}
+                          "moe_status_string", "moe_dispatch_positions_noalloc",
+                          "moe_kernel_launches"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -169,3 +170,13 @@ def test_noise_pointers_must_match_the_mode():
         for ins, outs in cases:
             for stage in ("moe_forward", "moe_router"):
                 assert getattr(_lib, stage)(p, ins, outs, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_launch_counter_does_not_move_on_rejected_calls():
+    n0 = _lib.moe_kernel_launches()
+    cfg = config("mixtral")
+    p = make_params(cfg)
+    p.k = 0
+    ins, outs = _fake_io(cfg)
+    assert _lib.moe_forward(p, ins, outs, 1 << 44, 1 << 30, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0
