@@ -30,7 +30,9 @@
  *     (softmax, top-k, gates, balance statistic); the normal draws are an input.
  *
  * Every function here is pinned by CPU tests against values the pages print,
- * closed forms, invariants and brute force (tests/test_oracle_pins.py).
+ * closed forms, invariants and brute force (tests/test_oracle_pins.py); the
+ * backward pass against finite differences of the forward and the dense-MLP
+ * special case (tests/test_oracle_backward_pins.py).
  */
 #include <math.h>
 #include <stdint.h>
@@ -351,4 +353,298 @@ int orc_num_threads(void)
         }
     }
     return n;
+}
+
+/* ======================================================================== */
+/* Backward pass (training).  [Intro] §3.4-§3.5 trains the layer end to end:
+ * total_loss = task_loss + coef * aux_loss, then total_loss.backward().
+ * [Switch] §"负载均衡损失函数": in N * sum_i f_i P_i only P_i (the mean router
+ * probability) is differentiable; f_i counts an argmax and is not.  The
+ * discrete decisions (the top-k choice, capacity drops, pass-through) are
+ * held fixed: gradients reach the router only through the gate values and
+ * P_i, as automatic differentiation of the listings' forward would give.
+ *
+ * Given dy = dL/dy [T,d] and d_aux = dL/d aux, this returns dL/d of every
+ * input: x, W_gate, b_gate, W1, W3, W2, b1, b2 and, under noisy gating,
+ * W_noise and b_noise (the normal draws are data, not parameters).  The
+ * forward quantities are recomputed here in double precision from the
+ * inputs; idx and dropped are the forward's decisions. */
+
+/* d act / dz, from the definitions of act_fn (silu for SwiGLU). */
+static double act_grad(int act, double z)
+{
+    switch (act) {
+    case ORC_RELU: return z > 0.0 ? 1.0 : 0.0; /* the subgradient 0 at z = 0 */
+    case ORC_GELU_TANH: {
+        const double c = sqrt(2.0 / M_PI), a = 0.044715;
+        const double th = tanh(c * (z + a * z * z * z));
+        return 0.5 * (1.0 + th) + 0.5 * z * (1.0 - th * th) * c * (1.0 + 3.0 * a * z * z);
+    }
+    case ORC_GELU_ERF:
+        return 0.5 * (1.0 + erf(z / sqrt(2.0))) + z * exp(-0.5 * z * z) / sqrt(2.0 * M_PI);
+    default: {
+        const double s = 1.0 / (1.0 + exp(-z));
+        return s * (1.0 + z * (1.0 - s));
+    }
+    }
+}
+
+double orc_act_grad(int act, double z) { return act_grad(act, z); }
+
+/* Router quantities of token t in double: clean logits l, noise logits n and
+ * the logits the gating used (lg = l, or l + eps * (softplus(n) + min_std)). */
+static void router_row(int d, int E, long t, const void* x, int xc, const void* wg, int wgc,
+                       const void* bg, int bgc, const void* wn, const void* bn, const void* eps,
+                       int nc, double min_std, double* l, double* n, double* lg)
+{
+    for (int e = 0; e < E; ++e) {
+        double s = 0.0, u = 0.0;
+        for (int i = 0; i < d; ++i) {
+            const double xv = rd(x, xc, (size_t)t * d + i);
+            s += xv * rd(wg, wgc, (size_t)e * d + i);
+            if (wn) u += xv * rd(wn, nc, (size_t)e * d + i);
+        }
+        if (bg) s += rd(bg, bgc, (size_t)e);
+        if (wn && bn) u += rd(bn, nc, (size_t)e);
+        l[e] = s;
+        n[e] = u;
+        lg[e] = wn ? s + rd(eps, nc, (size_t)t * E + e) * (orc_softplus(u) + min_std) : s;
+    }
+}
+
+void orc_backward(int T, int d, int F, int E, int S, int k, int act, int renormalize, int residual_mode,
+                  const void* x, int x_code, const void* wg, int wg_code, const void* bg, int bg_code,
+                  const void* W1, const void* W3, const void* W2, int w_code,
+                  const void* b1, const void* b2, int b_code,
+                  const void* wn, const void* bn, const void* eps, int n_code, double min_std,
+                  const int32_t* idx, const uint8_t* dropped, const double* dy, double d_aux,
+                  double* dx, double* dwg, double* dbg, double* dw1, double* dw3, double* dw2,
+                  double* db1, double* db2, double* dwn, double* dbn)
+{
+    const int ES = E + S;
+    const size_t slots = (size_t)T * k;
+    /* gradient reaching each routed slot's gate, and each slot's input gradient */
+    double* dg = (double*)calloc(slots, sizeof(double));
+    double* dx_slot = (double*)calloc((slots + (size_t)T * S) * d, sizeof(double));
+    double* gate = (double*)malloc(sizeof(double) * slots);
+    double* probs = (double*)malloc(sizeof(double) * (size_t)T * E);
+    double* nlog = (double*)malloc(sizeof(double) * (size_t)T * E);
+    double* dl = (double*)calloc((size_t)T * E, sizeof(double));
+    double* dn = (double*)calloc((size_t)T * E, sizeof(double));
+    long long* counts = (long long*)calloc((size_t)E, sizeof(long long));
+
+    /* forward router: probabilities and gates ([Basic] softmax, [Intro] §3.3 gates) */
+    #pragma omp parallel
+    {
+        double* l = (double*)malloc(sizeof(double) * (size_t)E);
+        double* lg = (double*)malloc(sizeof(double) * (size_t)E);
+        #pragma omp for schedule(static)
+        for (long t = 0; t < T; ++t) {
+            router_row(d, E, t, x, x_code, wg, wg_code, bg, bg_code, wn, bn, eps, n_code, min_std, l,
+                       nlog + (size_t)t * E, lg);
+            double m = lg[0], den = 0.0;
+            for (int e = 1; e < E; ++e)
+                if (lg[e] > m) m = lg[e];
+            for (int e = 0; e < E; ++e) den += exp(lg[e] - m);
+            double* p = probs + (size_t)t * E;
+            for (int e = 0; e < E; ++e) p[e] = exp(lg[e] - m) / den;
+            double sel = 0.0;
+            for (int j = 0; j < k; ++j) sel += p[idx[(size_t)t * k + j]];
+            for (int j = 0; j < k; ++j) {
+                const double pj = p[idx[(size_t)t * k + j]];
+                gate[(size_t)t * k + j] = renormalize ? pj / sel : pj;
+            }
+        }
+        free(l);
+        free(lg);
+    }
+    for (size_t s = 0; s < slots; ++s) counts[idx[s]]++;
+
+    /* experts, one at a time in parallel: every weight gradient of expert e is
+     * private to its iteration.  do = gate * dy (gate 1 for shared experts). */
+    memset(dw1, 0, sizeof(double) * (size_t)ES * F * d);
+    if (dw3) memset(dw3, 0, sizeof(double) * (size_t)ES * F * d);
+    memset(dw2, 0, sizeof(double) * (size_t)ES * d * F);
+    if (db1) memset(db1, 0, sizeof(double) * (size_t)ES * F);
+    if (db2) memset(db2, 0, sizeof(double) * (size_t)ES * d);
+    #pragma omp parallel
+    {
+        double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+        double* z1 = (double*)malloc(sizeof(double) * (size_t)F);
+        double* z3 = (double*)malloc(sizeof(double) * (size_t)F);
+        double* h = (double*)malloc(sizeof(double) * (size_t)F);
+        double* dh = (double*)malloc(sizeof(double) * (size_t)F);
+        double* dz1 = (double*)malloc(sizeof(double) * (size_t)F);
+        double* dz3 = (double*)malloc(sizeof(double) * (size_t)F);
+        double* dout = (double*)malloc(sizeof(double) * (size_t)d);
+        #pragma omp for schedule(dynamic, 1)
+        for (long e = 0; e < ES; ++e) {
+            const int shared = e >= E;
+            const size_t w1o = (size_t)e * F * d, w2o = (size_t)e * d * F;
+            for (size_t s = 0; s < (shared ? (size_t)T : slots); ++s) {
+                const long t = shared ? (long)s : (long)(s / k);
+                if (!shared && (idx[s] != e || dropped[s])) continue;
+                for (int i = 0; i < d; ++i) xr[i] = rd(x, x_code, (size_t)t * d + i);
+                /* forward of the expert on this token */
+                for (int f = 0; f < F; ++f) {
+                    double a = 0.0, b = 0.0;
+                    for (int i = 0; i < d; ++i) {
+                        a += rd(W1, w_code, w1o + (size_t)f * d + i) * xr[i];
+                        if (act == ORC_SWIGLU) b += rd(W3, w_code, w1o + (size_t)f * d + i) * xr[i];
+                    }
+                    if (b1) a += rd(b1, b_code, (size_t)e * F + f);
+                    z1[f] = a;
+                    z3[f] = b;
+                    h[f] = act == ORC_SWIGLU ? act_fn(ORC_SWIGLU, a) * b : act_fn(act, a);
+                }
+                const double g = shared ? 1.0 : gate[s];
+                const double* dyr = dy + (size_t)t * d;
+                if (!shared) {
+                    /* dL/dgate = <dy, expert output> */
+                    double acc = 0.0;
+                    for (int o = 0; o < d; ++o) {
+                        double out = 0.0;
+                        for (int f = 0; f < F; ++f) out += rd(W2, w_code, w2o + (size_t)o * F + f) * h[f];
+                        if (b2) out += rd(b2, b_code, (size_t)e * d + o);
+                        acc += dyr[o] * out;
+                    }
+                    dg[s] = acc;
+                }
+                for (int o = 0; o < d; ++o) dout[o] = g * dyr[o];
+                /* second layer: out = W2 h + b2 */
+                for (int f = 0; f < F; ++f) {
+                    double a = 0.0;
+                    for (int o = 0; o < d; ++o) a += rd(W2, w_code, w2o + (size_t)o * F + f) * dout[o];
+                    dh[f] = a;
+                }
+                for (int o = 0; o < d; ++o) {
+                    for (int f = 0; f < F; ++f) dw2[w2o + (size_t)o * F + f] += dout[o] * h[f];
+                    if (db2) db2[(size_t)e * d + o] += dout[o];
+                }
+                /* activation */
+                for (int f = 0; f < F; ++f) {
+                    if (act == ORC_SWIGLU) {
+                        dz1[f] = dh[f] * z3[f] * act_grad(ORC_SWIGLU, z1[f]);
+                        dz3[f] = dh[f] * act_fn(ORC_SWIGLU, z1[f]);
+                    } else {
+                        dz1[f] = dh[f] * act_grad(act, z1[f]);
+                        dz3[f] = 0.0;
+                    }
+                }
+                /* first layer: z1 = W1 x + b1, z3 = W3 x */
+                double* dxs = dx_slot + (shared ? slots + (size_t)t * S + (size_t)(e - E) : s) * d;
+                for (int f = 0; f < F; ++f) {
+                    if (db1) db1[(size_t)e * F + f] += dz1[f];
+                    for (int i = 0; i < d; ++i) {
+                        dw1[w1o + (size_t)f * d + i] += dz1[f] * xr[i];
+                        if (act == ORC_SWIGLU) dw3[w1o + (size_t)f * d + i] += dz3[f] * xr[i];
+                    }
+                }
+                for (int i = 0; i < d; ++i) {
+                    double a = 0.0;
+                    for (int f = 0; f < F; ++f) {
+                        a += rd(W1, w_code, w1o + (size_t)f * d + i) * dz1[f];
+                        if (act == ORC_SWIGLU) a += rd(W3, w_code, w1o + (size_t)f * d + i) * dz3[f];
+                    }
+                    dxs[i] = a;
+                }
+            }
+        }
+        free(xr);
+        free(z1);
+        free(z3);
+        free(h);
+        free(dh);
+        free(dz1);
+        free(dz3);
+        free(dout);
+    }
+
+    /* router: gates -> probabilities -> logits (softmax Jacobian), plus the balance
+     * statistic's P_e term: d aux / d p[t,e] = E * f_e / T with f_e = counts_e / (T k) */
+    #pragma omp parallel
+    {
+        double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+        #pragma omp for schedule(static)
+        for (long t = 0; t < T; ++t) {
+            const double* p = probs + (size_t)t * E;
+            for (int e = 0; e < E; ++e)
+                dp[e] = d_aux * (double)E * ((double)counts[e] / ((double)T * k)) / (double)T;
+            double sel = 0.0, dot = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const size_t s = (size_t)t * k + j;
+                sel += p[idx[s]];
+                dot += dg[s] * p[idx[s]];
+            }
+            for (int j = 0; j < k; ++j) {
+                const size_t s = (size_t)t * k + j;
+                /* renormalised: g_j = p_j / sum_sel p, so dp_i = dg_i / sel - sum_j dg_j p_j / sel^2 */
+                dp[idx[s]] += renormalize ? dg[s] / sel - dot / (sel * sel) : dg[s];
+            }
+            double pdp = 0.0;
+            for (int e = 0; e < E; ++e) pdp += p[e] * dp[e];
+            for (int e = 0; e < E; ++e) {
+                const double g = p[e] * (dp[e] - pdp);
+                dl[(size_t)t * E + e] = g;
+                if (wn) {
+                    /* d/dn of eps * softplus(n) is eps * sigmoid(n) */
+                    const double u = nlog[(size_t)t * E + e];
+                    dn[(size_t)t * E + e] = g * rd(eps, n_code, (size_t)t * E + e) / (1.0 + exp(-u));
+                }
+            }
+        }
+        free(dp);
+    }
+
+    /* dx: expert slots + shared experts + pass-through + router (+ noise projection) */
+    #pragma omp parallel for schedule(static)
+    for (long t = 0; t < T; ++t) {
+        int n_dropped = 0;
+        for (int j = 0; j < k; ++j) n_dropped += dropped[(size_t)t * k + j] ? 1 : 0;
+        const int pass = residual_mode == 1 || (k >= 1 && n_dropped == k);
+        for (int i = 0; i < d; ++i) {
+            double a = pass ? dy[(size_t)t * d + i] : 0.0;
+            for (int j = 0; j < k; ++j) {
+                const size_t s = (size_t)t * k + j;
+                if (!dropped[s]) a += dx_slot[s * d + i];
+            }
+            for (int sh = 0; sh < S; ++sh) a += dx_slot[(slots + (size_t)t * S + sh) * d + i];
+            for (int e = 0; e < E; ++e) {
+                a += dl[(size_t)t * E + e] * rd(wg, wg_code, (size_t)e * d + i);
+                if (wn) a += dn[(size_t)t * E + e] * rd(wn, n_code, (size_t)e * d + i);
+            }
+            dx[(size_t)t * d + i] = a;
+        }
+    }
+
+    /* router weights: dW[e,i] = sum_t dl[t,e] x[t,i], db[e] = sum_t dl[t,e] */
+    #pragma omp parallel for schedule(static)
+    for (long e = 0; e < E; ++e) {
+        for (int i = 0; i < d; ++i) {
+            double a = 0.0, u = 0.0;
+            for (long t = 0; t < T; ++t) {
+                const double xv = rd(x, x_code, (size_t)t * d + i);
+                a += dl[(size_t)t * E + e] * xv;
+                u += dn[(size_t)t * E + e] * xv;
+            }
+            dwg[(size_t)e * d + i] = a;
+            if (dwn) dwn[(size_t)e * d + i] = u;
+        }
+        double a = 0.0, u = 0.0;
+        for (long t = 0; t < T; ++t) {
+            a += dl[(size_t)t * E + e];
+            u += dn[(size_t)t * E + e];
+        }
+        if (dbg) dbg[e] = a;
+        if (dbn) dbn[e] = u;
+    }
+
+    free(dg);
+    free(dx_slot);
+    free(gate);
+    free(probs);
+    free(nlog);
+    free(dl);
+    free(dn);
+    free(counts);
 }

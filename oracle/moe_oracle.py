@@ -80,6 +80,11 @@ def _lib():
         L.orc_output_rows.restype = None
         L.orc_output_rows.argtypes = [i32] * 8 + [vp, i32, vp, vp, vp, i32, vp, vp, i32,
                                                   vp, vp, vp, i32, vp, vp]
+        L.orc_act_grad.restype = dbl
+        L.orc_act_grad.argtypes = [i32, dbl]
+        L.orc_backward.restype = None
+        L.orc_backward.argtypes = ([i32] * 9 + [vp, i32, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, i32,
+                                                vp, vp, vp, i32, dbl, vp, vp, vp, dbl] + [vp] * 10)
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
         _lib_handle = L
@@ -253,6 +258,65 @@ def output_rows(x, W1, W3, W2, b1, b2, idx, gate_vals, dropped, *, E: int, S: in
                            _ptr(ba1), _ptr(ba2), bc,
                            _ptr(ia), _ptr(ga), _ptr(da), tok.shape[0], _ptr(tok), _ptr(y))
     return y
+
+
+def act_grad(name: str, z: float) -> float:
+    return float(_lib().orc_act_grad(ACTS[name], float(z)))
+
+
+def backward(x, Wg, bg, W1, W3, W2, b1, b2, *, idx, dropped, dy, d_aux: float, E: int, S: int,
+             act_name: str, renormalize: bool, residual_mode: int, noise=None) -> dict:
+    """Gradients (fp64) of L with dL/dy = dy and dL/daux = d_aux, the forward's
+    top-k choice ``idx`` and capacity drops ``dropped`` held fixed.
+
+    Returns dx, dW_gate, db_gate, dW1, dW3, dW2, db1, db2, dW_noise, db_noise
+    (None for inputs the layer does not have)."""
+    xa, xc = _as_array(x)
+    ga, gc = _as_array(Wg)
+    gba, gbc = _as_array(bg)
+    w1, wc = _as_array(W1)
+    w3, _ = _as_array(W3)
+    w2, _ = _as_array(W2)
+    ba1, bc = _as_array(b1)
+    ba2, bc2 = _as_array(b2)
+    if b1 is None:
+        bc = bc2
+    if noise is not None:
+        Wn, bn, eps, min_std = noise
+        na, nc = _as_array(Wn)
+        nba, nbc = _as_array(bn)
+        ea, ec = _as_array(eps)
+        if (bn is not None and nbc != nc) or ec != nc:
+            raise TypeError("W_noise, b_noise and eps must share a storage type")
+    else:
+        na = nba = ea = None
+        nc, min_std = 0, 0.0
+    T, d = xa.shape
+    F = w1.shape[1]
+    ia = _i32(idx)
+    k = ia.shape[1]
+    da = np.ascontiguousarray(np.asarray(dropped, dtype=np.uint8))
+    if not isinstance(dy, np.ndarray):
+        import torch  # a tensor handed in by the caller
+        dy = dy.detach().to("cpu", torch.float64).numpy()
+    dya = np.ascontiguousarray(dy, dtype=np.float64)
+    ES = E + S
+    out = {"dx": np.empty((T, d)), "dW_gate": np.empty((E, d)),
+           "db_gate": np.empty(E) if bg is not None else None,
+           "dW1": np.empty((ES, F, d)), "dW3": np.empty((ES, F, d)) if W3 is not None else None,
+           "dW2": np.empty((ES, d, F)), "db1": np.empty((ES, F)) if b1 is not None else None,
+           "db2": np.empty((ES, d)) if b2 is not None else None,
+           "dW_noise": np.empty((E, d)) if noise is not None else None,
+           "db_noise": np.empty(E) if noise is not None and noise[1] is not None else None}
+    o = out
+    _lib().orc_backward(T, d, F, E, S, k, ACTS[act_name], int(bool(renormalize)), int(residual_mode),
+                        _ptr(xa), xc, _ptr(ga), gc, _ptr(gba), gbc, _ptr(w1), _ptr(w3), _ptr(w2), wc,
+                        _ptr(ba1), _ptr(ba2), bc, _ptr(na), _ptr(nba), _ptr(ea), nc, float(min_std),
+                        _ptr(ia), _ptr(da), _ptr(dya), float(d_aux),
+                        _ptr(o["dx"]), _ptr(o["dW_gate"]), _ptr(o["db_gate"]), _ptr(o["dW1"]),
+                        _ptr(o["dW3"]), _ptr(o["dW2"]), _ptr(o["db1"]), _ptr(o["db2"]),
+                        _ptr(o["dW_noise"]), _ptr(o["db_noise"]))
+    return out
 
 
 def num_threads() -> int:
