@@ -70,6 +70,9 @@ typedef enum {
 #define MOE_FLAG_UNFUSED_EXPERTS 4u /* run the routed experts' two layers as two
                                        grouped-GEMM launches instead of one fused
                                        persistent launch (cross-check path) */
+#define MOE_FLAG_TRAINING 8u /* the workspace also holds what moe_backward needs (the
+                                forward keeps the router logits; backward buffers are
+                                reserved); required by moe_backward */
 
 /* Limits of this build. */
 #define MOE_MAX_EXPERTS 512 /* E (routed) */
@@ -185,6 +188,42 @@ moe_status_t moe_grouped_gemm(const moe_params_t* params, const moe_inputs_t* in
 moe_status_t moe_combine(const moe_params_t* params, const moe_inputs_t* inputs,
                          moe_outputs_t* outputs, void* workspace, size_t workspace_bytes,
                          void* stream);
+
+/* Gradients written by moe_backward (caller-owned device arrays, 16-byte aligned). */
+typedef struct {
+    void* dx;         /* [T, d] dtype */
+    float* dW_gate;   /* [E, d] fp32 */
+    float* db_gate;   /* [E] fp32; required iff inputs.b_gate != NULL, else NULL */
+    void* dW1;        /* [E+S, F, d] dtype */
+    void* dW3;        /* [E+S, F, d] dtype; required iff act == SWIGLU, else NULL */
+    void* dW2;        /* [E+S, d, F] dtype */
+    void* db1;        /* [E+S, F] dtype; required iff inputs.b1 != NULL, else NULL */
+    void* db2;        /* [E+S, d] dtype; required iff inputs.b2 != NULL, else NULL */
+    float* dW_noise;  /* [E, d] fp32; required iff noisy_gating, else NULL */
+    float* db_noise;  /* [E] fp32; required iff noisy_gating and b_noise != NULL, else NULL */
+} moe_grads_t;
+
+/* Backward pass of the layer ([Intro] §3.4-§3.5 trains the layer end to end
+ * with task loss + coef * aux loss; [Switch] §"负载均衡损失函数": P_i is
+ * differentiable, f_i is not).  Given dy = dL/dy [T, d] (dtype, device) and
+ * d_aux = dL/d aux (e.g. the aux-loss coefficient), writes every gradient of
+ * moe_grads_t.  The forward's discrete decisions (top-k, capacity drops,
+ * pass-through) are held fixed: the router receives gradient through the gate
+ * values and P_i only.  Gate gradients pass through the renormalisation when it
+ * applies; under noisy gating the noise projection receives
+ * dL/dn = dL/dlogit * eps * sigmoid(n) (the draws are data).
+ *
+ * Requires MOE_FLAG_TRAINING in params.flags and, on the same workspace and
+ * stream, a moe_forward with the same params, inputs and outputs whose results
+ * are still in place (the backward reads expert_idx, gates, counts and the
+ * optional logits from `outputs`, and the permuted activations, hidden
+ * activations and expert outputs from the workspace).  Gradients are computed
+ * in fp32 and rounded once to the destination type; weight gradients are
+ * written (not accumulated).  Validation happens before any launch. */
+moe_status_t moe_backward(const moe_params_t* params, const moe_inputs_t* inputs,
+                          const moe_outputs_t* outputs, const void* dy, float d_aux,
+                          const moe_grads_t* grads, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* Synchronises `stream`, reads and clears the workspace's device error word.
  * Returns MOE_ERR_DEVICE_TIMEOUT if a bounded device wait expired since the last

@@ -26,6 +26,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_FLAG_FFMA_EXPERTS = 1
 MOE_FLAG_FFMA_ROUTER = 2
 MOE_FLAG_UNFUSED_EXPERTS = 4
+MOE_FLAG_TRAINING = 8
 MOE_MAX_EXPERTS = 512
 MOE_MAX_TOPK = 32
 MOE_NOALLOC_MAX_SLOTS = 131072
@@ -48,6 +49,11 @@ class moe_outputs_t(ctypes.Structure):
     _fields_ = [("y", _vp), ("expert_idx", _vp), ("gates", _vp), ("counts", _vp),
                 ("dropped", _vp), ("aux", _vp), ("logits", _vp), ("probs", _vp),
                 ("perm_row", _vp)]
+
+
+class moe_grads_t(ctypes.Structure):
+    _fields_ = [("dx", _vp), ("dW_gate", _vp), ("db_gate", _vp), ("dW1", _vp), ("dW3", _vp),
+                ("dW2", _vp), ("db1", _vp), ("db2", _vp), ("dW_noise", _vp), ("db_noise", _vp)]
 
 
 _P = ctypes.POINTER
@@ -77,6 +83,9 @@ def load(build_if_stale: bool = True):
         f = getattr(L, name)
         f.restype = _i32
         f.argtypes = _STAGE_ARGS
+    L.moe_backward.restype = _i32
+    L.moe_backward.argtypes = [_P(moe_params_t), _P(moe_inputs_t), _P(moe_outputs_t), _vp, _f32,
+                               _P(moe_grads_t), _vp, ctypes.c_size_t, _vp]
     L.moe_last_device_status.restype = _i32
     L.moe_last_device_status.argtypes = [_vp, ctypes.c_size_t, _vp]
     L.moe_dispatch_positions_noalloc.restype = _i32
@@ -129,6 +138,12 @@ def moe_grouped_gemm(params, inputs, outputs, workspace, workspace_bytes, stream
 
 def moe_combine(params, inputs, outputs, workspace, workspace_bytes, stream):
     return _stage("moe_combine", params, inputs, outputs, workspace, workspace_bytes, stream)
+
+
+def moe_backward(params, inputs, outputs, dy, d_aux, grads, workspace, workspace_bytes, stream):
+    return load().moe_backward(ctypes.byref(params), ctypes.byref(inputs), ctypes.byref(outputs), _vp(dy),
+                               _f32(d_aux), ctypes.byref(grads), _vp(workspace),
+                               ctypes.c_size_t(workspace_bytes), _vp(stream))
 
 
 def moe_dispatch_positions_noalloc(params, expert_idx, counts, dropped, perm_row, stream):

@@ -43,7 +43,13 @@ struct Layout {
     size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
     int ffn_sync_n;
     size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
-        off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys, total;
+        off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys;
+    // backward (MOE_FLAG_TRAINING): gate and router gradients, the router's share of dx,
+    // dYp (reused for dXp), pre-activations (overwritten in place by their gradients;
+    // relu: dZ1 only), shared-expert pre-activations and input gradient
+    size_t off_bw_dgate, off_bw_dl, off_bw_dn, off_bw_dxr, off_bw_dyp, off_bw_z1, off_bw_z3, off_bw_zs1,
+        off_bw_zs3, off_bw_dxs;
+    size_t total;
 };
 
 long long capacity_of(const moe_params_t& p)
@@ -66,7 +72,8 @@ moe_status_t validate_params(const moe_params_t* p)
     if (p->residual_mode != 0 && p->residual_mode != 1) return MOE_ERR_INVALID_ARG;
     if (p->act < MOE_ACT_RELU || p->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-    if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER | MOE_FLAG_UNFUSED_EXPERTS)) != 0u)
+    if ((p->flags & ~(MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_FFMA_ROUTER | MOE_FLAG_UNFUSED_EXPERTS | MOE_FLAG_TRAINING)) !=
+        0u)
         return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (p->noisy_gating != 0 && p->noisy_gating != 1) return MOE_ERR_INVALID_ARG;
@@ -135,6 +142,19 @@ Layout make_layout(const moe_params_t& p)
     L.off_yp = take(L.esz * (size_t)L.rows_cap * L.d);
     L.off_hs = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.S * L.F : 0);
     L.off_ys = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.d : 0);
+    const bool train = (p.flags & MOE_FLAG_TRAINING) != 0u;
+    const bool swiglu = p.act == MOE_ACT_SWIGLU;
+    auto bw = [&](size_t bytes) { return take(train ? bytes : 0); };
+    L.off_bw_dgate = bw(sizeof(float) * (size_t)slots);
+    L.off_bw_dl = bw(sizeof(float) * (size_t)L.T * L.E);
+    L.off_bw_dn = bw(noisy ? sizeof(float) * (size_t)L.T * L.E : 0);
+    L.off_bw_dxr = bw(sizeof(float) * (size_t)L.T * L.d);
+    L.off_bw_dyp = bw(L.esz * (size_t)L.rows_cap * L.d);
+    L.off_bw_z1 = bw(L.esz * (size_t)L.rows_cap * L.F);
+    L.off_bw_z3 = bw(swiglu ? L.esz * (size_t)L.rows_cap * L.F : 0);
+    L.off_bw_zs1 = bw(L.S > 0 ? L.esz * (size_t)L.T * L.S * L.F : 0);
+    L.off_bw_zs3 = bw(L.S > 0 ? L.esz * (size_t)L.T * L.S * L.F : 0);
+    L.off_bw_dxs = bw(L.S > 0 ? L.esz * (size_t)L.T * L.d : 0);
     L.total = o;
     return L;
 }
@@ -312,6 +332,8 @@ moe_status_t stage_router(Ctx& c)
         a.min_std = c.p.noise_min_std;
     }
     if (!c.L.tc_router) {
+        // training keeps the logits for the backward pass
+        if (a.logits == nullptr && (c.p.flags & MOE_FLAG_TRAINING)) a.logits = c.at<float>(c.L.off_logits);
         cudaError_t e = cudaSuccess;
         if (noisy) {  // noise projection x W_noise^T first, then the routing pass adds the noise
             RouterArgs r = a;
@@ -549,6 +571,406 @@ moe_status_t run_stages(const moe_params_t* params, const moe_inputs_t* in, moe_
     return MOE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Backward pass
+
+moe_status_t validate_grads(const moe_params_t& p, const moe_inputs_t* in, const void* dy, float d_aux,
+                            const moe_grads_t* g)
+{
+    if (g == nullptr || dy == nullptr || !aligned16(dy) || !std::isfinite(d_aux)) return MOE_ERR_INVALID_ARG;
+    if (!g->dx || !g->dW_gate || !g->dW1 || !g->dW2) return MOE_ERR_INVALID_ARG;
+    const bool swiglu = p.act == MOE_ACT_SWIGLU, noisy = p.noisy_gating == 1;
+    if ((g->dW3 != nullptr) != swiglu || (g->db_gate != nullptr) != (in->b_gate != nullptr) ||
+        (g->db1 != nullptr) != (in->b1 != nullptr) || (g->db2 != nullptr) != (in->b2 != nullptr) ||
+        (g->dW_noise != nullptr) != noisy || (g->db_noise != nullptr) != (noisy && in->b_noise != nullptr))
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {g->dx, g->dW_gate, g->db_gate, g->dW1, g->dW3, g->dW2, g->db1, g->db2, g->dW_noise,
+                          g->db_noise};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+const void* offset_elems(const void* p, size_t n, size_t esz)
+{
+    return p == nullptr ? nullptr : static_cast<const char*>(p) + n * esz;
+}
+
+moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t* gr)
+{
+    const Layout& L = c.L;
+    const size_t esz = L.esz;
+    const int types = c.bf16 ? kBwdTypesBf16 : kBwdTypesF32;
+    const bool swiglu = c.p.act == MOE_ACT_SWIGLU, noisy = c.p.noisy_gating == 1;
+    const float* logits = c.out->logits != nullptr ? c.out->logits : c.at<float>(L.off_logits);
+    float* dgate = c.at<float>(L.off_bw_dgate);
+    float* dl = c.at<float>(L.off_bw_dl);
+    float* dn = noisy ? c.at<float>(L.off_bw_dn) : nullptr;
+    float* dxr = c.at<float>(L.off_bw_dxr);
+    void* dyp = c.at<void>(L.off_bw_dyp);
+    void* z1 = c.at<void>(L.off_bw_z1);
+    void* z3 = swiglu ? c.at<void>(L.off_bw_z3) : nullptr;
+    const int* mtile = c.at<int>(L.off_mtile);
+    const int* row_off = c.at<int>(L.off_row_off);
+    const int* kept = c.at<int>(L.off_kept);
+    const int32_t* slot_row = c.at<int32_t>(L.off_slot_row);
+    const int mt_routed = L.rows_cap / kSegRows;
+    auto grid_for = [&](long long tiles) { return (int)std::max(1ll, std::min(tiles, (long long)c.sms * 4)); };
+    auto tiles = [](int M, int N) { return (long long)ceil_div(M, 128) * ceil_div(N, 64); };
+    cudaError_t e = cudaSuccess;
+    auto gemm = [&](const BwdGemmArgs& a, int ty, long long n_tiles) {
+        if (e == cudaSuccess) e = launch_gemm_bwd_ffma(a, ty, grid_for(n_tiles), c.st, take_pdl(c));
+    };
+    auto colsum = [&](const ColsumArgs& a, int ty) {
+        if (e == cudaSuccess) e = launch_colsum(a, ty, c.sms, c.st, take_pdl(c));
+    };
+
+    // combine: dYp = gate * dy on each kept slot's row, dgate = <dy, Yp>
+    BwdCombineArgs cb{};
+    cb.dy = dy;
+    cb.yp = c.at<void>(L.off_yp);
+    cb.dyp = dyp;
+    cb.slot_row = slot_row;
+    cb.gates = c.out->gates;
+    cb.dgate = dgate;
+    cb.T = L.T;
+    cb.d = L.d;
+    cb.k = L.k;
+    e = launch_bwd_combine(cb, c.bf16, c.sms, c.st, take_pdl(c));
+
+    // router: logit (and noise) gradients, then the router's weight and input gradients
+    RouterBwdArgs rb{};
+    rb.logits = logits;
+    rb.idx = c.out->expert_idx;
+    rb.dgate = dgate;
+    rb.counts = c.out->counts;
+    rb.d_aux = d_aux;
+    rb.T = L.T;
+    rb.E = L.E;
+    rb.k = L.k;
+    rb.renormalize = c.p.renormalize;
+    rb.dl = dl;
+    if (noisy) {
+        rb.noise_parts = c.at<float>(L.off_nlogits);
+        rb.k_splits = L.r_ksplits;
+        rb.bn = c.in->b_noise;
+        rb.eps = c.in->noise_eps;
+        rb.dn = dn;
+    }
+    if (e == cudaSuccess) e = launch_router_bwd(rb, c.sms, c.st, take_pdl(c));
+    {
+        BwdGemmArgs a{};  // dW_gate[e, i] = sum_t dl[t, e] x[t, i]
+        a.mode = kBwdFixed;
+        a.epi = kEpiStore;
+        a.A = dl;
+        a.a_sm = 1;
+        a.a_sk = L.E;
+        a.B = c.in->x;
+        a.b_sk = L.d;
+        a.b_sn = 1;
+        a.C = gr->dW_gate;
+        a.c_sm = L.d;
+        a.M = L.E;
+        a.N = L.d;
+        a.K = L.T;
+        const int ty = c.bf16 ? kBwdTypesF32xBf16 : kBwdTypesF32;
+        gemm(a, ty, tiles(a.M, a.N));
+        if (noisy) {
+            a.A = dn;
+            a.C = gr->dW_noise;
+            gemm(a, ty, tiles(a.M, a.N));
+        }
+        ColsumArgs s{};
+        s.lda = L.E;
+        s.fixed_rows = L.T;
+        s.G = 1;
+        s.N = L.E;
+        if (gr->db_gate) {
+            s.A = dl;
+            s.out = gr->db_gate;
+            colsum(s, kBwdTypesF32);
+        }
+        if (gr->db_noise) {
+            s.A = dn;
+            s.out = gr->db_noise;
+            colsum(s, kBwdTypesF32);
+        }
+        BwdGemmArgs r{};  // dx_router[t, i] = sum_e dl[t, e] W_gate[e, i] (+ dn W_noise)
+        r.mode = kBwdFixed;
+        r.epi = kEpiStore;
+        r.A = dl;
+        r.A2 = dn;
+        r.a_sm = L.E;
+        r.a_sk = 1;
+        r.B = c.in->W_gate;
+        r.B2 = noisy ? c.in->W_noise : nullptr;
+        r.b_sk = L.d;
+        r.b_sn = 1;
+        r.C = dxr;
+        r.c_sm = L.d;
+        r.M = L.T;
+        r.N = L.d;
+        r.K = L.E;
+        gemm(r, kBwdTypesF32, tiles(r.M, r.N));
+    }
+
+    // routed experts
+    BwdGemmArgs rows{};  // row-grouped products over the expert segments
+    rows.mode = kBwdRows;
+    rows.mtile_off = mtile;
+    rows.row_off = row_off;
+    rows.rows = kept;
+    rows.G = L.E;
+    BwdGemmArgs red = rows;  // products reduced over the rows of each segment
+    red.mode = kBwdReduce;
+    const long long mt_tiles = mt_routed;
+    if (c.p.act != MOE_ACT_RELU) {  // recompute the pre-activations z1 (+ b1) and z3
+        BwdGemmArgs a = rows;
+        a.epi = kEpiStore;
+        a.A = c.at<void>(L.off_xp);
+        a.a_sm = L.d;
+        a.a_sk = 1;
+        a.B = c.in->W1;
+        a.b_sk = 1;
+        a.b_sn = L.d;
+        a.b_gs = (long long)L.F * L.d;
+        a.C = z1;
+        a.c_sm = L.F;
+        a.bias = c.in->b1;
+        a.N = L.F;
+        a.K = L.d;
+        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+        if (swiglu) {
+            a.B = c.in->W3;
+            a.C = z3;
+            a.bias = nullptr;
+            gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+        }
+    }
+    {
+        BwdGemmArgs a = red;  // dW2_e = dYp_e^T H_e
+        a.epi = kEpiStore;
+        a.A = dyp;
+        a.a_sm = 1;
+        a.a_sk = L.d;
+        a.B = c.at<void>(L.off_h);
+        a.b_sk = L.F;
+        a.b_sn = 1;
+        a.C = gr->dW2;
+        a.c_gs = (long long)L.d * L.F;
+        a.c_sm = L.F;
+        a.M = L.d;
+        a.N = L.F;
+        gemm(a, types, L.E * tiles(a.M, a.N));
+    }
+    if (gr->db2) {
+        ColsumArgs s{};
+        s.A = dyp;
+        s.lda = L.d;
+        s.row_off = row_off;
+        s.rows = kept;
+        s.G = L.E;
+        s.N = L.d;
+        s.out = gr->db2;
+        colsum(s, types);
+    }
+    {
+        BwdGemmArgs a = rows;  // dH = dYp W2_e, then the activation backward
+        a.A = dyp;
+        a.a_sm = L.d;
+        a.a_sk = 1;
+        a.B = c.in->W2;
+        a.b_sk = L.F;
+        a.b_sn = 1;
+        a.b_gs = (long long)L.d * L.F;
+        a.C = z1;
+        a.c_sm = L.F;
+        a.N = L.F;
+        a.K = L.d;
+        if (c.p.act == MOE_ACT_RELU) {
+            a.epi = kEpiReluBwd;
+            a.e1 = c.at<void>(L.off_h);
+        } else if (swiglu) {
+            a.epi = kEpiSwigluBwd;
+            a.e1 = z1;
+            a.e2 = z3;
+            a.C2 = z3;
+        } else {
+            a.epi = c.p.act == MOE_ACT_GELU_TANH ? kEpiGeluTanhBwd : kEpiGeluErfBwd;
+            a.e1 = z1;
+        }
+        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+    }
+    {
+        BwdGemmArgs a = red;  // dW1_e = dZ1_e^T Xp_e (and dW3_e from dZ3)
+        a.epi = kEpiStore;
+        a.A = z1;
+        a.a_sm = 1;
+        a.a_sk = L.F;
+        a.B = c.at<void>(L.off_xp);
+        a.b_sk = L.d;
+        a.b_sn = 1;
+        a.C = gr->dW1;
+        a.c_gs = (long long)L.F * L.d;
+        a.c_sm = L.d;
+        a.M = L.F;
+        a.N = L.d;
+        gemm(a, types, L.E * tiles(a.M, a.N));
+        if (swiglu) {
+            a.A = z3;
+            a.C = gr->dW3;
+            gemm(a, types, L.E * tiles(a.M, a.N));
+        }
+    }
+    if (gr->db1) {
+        ColsumArgs s{};
+        s.A = z1;
+        s.lda = L.F;
+        s.row_off = row_off;
+        s.rows = kept;
+        s.G = L.E;
+        s.N = L.F;
+        s.out = gr->db1;
+        colsum(s, types);
+    }
+    {
+        BwdGemmArgs a = rows;  // dXp = dZ1 W1_e (+ dZ3 W3_e), into the dYp buffer
+        a.epi = kEpiStore;
+        a.A = z1;
+        a.A2 = z3;
+        a.a_sm = L.F;
+        a.a_sk = 1;
+        a.B = c.in->W1;
+        a.B2 = swiglu ? c.in->W3 : nullptr;
+        a.b_sk = L.d;
+        a.b_sn = 1;
+        a.b_gs = (long long)L.F * L.d;
+        a.C = dyp;
+        a.c_sm = L.d;
+        a.N = L.d;
+        a.K = L.F;
+        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+    }
+
+    // shared experts: gate 1 on every token (SwiGLU), hidden S*F, dO = dy
+    void* dxs = nullptr;
+    if (L.S > 0) {
+        void* zs1 = c.at<void>(L.off_bw_zs1);
+        void* zs3 = c.at<void>(L.off_bw_zs3);
+        dxs = c.at<void>(L.off_bw_dxs);
+        const long long SF = (long long)L.S * L.F;
+        BwdGemmArgs a{};
+        a.mode = kBwdFixed;
+        a.epi = kEpiStore;
+        a.A = c.in->x;  // z = x W^T over the S*F concatenated rows
+        a.a_sm = L.d;
+        a.a_sk = 1;
+        a.B = c.in->W1;
+        a.b_sk = 1;
+        a.b_sn = L.d;
+        a.b_gs = (long long)L.F * L.d;
+        a.b_g0 = L.E;
+        a.C = zs1;
+        a.c_sm = SF;
+        a.M = L.T;
+        a.N = (int)SF;
+        a.K = L.d;
+        gemm(a, types, tiles(a.M, a.N));
+        a.B = c.in->W3;
+        a.C = zs3;
+        gemm(a, types, tiles(a.M, a.N));
+        for (int sh = 0; sh < L.S; ++sh) {
+            BwdGemmArgs b{};  // dH_s = dy W2_s with the SwiGLU backward, on columns s*F ..
+            b.mode = kBwdFixed;
+            b.epi = kEpiSwigluBwd;
+            b.A = dy;
+            b.a_sm = L.d;
+            b.a_sk = 1;
+            b.B = c.in->W2;
+            b.b_sk = L.F;
+            b.b_sn = 1;
+            b.b_gs = (long long)L.d * L.F;
+            b.b_g0 = L.E + sh;
+            b.C = const_cast<void*>(offset_elems(zs1, (size_t)sh * L.F, esz));
+            b.C2 = const_cast<void*>(offset_elems(zs3, (size_t)sh * L.F, esz));
+            b.e1 = b.C;
+            b.e2 = b.C2;
+            b.c_sm = SF;
+            b.M = L.T;
+            b.N = L.F;
+            b.K = L.d;
+            // dW2_s = dy^T H_s first (it reads H_s, which the SwiGLU backward leaves alone)
+            BwdGemmArgs w{};
+            w.mode = kBwdFixed;
+            w.epi = kEpiStore;
+            w.A = dy;
+            w.a_sm = 1;
+            w.a_sk = L.d;
+            w.B = offset_elems(c.at<void>(L.off_hs), (size_t)sh * L.F, esz);
+            w.b_sk = SF;
+            w.b_sn = 1;
+            w.C = const_cast<void*>(offset_elems(gr->dW2, (size_t)(L.E + sh) * L.d * L.F, esz));
+            w.c_sm = L.F;
+            w.M = L.d;
+            w.N = L.F;
+            w.K = L.T;
+            gemm(w, types, tiles(w.M, w.N));
+            gemm(b, types, tiles(b.M, b.N));
+        }
+        BwdGemmArgs w{};  // dW1_s = dZs1^T x, dW3_s = dZs3^T x over the S*F rows
+        w.mode = kBwdFixed;
+        w.epi = kEpiStore;
+        w.A = zs1;
+        w.a_sm = 1;
+        w.a_sk = SF;
+        w.B = c.in->x;
+        w.b_sk = L.d;
+        w.b_sn = 1;
+        w.C = const_cast<void*>(offset_elems(gr->dW1, (size_t)L.E * L.F * L.d, esz));
+        w.c_sm = L.d;
+        w.M = (int)SF;
+        w.N = L.d;
+        w.K = L.T;
+        gemm(w, types, tiles(w.M, w.N));
+        w.A = zs3;
+        w.C = const_cast<void*>(offset_elems(gr->dW3, (size_t)L.E * L.F * L.d, esz));
+        gemm(w, types, tiles(w.M, w.N));
+        BwdGemmArgs x{};  // dXs = dZs1 W1_s + dZs3 W3_s
+        x.mode = kBwdFixed;
+        x.epi = kEpiStore;
+        x.A = zs1;
+        x.A2 = zs3;
+        x.a_sm = SF;
+        x.a_sk = 1;
+        x.B = c.in->W1;
+        x.B2 = c.in->W3;
+        x.b_sk = L.d;
+        x.b_sn = 1;
+        x.b_gs = (long long)L.F * L.d;
+        x.b_g0 = L.E;
+        x.C = dxs;
+        x.c_sm = L.d;
+        x.M = L.T;
+        x.N = L.d;
+        x.K = (int)SF;
+        gemm(x, types, tiles(x.M, x.N));
+    }
+
+    BwdUnpermuteArgs u{};
+    u.dy = dy;
+    u.dxp = dyp;
+    u.dxs = dxs;
+    u.dxr = dxr;
+    u.slot_row = slot_row;
+    u.T = L.T;
+    u.d = L.d;
+    u.k = L.k;
+    u.residual_mode = c.p.residual_mode;
+    u.dx = gr->dx;
+    if (e == cudaSuccess) e = launch_bwd_unpermute(u, c.bf16, c.sms, c.st, take_pdl(c));
+    return cuda_status(e);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -594,6 +1016,22 @@ moe_status_t moe_combine(const moe_params_t* params, const moe_inputs_t* inputs,
                          void* workspace, size_t workspace_bytes, void* stream)
 {
     return run_stages(params, inputs, outputs, workspace, workspace_bytes, stream, {stage_combine});
+}
+
+moe_status_t moe_backward(const moe_params_t* params, const moe_inputs_t* inputs, const moe_outputs_t* outputs,
+                          const void* dy, float d_aux, const moe_grads_t* grads, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    moe_status_t s = validate_params(params);
+    if (s != MOE_OK) return s;
+    if (!(params->flags & MOE_FLAG_TRAINING) || outputs == nullptr || inputs == nullptr) return MOE_ERR_INVALID_ARG;
+    s = validate_grads(*params, inputs, dy, d_aux, grads);
+    if (s != MOE_OK) return s;
+    moe_outputs_t out = *outputs;  // read only
+    Ctx c;
+    s = prepare(params, inputs, &out, workspace, workspace_bytes, stream, c);
+    if (s != MOE_OK) return s;
+    return run_backward(c, dy, d_aux, grads);
 }
 
 moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, void* stream)

@@ -355,6 +355,33 @@ __device__ __forceinline__ float activate_bf16out(float z)
     }
 }
 
+// Derivatives for the backward pass (fp32), from the definitions above:
+//   silu'(z) = s (1 + z (1 - s)),  s = 1 / (1 + e^-z);
+//   GELU(tanh)'(z) = (1 + th) / 2 + z (1 - th^2) c (1 + 3 a z^2) / 2,  th = tanh(c (z + a z^3));
+//   GELU(erf)'(z) = Phi(z) + z phi(z).
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+__device__ __forceinline__ float silu_grad_f32(float z)
+{
+    const float s = 1.0f / (1.0f + expf(-z));
+    return s * (1.0f + z * (1.0f - s));
+}
+template <int ACT>
+__device__ __forceinline__ float act_grad_f32(float z)
+{
+    if constexpr (ACT == kActRelu) {
+        return z > 0.0f ? 1.0f : 0.0f;
+    } else if constexpr (ACT == kActGeluTanh) {
+        const float c = 0.7978845608028654f, a = 0.044715f;  // sqrt(2/pi)
+        const float th = tanhf(c * (z + a * z * z * z));
+        return 0.5f * (1.0f + th) + 0.5f * z * (1.0f - th * th) * c * (1.0f + 3.0f * a * z * z);
+    } else if constexpr (ACT == kActGeluErf) {
+        // 1/sqrt(2) and 1/sqrt(2 pi)
+        return 0.5f * (1.0f + erff(z * 0.7071067811865476f)) + z * expf(-0.5f * z * z) * 0.3989422804014327f;
+    } else {
+        return silu_grad_f32(z);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Grouped GEMM problem description (shared by the tcgen05 and FFMA kernels).
 //

@@ -134,6 +134,98 @@ cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* 
                              cudaStream_t st, bool pdl);
 constexpr int kFfmaTileN = 64;
 
+// ---- backward: grouped GEMMs ---------------------------------------------------
+// C_g[m, n] = sum_k A_g(m, k) B_g(k, n) (+ a second product A2 B2 with the same
+// strides), element (m, k) of A at A[a_base + m*a_sm + k*a_sk], (k, n) of B at
+// B[b_base + k*b_sk + n*b_sn], output at C[c_base + m*c_sm + n].  Per group g:
+//   kBwdRows   M = rows[g]:   a_base = row_off[g]*a_sm, c_base = row_off[g]*c_sm,
+//                             b_base = (b_g0+g)*b_gs; tiles from mtile_off (128 rows)
+//   kBwdReduce K = rows[g]:   a_base = row_off[g]*a_sk, b_base = row_off[g]*b_sk,
+//                             c_base = (c_g0+g)*c_gs; M, N fixed
+//   kBwdFixed  one group:     a_base = 0, b_base = b_g0*b_gs, c_base = 0
+// Epilogues: store; relu backward (e1 = the saved relu output h); GELU backward
+// (e1 = the pre-activation z); SwiGLU backward (e1 = z1, e2 = z3; writes
+// dz1 = v z3 silu'(z1) to C and dz3 = v silu(z1) to C2); e1, e2, C2 share C's indexing.
+enum BwdMode : int { kBwdFixed = 0, kBwdRows = 1, kBwdReduce = 2 };
+enum BwdEpi : int { kEpiStore = 0, kEpiReluBwd = 1, kEpiGeluTanhBwd = 2, kEpiGeluErfBwd = 3, kEpiSwigluBwd = 4 };
+enum BwdTypes : int { kBwdTypesBf16 = 0, kBwdTypesF32 = 1, kBwdTypesF32xBf16 = 2 };  // (A,B,C) element types
+struct BwdGemmArgs {
+    int mode, epi;
+    const void* A;
+    const void* A2;
+    long long a_sm, a_sk;
+    const void* B;
+    const void* B2;
+    long long b_sk, b_sn, b_gs;
+    int b_g0;
+    void* C;
+    void* C2;
+    long long c_sm, c_gs;
+    int c_g0;
+    const void* e1;
+    const void* e2;
+    const void* bias;     // store epilogue: + bias[(b_g0 + g) * N + n] (element type of C), or nullptr
+    int M, N, K;
+    const int* mtile_off;
+    const int* row_off;
+    const int* rows;
+    int G;
+};
+cudaError_t launch_gemm_bwd_ffma(const BwdGemmArgs& a, int types, int grid, cudaStream_t st, bool pdl);
+
+// ---- backward: memory-bound kernels ---------------------------------------------
+struct BwdCombineArgs {
+    const void* dy;        // [T, d]
+    const void* yp;        // [rows_cap, d] forward expert outputs
+    void* dyp;             // [rows_cap, d] out: gate * dy on the slot's row
+    const int32_t* slot_row;
+    const float* gates;    // [T, k]
+    float* dgate;          // [T, k] out
+    int T, d, k;
+};
+cudaError_t launch_bwd_combine(const BwdCombineArgs& a, bool bf16, int sms, cudaStream_t st, bool pdl);
+
+struct RouterBwdArgs {
+    const float* logits;   // [T, E] the logits the gating used
+    const int32_t* idx;    // [T, k]
+    const float* dgate;    // [T, k]
+    const int32_t* counts; // [E]
+    float d_aux;
+    int T, E, k, renormalize;
+    float* dl;             // [T, E] out
+    // noisy gating (eps == nullptr: off)
+    const float* noise_parts;  // [k_splits, T, E] noise logits without b_noise
+    int k_splits;
+    const float* bn;
+    const float* eps;
+    float* dn;             // [T, E] out
+};
+cudaError_t launch_router_bwd(const RouterBwdArgs& a, int sms, cudaStream_t st, bool pdl);
+
+// out[(out_g0 + g) * N + n] = sum_{r < rows[g]} A[(row_off[g] + r) * lda + n]
+// (row_off == nullptr: one group of fixed_rows rows from row 0)
+struct ColsumArgs {
+    const void* A;
+    long long lda;
+    const int* row_off;
+    const int* rows;
+    int fixed_rows;
+    int G, N, out_g0;
+    void* out;
+};
+cudaError_t launch_colsum(const ColsumArgs& a, int types, int sms, cudaStream_t st, bool pdl);
+
+struct BwdUnpermuteArgs {
+    const void* dy;        // [T, d]
+    const void* dxp;       // [rows_cap, d]
+    const void* dxs;       // [T, d] shared experts' input gradient, or nullptr
+    const float* dxr;      // [T, d] router's input gradient
+    const int32_t* slot_row;
+    int T, d, k, residual_mode;
+    void* dx;              // [T, d] out
+};
+cudaError_t launch_bwd_unpermute(const BwdUnpermuteArgs& a, bool bf16, int sms, cudaStream_t st, bool pdl);
+
 // ---- stage 4: combine ------------------------------------------------------
 struct CombineArgs {
     const void* yp;       // [rows_cap, d]

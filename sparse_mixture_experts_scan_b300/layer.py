@@ -100,6 +100,40 @@ class MoELayer:
                  self.workspace_bytes, _stream_handle(stream)), stage)
         return self.out
 
+    def backward(self, dy: torch.Tensor, d_aux: float = 0.0, stream=None) -> dict:
+        """moe_backward for the last run() of this layer (needs MOE_FLAG_TRAINING).
+
+        Allocates the gradient arrays on first use; returns them by input name."""
+        if not (self.params.flags & _lib.MOE_FLAG_TRAINING):
+            raise ValueError("the layer was built without MOE_FLAG_TRAINING")
+        cfg, dev, w = self.cfg, self.device, self.weights
+        if not hasattr(self, "grads"):
+            ES = cfg.E + cfg.S
+            dt = cfg.torch_dtype
+            f32 = torch.float32
+            like = lambda key, shape, dtype: (torch.empty(shape, dtype=dtype, device=dev)  # noqa: E731
+                                              if w.get(key) is not None else None)
+            self.grads = {
+                "dx": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev),
+                "dW_gate": torch.empty(cfg.E, cfg.d, dtype=f32, device=dev),
+                "db_gate": like("b_gate", (cfg.E,), f32),
+                "dW1": torch.empty(ES, cfg.F, cfg.d, dtype=dt, device=dev),
+                "dW3": like("W3", (ES, cfg.F, cfg.d), dt),
+                "dW2": torch.empty(ES, cfg.d, cfg.F, dtype=dt, device=dev),
+                "db1": like("b1", (ES, cfg.F), dt),
+                "db2": like("b2", (ES, cfg.d), dt),
+                "dW_noise": like("W_noise", (cfg.E, cfg.d), f32),
+                "db_noise": like("b_noise", (cfg.E,), f32),
+            }
+            g = self.grads
+            self._grads_c = _lib.moe_grads_t(**{k: _ptr(v) for k, v in g.items()})
+        dy = dy.contiguous()
+        self._dy = dy  # alive until the next call
+        check(_lib.moe_backward(self.params, self.inputs, self.outputs, dy.data_ptr(), float(d_aux),
+                                self._grads_c, self.workspace.data_ptr(), self.workspace_bytes,
+                                _stream_handle(stream)), "moe_backward")
+        return self.grads
+
     def device_status(self, stream=None) -> int:
         return _lib.moe_last_device_status(self.workspace.data_ptr(), self.workspace_bytes,
                                            _stream_handle(stream))

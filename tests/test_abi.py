@@ -12,7 +12,7 @@ def test_library_exports_every_header_function():
     assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
                           "moe_status_string", "moe_dispatch_positions_noalloc",
-                          "moe_kernel_launches"}
+                          "moe_kernel_launches", "moe_backward"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -49,7 +49,7 @@ def test_workspace_grows_with_tokens():
 
 @pytest.mark.parametrize("field,value", [
     ("k", 0), ("k", 9), ("E", 0), ("E", 513), ("d_model", 12), ("d_ff", 20), ("T", 0),
-    ("renormalize", 2), ("residual_mode", 5), ("act", 7), ("dtype", 3), ("flags", 8),
+    ("renormalize", 2), ("residual_mode", 5), ("act", 7), ("dtype", 3), ("flags", 16),
     ("n_shared", -1)])
 def test_invalid_params_rejected(field, value):
     p = make_params(config("mixtral"))
@@ -179,4 +179,45 @@ def test_launch_counter_does_not_move_on_rejected_calls():
     p.k = 0
     ins, outs = _fake_io(cfg)
     assert _lib.moe_forward(p, ins, outs, 1 << 44, 1 << 30, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0
+
+
+def test_training_flag_reserves_backward_buffers():
+    for name in ("switch", "mixtral", "deepseek", "tiny"):
+        cfg = config(name)
+        n0 = _lib.moe_workspace_size(make_params(cfg))[1]
+        n1 = _lib.moe_workspace_size(make_params(cfg, flags=_lib.MOE_FLAG_TRAINING))[1]
+        assert n1 > n0 + 4 * cfg.T * cfg.d  # at least the router's share of dx
+
+
+def _fake_grads(cfg, ins, base=1 << 41):
+    a = lambda i: base + i * (1 << 30)  # noqa: E731
+    return _lib.moe_grads_t(dx=a(0), dW_gate=a(1), db_gate=a(2) if ins.b_gate else None, dW1=a(3),
+                            dW3=a(4) if cfg.act == "swiglu" else None, dW2=a(5),
+                            db1=a(6) if ins.b1 else None, db2=a(7) if ins.b2 else None)
+
+
+def test_backward_validation_happens_before_any_launch():
+    cfg = config("mixtral")
+    p = make_params(cfg, flags=_lib.MOE_FLAG_TRAINING)
+    _, need = _lib.moe_workspace_size(p)
+    ins, outs = _fake_io(cfg)
+    dy = 1 << 42
+    n0 = _lib.moe_kernel_launches()
+    # no training flag
+    p0 = make_params(cfg)
+    assert _lib.moe_backward(p0, ins, outs, dy, 0.0, _fake_grads(cfg, ins), 1 << 44, need,
+                             None) == _lib.MOE_ERR_INVALID_ARG
+    # missing dy, non-finite d_aux, missing or extra gradient arrays, unaligned pointers
+    g = _fake_grads(cfg, ins)
+    assert _lib.moe_backward(p, ins, outs, None, 0.0, g, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_backward(p, ins, outs, dy, float("nan"), g, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+    for field, value in (("dW3", None), ("dx", None), ("db1", 1 << 43), ("dW_noise", 1 << 43),
+                         ("dW2", (1 << 43) + 4)):
+        g = _fake_grads(cfg, ins)
+        setattr(g, field, value)
+        assert _lib.moe_backward(p, ins, outs, dy, 0.0, g, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert _lib.moe_backward(p, ins, outs, dy, 0.0, _fake_grads(cfg, ins), 1 << 44, need - 1,
+                             None) == _lib.MOE_ERR_WORKSPACE
     assert _lib.moe_kernel_launches() == n0
