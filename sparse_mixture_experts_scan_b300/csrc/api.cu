@@ -596,6 +596,259 @@ const void* offset_elems(const void* p, size_t n, size_t esz)
     return p == nullptr ? nullptr : static_cast<const char*>(p) + n * esz;
 }
 
+// Routed and shared experts' backward on the tensor core (bf16 layers).
+cudaError_t experts_bwd_tc(Ctx& c, const void* dy, const moe_grads_t* gr)
+{
+    const Layout& L = c.L;
+    const size_t esz = L.esz;
+    const bool swiglu = c.p.act == MOE_ACT_SWIGLU;
+    void* dyp = c.at<void>(L.off_bw_dyp);
+    void* z1 = c.at<void>(L.off_bw_z1);
+    void* z3 = swiglu ? c.at<void>(L.off_bw_z3) : nullptr;
+    void* h = c.at<void>(L.off_h);
+    void* xp = c.at<void>(L.off_xp);
+    const int* mtile = c.at<int>(L.off_mtile);
+    const int* row_off = c.at<int>(L.off_row_off);
+    const int* kept = c.at<int>(L.off_kept);
+    const uint64_t R = (uint64_t)L.rows_cap, ES = (uint64_t)(L.E + L.S), SF = (uint64_t)L.S * L.F;
+    const int mt_routed = L.rows_cap / kSegRows;
+    auto grid_for = [&](long long tiles) { return (int)std::max(1ll, std::min(tiles, (long long)c.sms)); };
+    auto tiles = [](int M, int N) { return (long long)ceil_div(M, 128) * ceil_div(N, 256); };
+
+    // tensor maps: K-major A (box 64 x 128) and MN-major operands (box 64 x 64)
+    CUtensorMap kDyp, kZ1, kZ3, mDyp, mZ1, mZ3, mH, mXp, mW2, mW1, mW3;
+    bool ok = true;
+    if (R > 0)
+        ok = encode_bf16_2d(&kDyp, dyp, R, L.d, 128) && encode_bf16_2d(&kZ1, z1, R, L.F, 128) &&
+             encode_bf16_2d(&mDyp, dyp, R, L.d, 64) && encode_bf16_2d(&mZ1, z1, R, L.F, 64) &&
+             encode_bf16_2d(&mH, h, R, L.F, 64) && encode_bf16_2d(&mXp, xp, R, L.d, 64) &&
+             (!swiglu || (encode_bf16_2d(&kZ3, z3, R, L.F, 128) && encode_bf16_2d(&mZ3, z3, R, L.F, 64)));
+    ok = ok && encode_bf16_2d(&mW2, c.in->W2, ES * L.d, L.F, 64) && encode_bf16_2d(&mW1, c.in->W1, ES * L.F, L.d, 64) &&
+         (!swiglu || encode_bf16_2d(&mW3, c.in->W3, ES * L.F, L.d, 64));
+    if (!ok) return cudaErrorInvalidValue;
+    if (!swiglu) {
+        kZ3 = kZ1;
+        mZ3 = mZ1;
+        mW3 = mW1;
+    }
+
+    cudaError_t e = cudaSuccess;
+    auto bwd = [&](const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2,
+                   const BwdTcArgs& args, int mode, int epi, long long n_tiles) {
+        const CUtensorMap maps[4] = {a, b, a2, b2};
+        if (e == cudaSuccess) e = launch_gemm_bwd_tc(maps, args, mode, epi, grid_for(n_tiles), c.st, take_pdl(c));
+    };
+    BwdTcArgs rows{};  // row-grouped (dgrad) products over the expert segments
+    rows.mtile_off = mtile;
+    rows.row_off = row_off;
+    rows.rows = kept;
+    rows.G = L.E;
+    rows.err = c.err();
+    BwdTcArgs red = rows;  // products reduced over each segment's rows (wgrad)
+    red.mtile_off = nullptr;
+
+    if (R > 0) {
+        // the 64-row K blocks of the reductions read up to 63 rows past each segment's
+        // kept rows: make them zero in every operand
+        ZeroPadArgs zp{};
+        zp.row_off = row_off;
+        zp.rows = kept;
+        zp.G = L.E;
+        zp.buf[0] = dyp;
+        zp.buf[1] = h;
+        zp.buf[2] = xp;
+        zp.row_bytes[0] = (int)(L.d * esz);
+        zp.row_bytes[1] = (int)(L.F * esz);
+        zp.row_bytes[2] = (int)(L.d * esz);
+        e = launch_zero_pad_rows(zp, c.sms, c.st, take_pdl(c));
+    }
+    if (c.p.act != MOE_ACT_RELU && mt_routed > 0) {
+        // recompute the pre-activations with the forward's grouped GEMM (no activation)
+        GroupedGemmArgs g{};
+        g.mtile_off = mtile;
+        g.row_off = row_off;
+        g.rows = kept;
+        g.G = L.E;
+        g.N = L.F;
+        g.K = L.d;
+        g.k_segments = 1;
+        g.b_rows_per_group = L.F;
+        g.out = z1;
+        g.ldo = L.F;
+        g.bias = c.in->b1;
+        g.a_rows_alloc = L.rows_cap;
+        g.err = c.err();
+        const int bn = swiglu ? c.bn1 / 2 : c.bn1;  // the B maps' box height
+        g.n_tiles = ceil_div(L.F, bn);
+        const int grid = std::max(1, std::min(mt_routed * g.n_tiles, c.sms));
+        if (e == cudaSuccess) e = launch_gemm_tc(c.mA1, c.mB1, c.mB1, g, kActNone, bn, grid, c.st, take_pdl(c));
+        if (swiglu) {
+            g.out = z3;
+            if (e == cudaSuccess) e = launch_gemm_tc(c.mA1, c.mB3, c.mB3, g, kActNone, bn, grid, c.st, take_pdl(c));
+        }
+    }
+    {
+        BwdTcArgs a = red;  // dW2_e = dYp_e^T H_e
+        a.M = L.d;
+        a.N = L.F;
+        a.C = gr->dW2;
+        a.ldc = L.F;
+        a.c_gs = (long long)L.d * L.F;
+        if (R > 0) bwd(mDyp, mH, mDyp, mH, a, kBwdReduce, kEpiStore, L.E * tiles(a.M, a.N));
+        else if (e == cudaSuccess) e = cudaMemsetAsync(gr->dW2, 0, esz * L.E * L.d * L.F, c.st);
+    }
+    if (gr->db2 && e == cudaSuccess) {
+        ColsumArgs s{};
+        s.A = dyp;
+        s.lda = L.d;
+        s.row_off = row_off;
+        s.rows = kept;
+        s.G = L.E;
+        s.N = L.d;
+        s.out = gr->db2;
+        e = launch_colsum(s, kBwdTypesBf16, c.sms, c.st, take_pdl(c));
+    }
+    if (mt_routed > 0) {
+        BwdTcArgs a = rows;  // dH = dYp W2_e with the activation backward
+        a.N = L.F;
+        a.K = L.d;
+        a.b_rows_per_group = L.d;
+        a.C = z1;
+        a.ldc = L.F;
+        int epi;
+        if (c.p.act == MOE_ACT_RELU) {
+            epi = kEpiReluBwd;
+            a.e1 = h;
+        } else if (swiglu) {
+            epi = kEpiSwigluBwd;
+            a.e1 = z1;
+            a.e2 = z3;
+            a.C2 = z3;
+        } else {
+            epi = c.p.act == MOE_ACT_GELU_TANH ? kEpiGeluTanhBwd : kEpiGeluErfBwd;
+            a.e1 = z1;
+        }
+        bwd(kDyp, mW2, kDyp, mW2, a, kBwdRows, epi, (long long)mt_routed * ceil_div(a.N, 256));
+    }
+    {
+        BwdTcArgs a = red;  // dW1_e = dZ1_e^T Xp_e, dW3_e = dZ3_e^T Xp_e
+        a.M = L.F;
+        a.N = L.d;
+        a.C = gr->dW1;
+        a.ldc = L.d;
+        a.c_gs = (long long)L.F * L.d;
+        if (R > 0) {
+            bwd(mZ1, mXp, mZ1, mXp, a, kBwdReduce, kEpiStore, L.E * tiles(a.M, a.N));
+            if (swiglu) {
+                a.C = gr->dW3;
+                bwd(mZ3, mXp, mZ3, mXp, a, kBwdReduce, kEpiStore, L.E * tiles(a.M, a.N));
+            }
+        } else {
+            if (e == cudaSuccess) e = cudaMemsetAsync(gr->dW1, 0, esz * L.E * L.F * L.d, c.st);
+            if (swiglu && e == cudaSuccess) e = cudaMemsetAsync(gr->dW3, 0, esz * L.E * L.F * L.d, c.st);
+        }
+    }
+    if (gr->db1 && e == cudaSuccess) {
+        ColsumArgs s{};
+        s.A = z1;
+        s.lda = L.F;
+        s.row_off = row_off;
+        s.rows = kept;
+        s.G = L.E;
+        s.N = L.F;
+        s.out = gr->db1;
+        e = launch_colsum(s, kBwdTypesBf16, c.sms, c.st, take_pdl(c));
+    }
+    if (mt_routed > 0) {
+        BwdTcArgs a = rows;  // dXp = dZ1 W1_e (+ dZ3 W3_e), into the dYp buffer
+        a.N = L.d;
+        a.K = L.F;
+        a.b_rows_per_group = L.F;
+        a.two_seg = swiglu ? 1 : 0;
+        a.C = dyp;
+        a.ldc = L.d;
+        bwd(kZ1, mW1, kZ3, mW3, a, kBwdRows, kEpiStore, (long long)mt_routed * ceil_div(a.N, 256));
+    }
+
+    if (L.S > 0) {
+        // shared experts: one group of all T tokens, gate 1, SwiGLU, hidden S*F
+        void* zs1 = c.at<void>(L.off_bw_zs1);
+        void* zs3 = c.at<void>(L.off_bw_zs3);
+        void* dxs = c.at<void>(L.off_bw_dxs);
+        const uint64_t T = (uint64_t)L.T;
+        CUtensorMap kDy, mDy, kZs1, kZs3, mZs1, mZs3, mHs, mX;
+        ok = encode_bf16_2d(&kDy, dy, T, L.d, 128) && encode_bf16_2d(&mDy, dy, T, L.d, 64) &&
+             encode_bf16_2d(&kZs1, zs1, T, SF, 128) && encode_bf16_2d(&kZs3, zs3, T, SF, 128) &&
+             encode_bf16_2d(&mZs1, zs1, T, SF, 64) && encode_bf16_2d(&mZs3, zs3, T, SF, 64) &&
+             encode_bf16_2d(&mHs, c.at<void>(L.off_hs), T, SF, 64) && encode_bf16_2d(&mX, c.in->x, T, L.d, 64);
+        if (!ok) return cudaErrorInvalidValue;
+        GroupedGemmArgs g{};  // z = x W^T over the S*F concatenated rows
+        g.G = 1;
+        g.fixed_rows = L.T;
+        g.N = (int)SF;
+        g.K = L.d;
+        g.k_segments = 1;
+        g.b_rows_per_group = L.F;
+        g.b_group0 = L.E;
+        g.out = zs1;
+        g.ldo = (int)SF;
+        g.a_rows_alloc = L.T;
+        g.err = c.err();
+        const int bn = c.bn1 / 2;  // SwiGLU: the W1 / W3 maps' box height
+        g.n_tiles = ceil_div((int)SF, bn);
+        const int grid = std::max(1, std::min(ceil_div(L.T, 128) * g.n_tiles, c.sms));
+        if (e == cudaSuccess) e = launch_gemm_tc(c.mAs1, c.mB1, c.mB1, g, kActNone, bn, grid, c.st, take_pdl(c));
+        g.out = zs3;
+        if (e == cudaSuccess) e = launch_gemm_tc(c.mAs1, c.mB3, c.mB3, g, kActNone, bn, grid, c.st, take_pdl(c));
+        BwdTcArgs f{};
+        f.G = 1;
+        f.fixed_rows = L.T;
+        f.err = c.err();
+        for (int sh = 0; sh < L.S; ++sh) {
+            BwdTcArgs w = f;  // dW2_s = dy^T H_s (columns s*F .. of the shared hidden)
+            w.M = L.d;
+            w.N = L.F;
+            w.b_col0 = sh * L.F;
+            w.C = gr->dW2;
+            w.c_g0 = L.E + sh;
+            w.c_gs = (long long)L.d * L.F;
+            w.ldc = L.F;
+            bwd(mDy, mHs, mDy, mHs, w, kBwdReduce, kEpiStore, tiles(w.M, w.N));
+            BwdTcArgs a = f;  // dH_s = dy W2_s with the SwiGLU backward, in place
+            a.N = L.F;
+            a.K = L.d;
+            a.b_g0 = L.E + sh;
+            a.b_rows_per_group = L.d;
+            a.C = const_cast<void*>(offset_elems(zs1, (size_t)sh * L.F, esz));
+            a.C2 = const_cast<void*>(offset_elems(zs3, (size_t)sh * L.F, esz));
+            a.e1 = a.C;
+            a.e2 = a.C2;
+            a.ldc = (long long)SF;
+            bwd(kDy, mW2, kDy, mW2, a, kBwdRows, kEpiSwigluBwd, (long long)ceil_div(L.T, 128) * ceil_div(L.F, 256));
+        }
+        BwdTcArgs w = f;  // dW1_s = dZs1^T x, dW3_s = dZs3^T x
+        w.M = (int)SF;
+        w.N = L.d;
+        w.C = gr->dW1;
+        w.c_g0 = L.E;
+        w.c_gs = (long long)L.F * L.d;
+        w.ldc = L.d;
+        bwd(mZs1, mX, mZs1, mX, w, kBwdReduce, kEpiStore, tiles(w.M, w.N));
+        w.C = gr->dW3;
+        bwd(mZs3, mX, mZs3, mX, w, kBwdReduce, kEpiStore, tiles(w.M, w.N));
+        BwdTcArgs a = f;  // dXs = dZs1 W1_s + dZs3 W3_s
+        a.N = L.d;
+        a.K = (int)SF;
+        a.b_g0 = L.E;
+        a.b_rows_per_group = L.F;
+        a.two_seg = 1;
+        a.C = dxs;
+        a.ldc = L.d;
+        bwd(kZs1, mW1, kZs3, mW3, a, kBwdRows, kEpiStore, (long long)ceil_div(L.T, 128) * ceil_div(L.d, 256));
+    }
+    return e;
+}
+
 moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t* gr)
 {
     const Layout& L = c.L;
@@ -714,246 +967,250 @@ moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t
         gemm(r, kBwdTypesF32, tiles(r.M, r.N));
     }
 
-    // routed experts
-    BwdGemmArgs rows{};  // row-grouped products over the expert segments
-    rows.mode = kBwdRows;
-    rows.mtile_off = mtile;
-    rows.row_off = row_off;
-    rows.rows = kept;
-    rows.G = L.E;
-    BwdGemmArgs red = rows;  // products reduced over the rows of each segment
-    red.mode = kBwdReduce;
-    const long long mt_tiles = mt_routed;
-    if (c.p.act != MOE_ACT_RELU) {  // recompute the pre-activations z1 (+ b1) and z3
-        BwdGemmArgs a = rows;
-        a.epi = kEpiStore;
-        a.A = c.at<void>(L.off_xp);
-        a.a_sm = L.d;
-        a.a_sk = 1;
-        a.B = c.in->W1;
-        a.b_sk = 1;
-        a.b_sn = L.d;
-        a.b_gs = (long long)L.F * L.d;
-        a.C = z1;
-        a.c_sm = L.F;
-        a.bias = c.in->b1;
-        a.N = L.F;
-        a.K = L.d;
-        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
-        if (swiglu) {
-            a.B = c.in->W3;
-            a.C = z3;
-            a.bias = nullptr;
+    void* dxs = L.S > 0 ? c.at<void>(L.off_bw_dxs) : nullptr;
+    if (c.use_tc) {
+        if (e == cudaSuccess) e = experts_bwd_tc(c, dy, gr);
+    } else {
+        // routed experts
+        BwdGemmArgs rows{};  // row-grouped products over the expert segments
+        rows.mode = kBwdRows;
+        rows.mtile_off = mtile;
+        rows.row_off = row_off;
+        rows.rows = kept;
+        rows.G = L.E;
+        BwdGemmArgs red = rows;  // products reduced over the rows of each segment
+        red.mode = kBwdReduce;
+        const long long mt_tiles = mt_routed;
+        if (c.p.act != MOE_ACT_RELU) {  // recompute the pre-activations z1 (+ b1) and z3
+            BwdGemmArgs a = rows;
+            a.epi = kEpiStore;
+            a.A = c.at<void>(L.off_xp);
+            a.a_sm = L.d;
+            a.a_sk = 1;
+            a.B = c.in->W1;
+            a.b_sk = 1;
+            a.b_sn = L.d;
+            a.b_gs = (long long)L.F * L.d;
+            a.C = z1;
+            a.c_sm = L.F;
+            a.bias = c.in->b1;
+            a.N = L.F;
+            a.K = L.d;
             gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+            if (swiglu) {
+                a.B = c.in->W3;
+                a.C = z3;
+                a.bias = nullptr;
+                gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+            }
         }
-    }
-    {
-        BwdGemmArgs a = red;  // dW2_e = dYp_e^T H_e
-        a.epi = kEpiStore;
-        a.A = dyp;
-        a.a_sm = 1;
-        a.a_sk = L.d;
-        a.B = c.at<void>(L.off_h);
-        a.b_sk = L.F;
-        a.b_sn = 1;
-        a.C = gr->dW2;
-        a.c_gs = (long long)L.d * L.F;
-        a.c_sm = L.F;
-        a.M = L.d;
-        a.N = L.F;
-        gemm(a, types, L.E * tiles(a.M, a.N));
-    }
-    if (gr->db2) {
-        ColsumArgs s{};
-        s.A = dyp;
-        s.lda = L.d;
-        s.row_off = row_off;
-        s.rows = kept;
-        s.G = L.E;
-        s.N = L.d;
-        s.out = gr->db2;
-        colsum(s, types);
-    }
-    {
-        BwdGemmArgs a = rows;  // dH = dYp W2_e, then the activation backward
-        a.A = dyp;
-        a.a_sm = L.d;
-        a.a_sk = 1;
-        a.B = c.in->W2;
-        a.b_sk = L.F;
-        a.b_sn = 1;
-        a.b_gs = (long long)L.d * L.F;
-        a.C = z1;
-        a.c_sm = L.F;
-        a.N = L.F;
-        a.K = L.d;
-        if (c.p.act == MOE_ACT_RELU) {
-            a.epi = kEpiReluBwd;
-            a.e1 = c.at<void>(L.off_h);
-        } else if (swiglu) {
-            a.epi = kEpiSwigluBwd;
-            a.e1 = z1;
-            a.e2 = z3;
-            a.C2 = z3;
-        } else {
-            a.epi = c.p.act == MOE_ACT_GELU_TANH ? kEpiGeluTanhBwd : kEpiGeluErfBwd;
-            a.e1 = z1;
-        }
-        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
-    }
-    {
-        BwdGemmArgs a = red;  // dW1_e = dZ1_e^T Xp_e (and dW3_e from dZ3)
-        a.epi = kEpiStore;
-        a.A = z1;
-        a.a_sm = 1;
-        a.a_sk = L.F;
-        a.B = c.at<void>(L.off_xp);
-        a.b_sk = L.d;
-        a.b_sn = 1;
-        a.C = gr->dW1;
-        a.c_gs = (long long)L.F * L.d;
-        a.c_sm = L.d;
-        a.M = L.F;
-        a.N = L.d;
-        gemm(a, types, L.E * tiles(a.M, a.N));
-        if (swiglu) {
-            a.A = z3;
-            a.C = gr->dW3;
+        {
+            BwdGemmArgs a = red;  // dW2_e = dYp_e^T H_e
+            a.epi = kEpiStore;
+            a.A = dyp;
+            a.a_sm = 1;
+            a.a_sk = L.d;
+            a.B = c.at<void>(L.off_h);
+            a.b_sk = L.F;
+            a.b_sn = 1;
+            a.C = gr->dW2;
+            a.c_gs = (long long)L.d * L.F;
+            a.c_sm = L.F;
+            a.M = L.d;
+            a.N = L.F;
             gemm(a, types, L.E * tiles(a.M, a.N));
         }
-    }
-    if (gr->db1) {
-        ColsumArgs s{};
-        s.A = z1;
-        s.lda = L.F;
-        s.row_off = row_off;
-        s.rows = kept;
-        s.G = L.E;
-        s.N = L.F;
-        s.out = gr->db1;
-        colsum(s, types);
-    }
-    {
-        BwdGemmArgs a = rows;  // dXp = dZ1 W1_e (+ dZ3 W3_e), into the dYp buffer
-        a.epi = kEpiStore;
-        a.A = z1;
-        a.A2 = z3;
-        a.a_sm = L.F;
-        a.a_sk = 1;
-        a.B = c.in->W1;
-        a.B2 = swiglu ? c.in->W3 : nullptr;
-        a.b_sk = L.d;
-        a.b_sn = 1;
-        a.b_gs = (long long)L.F * L.d;
-        a.C = dyp;
-        a.c_sm = L.d;
-        a.N = L.d;
-        a.K = L.F;
-        gemm(a, types, mt_tiles * ceil_div(a.N, 64));
-    }
+        if (gr->db2) {
+            ColsumArgs s{};
+            s.A = dyp;
+            s.lda = L.d;
+            s.row_off = row_off;
+            s.rows = kept;
+            s.G = L.E;
+            s.N = L.d;
+            s.out = gr->db2;
+            colsum(s, types);
+        }
+        {
+            BwdGemmArgs a = rows;  // dH = dYp W2_e, then the activation backward
+            a.A = dyp;
+            a.a_sm = L.d;
+            a.a_sk = 1;
+            a.B = c.in->W2;
+            a.b_sk = L.F;
+            a.b_sn = 1;
+            a.b_gs = (long long)L.d * L.F;
+            a.C = z1;
+            a.c_sm = L.F;
+            a.N = L.F;
+            a.K = L.d;
+            if (c.p.act == MOE_ACT_RELU) {
+                a.epi = kEpiReluBwd;
+                a.e1 = c.at<void>(L.off_h);
+            } else if (swiglu) {
+                a.epi = kEpiSwigluBwd;
+                a.e1 = z1;
+                a.e2 = z3;
+                a.C2 = z3;
+            } else {
+                a.epi = c.p.act == MOE_ACT_GELU_TANH ? kEpiGeluTanhBwd : kEpiGeluErfBwd;
+                a.e1 = z1;
+            }
+            gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+        }
+        {
+            BwdGemmArgs a = red;  // dW1_e = dZ1_e^T Xp_e (and dW3_e from dZ3)
+            a.epi = kEpiStore;
+            a.A = z1;
+            a.a_sm = 1;
+            a.a_sk = L.F;
+            a.B = c.at<void>(L.off_xp);
+            a.b_sk = L.d;
+            a.b_sn = 1;
+            a.C = gr->dW1;
+            a.c_gs = (long long)L.F * L.d;
+            a.c_sm = L.d;
+            a.M = L.F;
+            a.N = L.d;
+            gemm(a, types, L.E * tiles(a.M, a.N));
+            if (swiglu) {
+                a.A = z3;
+                a.C = gr->dW3;
+                gemm(a, types, L.E * tiles(a.M, a.N));
+            }
+        }
+        if (gr->db1) {
+            ColsumArgs s{};
+            s.A = z1;
+            s.lda = L.F;
+            s.row_off = row_off;
+            s.rows = kept;
+            s.G = L.E;
+            s.N = L.F;
+            s.out = gr->db1;
+            colsum(s, types);
+        }
+        {
+            BwdGemmArgs a = rows;  // dXp = dZ1 W1_e (+ dZ3 W3_e), into the dYp buffer
+            a.epi = kEpiStore;
+            a.A = z1;
+            a.A2 = z3;
+            a.a_sm = L.F;
+            a.a_sk = 1;
+            a.B = c.in->W1;
+            a.B2 = swiglu ? c.in->W3 : nullptr;
+            a.b_sk = L.d;
+            a.b_sn = 1;
+            a.b_gs = (long long)L.F * L.d;
+            a.C = dyp;
+            a.c_sm = L.d;
+            a.N = L.d;
+            a.K = L.F;
+            gemm(a, types, mt_tiles * ceil_div(a.N, 64));
+        }
 
-    // shared experts: gate 1 on every token (SwiGLU), hidden S*F, dO = dy
-    void* dxs = nullptr;
-    if (L.S > 0) {
-        void* zs1 = c.at<void>(L.off_bw_zs1);
-        void* zs3 = c.at<void>(L.off_bw_zs3);
-        dxs = c.at<void>(L.off_bw_dxs);
-        const long long SF = (long long)L.S * L.F;
-        BwdGemmArgs a{};
-        a.mode = kBwdFixed;
-        a.epi = kEpiStore;
-        a.A = c.in->x;  // z = x W^T over the S*F concatenated rows
-        a.a_sm = L.d;
-        a.a_sk = 1;
-        a.B = c.in->W1;
-        a.b_sk = 1;
-        a.b_sn = L.d;
-        a.b_gs = (long long)L.F * L.d;
-        a.b_g0 = L.E;
-        a.C = zs1;
-        a.c_sm = SF;
-        a.M = L.T;
-        a.N = (int)SF;
-        a.K = L.d;
-        gemm(a, types, tiles(a.M, a.N));
-        a.B = c.in->W3;
-        a.C = zs3;
-        gemm(a, types, tiles(a.M, a.N));
-        for (int sh = 0; sh < L.S; ++sh) {
-            BwdGemmArgs b{};  // dH_s = dy W2_s with the SwiGLU backward, on columns s*F ..
-            b.mode = kBwdFixed;
-            b.epi = kEpiSwigluBwd;
-            b.A = dy;
-            b.a_sm = L.d;
-            b.a_sk = 1;
-            b.B = c.in->W2;
-            b.b_sk = L.F;
-            b.b_sn = 1;
-            b.b_gs = (long long)L.d * L.F;
-            b.b_g0 = L.E + sh;
-            b.C = const_cast<void*>(offset_elems(zs1, (size_t)sh * L.F, esz));
-            b.C2 = const_cast<void*>(offset_elems(zs3, (size_t)sh * L.F, esz));
-            b.e1 = b.C;
-            b.e2 = b.C2;
-            b.c_sm = SF;
-            b.M = L.T;
-            b.N = L.F;
-            b.K = L.d;
-            // dW2_s = dy^T H_s first (it reads H_s, which the SwiGLU backward leaves alone)
-            BwdGemmArgs w{};
+        // shared experts: gate 1 on every token (SwiGLU), hidden S*F, dO = dy
+        if (L.S > 0) {
+            void* zs1 = c.at<void>(L.off_bw_zs1);
+            void* zs3 = c.at<void>(L.off_bw_zs3);
+            const long long SF = (long long)L.S * L.F;
+            BwdGemmArgs a{};
+            a.mode = kBwdFixed;
+            a.epi = kEpiStore;
+            a.A = c.in->x;  // z = x W^T over the S*F concatenated rows
+            a.a_sm = L.d;
+            a.a_sk = 1;
+            a.B = c.in->W1;
+            a.b_sk = 1;
+            a.b_sn = L.d;
+            a.b_gs = (long long)L.F * L.d;
+            a.b_g0 = L.E;
+            a.C = zs1;
+            a.c_sm = SF;
+            a.M = L.T;
+            a.N = (int)SF;
+            a.K = L.d;
+            gemm(a, types, tiles(a.M, a.N));
+            a.B = c.in->W3;
+            a.C = zs3;
+            gemm(a, types, tiles(a.M, a.N));
+            for (int sh = 0; sh < L.S; ++sh) {
+                BwdGemmArgs b{};  // dH_s = dy W2_s with the SwiGLU backward, on columns s*F ..
+                b.mode = kBwdFixed;
+                b.epi = kEpiSwigluBwd;
+                b.A = dy;
+                b.a_sm = L.d;
+                b.a_sk = 1;
+                b.B = c.in->W2;
+                b.b_sk = L.F;
+                b.b_sn = 1;
+                b.b_gs = (long long)L.d * L.F;
+                b.b_g0 = L.E + sh;
+                b.C = const_cast<void*>(offset_elems(zs1, (size_t)sh * L.F, esz));
+                b.C2 = const_cast<void*>(offset_elems(zs3, (size_t)sh * L.F, esz));
+                b.e1 = b.C;
+                b.e2 = b.C2;
+                b.c_sm = SF;
+                b.M = L.T;
+                b.N = L.F;
+                b.K = L.d;
+                // dW2_s = dy^T H_s first (it reads H_s, which the SwiGLU backward leaves alone)
+                BwdGemmArgs w{};
+                w.mode = kBwdFixed;
+                w.epi = kEpiStore;
+                w.A = dy;
+                w.a_sm = 1;
+                w.a_sk = L.d;
+                w.B = offset_elems(c.at<void>(L.off_hs), (size_t)sh * L.F, esz);
+                w.b_sk = SF;
+                w.b_sn = 1;
+                w.C = const_cast<void*>(offset_elems(gr->dW2, (size_t)(L.E + sh) * L.d * L.F, esz));
+                w.c_sm = L.F;
+                w.M = L.d;
+                w.N = L.F;
+                w.K = L.T;
+                gemm(w, types, tiles(w.M, w.N));
+                gemm(b, types, tiles(b.M, b.N));
+            }
+            BwdGemmArgs w{};  // dW1_s = dZs1^T x, dW3_s = dZs3^T x over the S*F rows
             w.mode = kBwdFixed;
             w.epi = kEpiStore;
-            w.A = dy;
+            w.A = zs1;
             w.a_sm = 1;
-            w.a_sk = L.d;
-            w.B = offset_elems(c.at<void>(L.off_hs), (size_t)sh * L.F, esz);
-            w.b_sk = SF;
+            w.a_sk = SF;
+            w.B = c.in->x;
+            w.b_sk = L.d;
             w.b_sn = 1;
-            w.C = const_cast<void*>(offset_elems(gr->dW2, (size_t)(L.E + sh) * L.d * L.F, esz));
-            w.c_sm = L.F;
-            w.M = L.d;
-            w.N = L.F;
+            w.C = const_cast<void*>(offset_elems(gr->dW1, (size_t)L.E * L.F * L.d, esz));
+            w.c_sm = L.d;
+            w.M = (int)SF;
+            w.N = L.d;
             w.K = L.T;
             gemm(w, types, tiles(w.M, w.N));
-            gemm(b, types, tiles(b.M, b.N));
+            w.A = zs3;
+            w.C = const_cast<void*>(offset_elems(gr->dW3, (size_t)L.E * L.F * L.d, esz));
+            gemm(w, types, tiles(w.M, w.N));
+            BwdGemmArgs x{};  // dXs = dZs1 W1_s + dZs3 W3_s
+            x.mode = kBwdFixed;
+            x.epi = kEpiStore;
+            x.A = zs1;
+            x.A2 = zs3;
+            x.a_sm = SF;
+            x.a_sk = 1;
+            x.B = c.in->W1;
+            x.B2 = c.in->W3;
+            x.b_sk = L.d;
+            x.b_sn = 1;
+            x.b_gs = (long long)L.F * L.d;
+            x.b_g0 = L.E;
+            x.C = dxs;
+            x.c_sm = L.d;
+            x.M = L.T;
+            x.N = L.d;
+            x.K = (int)SF;
+            gemm(x, types, tiles(x.M, x.N));
         }
-        BwdGemmArgs w{};  // dW1_s = dZs1^T x, dW3_s = dZs3^T x over the S*F rows
-        w.mode = kBwdFixed;
-        w.epi = kEpiStore;
-        w.A = zs1;
-        w.a_sm = 1;
-        w.a_sk = SF;
-        w.B = c.in->x;
-        w.b_sk = L.d;
-        w.b_sn = 1;
-        w.C = const_cast<void*>(offset_elems(gr->dW1, (size_t)L.E * L.F * L.d, esz));
-        w.c_sm = L.d;
-        w.M = (int)SF;
-        w.N = L.d;
-        w.K = L.T;
-        gemm(w, types, tiles(w.M, w.N));
-        w.A = zs3;
-        w.C = const_cast<void*>(offset_elems(gr->dW3, (size_t)L.E * L.F * L.d, esz));
-        gemm(w, types, tiles(w.M, w.N));
-        BwdGemmArgs x{};  // dXs = dZs1 W1_s + dZs3 W3_s
-        x.mode = kBwdFixed;
-        x.epi = kEpiStore;
-        x.A = zs1;
-        x.A2 = zs3;
-        x.a_sm = SF;
-        x.a_sk = 1;
-        x.B = c.in->W1;
-        x.B2 = c.in->W3;
-        x.b_sk = L.d;
-        x.b_sn = 1;
-        x.b_gs = (long long)L.F * L.d;
-        x.b_g0 = L.E;
-        x.C = dxs;
-        x.c_sm = L.d;
-        x.M = L.T;
-        x.N = L.d;
-        x.K = (int)SF;
-        gemm(x, types, tiles(x.M, x.N));
+
     }
 
     BwdUnpermuteArgs u{};

@@ -190,6 +190,27 @@ __global__ void __launch_bounds__(256) k_bwd_unpermute(BwdUnpermuteArgs a)
     }
 }
 
+// One warp per (segment, pad row below the next 64-row boundary); 16-byte stores.
+__global__ void __launch_bounds__(256) k_zero_pad_rows(ZeroPadArgs a)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int items = a.G * 64;
+    for (int it = blockIdx.x * 8 + warp; it < items; it += gridDim.x * 8) {
+        const int g = it >> 6, p = it & 63;
+        const int kept = a.rows[g];
+        const int end = (kept + 63) / 64 * 64;
+        if (kept + p >= end) continue;
+        const long long row = (long long)a.row_off[g] + kept + p;
+        for (int b = 0; b < 3; ++b) {
+            if (a.buf[b] == nullptr) continue;
+            uint4* r = reinterpret_cast<uint4*>(static_cast<char*>(a.buf[b]) + row * a.row_bytes[b]);
+            for (int v = lane; v < a.row_bytes[b] / 16; v += 32) r[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
 int warp_grid(int T, int sms)
 {
     const int g = ceil_div(T, 8);
@@ -226,6 +247,12 @@ cudaError_t launch_colsum(const ColsumArgs& a, int types, int sms, cudaStream_t 
     case kBwdTypesBf16: return launch_kernel(k_colsum<__nv_bfloat16, __nv_bfloat16>, g, b, 0, st, pdl, a);
     default: return launch_kernel(k_colsum<float, float>, g, b, 0, st, pdl, a);
     }
+}
+
+cudaError_t launch_zero_pad_rows(const ZeroPadArgs& a, int sms, cudaStream_t st, bool pdl)
+{
+    const dim3 grid(warp_grid(a.G * 64, sms)), block(256);
+    return launch_kernel(k_zero_pad_rows, grid, block, 0, st, pdl, a);
 }
 
 cudaError_t launch_bwd_unpermute(const BwdUnpermuteArgs& a, bool bf16, int sms, cudaStream_t st, bool pdl)

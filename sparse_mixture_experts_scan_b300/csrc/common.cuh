@@ -264,6 +264,23 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile stored with the
+// 128-byte swizzle, as TMA writes a box of 64 MN-contiguous bf16 (128 B) by 64
+// K-rows: one 8 KB block per 64 MN elements.  Inside a block, K-rows are 128 B
+// apart and 8-row K groups 1024 B apart (stride-dimension offset); consecutive
+// 64-element MN blocks are 8192 B apart (leading-dimension offset).  A K-step of
+// 16 advances the start address by 16 rows = 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -271,6 +288,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+// The same with A and/or B MN-major (bit 15: A, bit 16: B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, bool a_mn, bool b_mn)
+{
+    return idesc_bf16_f32(M, N) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.

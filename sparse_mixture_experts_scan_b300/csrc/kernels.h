@@ -173,6 +173,44 @@ struct BwdGemmArgs {
 };
 cudaError_t launch_gemm_bwd_ffma(const BwdGemmArgs& a, int types, int grid, cudaStream_t st, bool pdl);
 
+// tcgen05 version for bf16 (BM = 128, BN = 256, BK = 64).  maps = {A, B, A2, B2}:
+//   kBwdRows:   A K-major (box {64, 128}) over the activation-gradient rows; B MN-major
+//               (box {64, 64}) over a weight viewed [groups * b_rows_per_group, N-extent];
+//               B row of (group g, k) = (b_g0 + g) * b_rows_per_group + k, column b_col0 + n.
+//               row_off == nullptr: one group of fixed_rows rows from row 0.
+//   kBwdReduce: A and B MN-major (box {64, 64}) over row-major activation buffers; the
+//               reduction runs over rows [row_off[g], row_off[g] + rows[g]) (or [0, fixed_rows));
+//               output rows m < M of C + (c_g0 + g) * c_gs, leading dimension ldc.
+struct BwdTcArgs {
+    const int* mtile_off;
+    const int* row_off;
+    const int* rows;
+    int G, fixed_rows;
+    int M, N, K;
+    int b_g0, b_rows_per_group, b_col0;
+    int two_seg;
+    void* C;
+    void* C2;
+    const void* e1;
+    const void* e2;
+    long long ldc, c_gs;
+    int c_g0;
+    uint32_t* err;
+};
+cudaError_t launch_gemm_bwd_tc(const CUtensorMap* maps, const BwdTcArgs& a, int mode, int epi, int grid,
+                               cudaStream_t st, bool pdl);
+
+// Zero rows [rows[e], ceil(rows[e] / 64) * 64) of each expert segment in up to three
+// row-major buffers (the rows a 64-row K block of a reduction reads past the kept rows).
+struct ZeroPadArgs {
+    const int* row_off;
+    const int* rows;
+    int G;
+    void* buf[3];
+    int row_bytes[3];
+};
+cudaError_t launch_zero_pad_rows(const ZeroPadArgs& a, int sms, cudaStream_t st, bool pdl);
+
 // ---- backward: memory-bound kernels ---------------------------------------------
 struct BwdCombineArgs {
     const void* dy;        // [T, d]

@@ -144,3 +144,31 @@ def test_aux_gradient_alone_reaches_only_the_router():
     ref = oracle_grads(cfg, inp, out, dy, 1.0)
     assert rel_frobenius(grads["dW_gate"].double().numpy(), ref["dW_gate"]) <= 1e-3
     assert rel_frobenius(grads["dx"].double().numpy(), ref["dx"]) <= 2e-2
+
+
+@pytest.mark.parametrize("name", ["relu_capacity_k1", "swiglu_shared", "gelu_tanh_bias_ragged",
+                                  "many_experts_drops", "noisy_switch_capacity"])
+def test_backward_ffma_experts_match_oracle(name):
+    # the CUDA-core cross-check path of the expert backward (bf16 layers)
+    cfg = CASES[name]
+    inp = _inputs(cfg)
+    dy = _dy(cfg)
+    layer = MoELayer(cfg, inp, flags=TRAIN | _lib.MOE_FLAG_FFMA_EXPERTS)
+    layer.run()
+    grads = to_cpu(layer.backward(dy, 0.37))
+    torch.cuda.synchronize()
+    assert layer.device_status() == _lib.MOE_OK
+    out = to_cpu(layer.out)
+    compare(cfg, grads, oracle_grads(cfg, inp, out, dy, 0.37), out)
+
+
+@pytest.mark.parametrize("name", ["relu_capacity_k1", "swiglu_shared", "gelu_tanh_bias_ragged"])
+def test_tensor_core_and_ffma_backward_agree(name):
+    cfg = CASES[name]
+    inp = _inputs(cfg)
+    dy = _dy(cfg)
+    _, g_tc, _ = run_backward(cfg, inp, dy, 0.37)
+    _, g_ff, _ = run_backward(cfg, inp, dy, 0.37, flags=_lib.MOE_FLAG_FFMA_EXPERTS)
+    for k, v in g_tc.items():
+        if v is not None:
+            assert rel_frobenius(v.double().numpy(), g_ff[k].double().numpy()) <= 1e-2, k
