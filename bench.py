@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--noisy", action="store_true",
                     help="noisy top-k gating (training-mode router; noise floor 0.01)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time a training step instead: moe_forward + moe_backward")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each stage directly instead of replaying a captured CUDA graph")
     return ap.parse_args()
@@ -607,10 +609,122 @@ def run_gpu(args):
     return 0
 
 
+def backward_work(cfg, out):
+    """Minimum work of the backward's expert stage for this batch.
+
+    Flops: dgrad and wgrad of every expert matrix on the kept rows (2 x the
+    forward's), plus the recomputed pre-activations (GELU: W1; SwiGLU: W1, W3).
+    Bytes: the weights of touched experts read once, every weight gradient
+    written once (untouched experts get zeros), and the row activations read or
+    written once: Xp, H, dYp, dXp (d, F, d, d per kept row)."""
+    import torch
+    kept = (out["dropped"] == 0)
+    idx = out["expert_idx"].long()
+    kept_per_e = torch.zeros(cfg.E, dtype=torch.long, device=idx.device)
+    kept_per_e.scatter_add_(0, idx[kept], torch.ones_like(idx[kept]))
+    touched = int((kept_per_e > 0).sum()) + cfg.S
+    rows = int(kept.sum()) + cfg.S * cfg.T
+    esz = 2 if cfg.dtype == "bf16" else 4
+    nmat = 3 if cfg.act == "swiglu" else 2
+    n_pre = {"relu": 0, "swiglu": 2}.get(cfg.act, 1)
+    flops = 2.0 * rows * cfg.d * cfg.F * (2 * nmat + n_pre)
+    w = nmat * cfg.d * cfg.F * esz
+    nbytes = touched * w + (cfg.E + cfg.S) * w + rows * esz * (3 * cfg.d + cfg.F)
+    return {"flops": flops, "bytes": nbytes, "rows": rows, "touched_experts": touched}
+
+
+def run_gpu_backward(args):
+    """Training step of the layer: moe_forward + moe_backward, CUDA graph per step."""
+    import torch
+
+    from sparse_mixture_experts_scan_b300 import MoELayer, _lib, make_inputs
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = bench_config(args)
+    inp = make_inputs(cfg, seed=rank, device=dev)
+    layer = MoELayer(cfg, inp, device=dev, flags=_lib.MOE_FLAG_TRAINING)
+    g = torch.Generator(device=dev).manual_seed(100 + rank)
+    dy = torch.randn(cfg.T, cfg.d, generator=g, device=dev).to(cfg.torch_dtype)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 1)):
+        layer.run("moe_forward")
+        layer.backward(dy, 0.01)
+    torch.cuda.synchronize()
+    n0 = _lib.moe_kernel_launches()
+    g_fwd, g_bwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fwd):
+        layer.run("moe_forward")
+    with torch.cuda.graph(g_bwd):
+        layer.backward(dy, 0.01)
+    launches = _lib.moe_kernel_launches() - n0
+    for _ in range(2):
+        g_fwd.replay()
+        g_bwd.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    nvml = NvmlSampler(dev.index)
+    with nvml:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            g_fwd.replay()
+            ev[i][1].record(stream)
+            g_bwd.replay()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    ms = fwd_ms + bwd_ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = layer.device_status()
+    if status != 0:
+        print(f"device status {status}", file=sys.stderr)
+        return 1
+    if rank != 0:
+        return 0
+    work = backward_work(cfg, layer.out)
+    pk = peaks()
+    hbm_bound = work["flops"] / work["bytes"] < pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if hbm_bound:
+        ach = work["bytes"] / (bwd_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
+    else:
+        ach = work["flops"] / (bwd_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"]}
+    roof.update({"traffic": None, "kernel": "the whole moe_backward call (every backward kernel; expert work only "
+                 "counted)", "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"],
+                 "peak_source": pk["source"] + " (burst)"})
+    line = {
+        "metric": "MoE layer training step (fwd + bwd) tokens/s on 1 B300", "value": world * cfg.T / (ms * 1e-3),
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; shapes and distributions of the workload; random-init weights)",
+        "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                   "l2": "flushed before each step", "launch": "CUDA graphs of moe_forward and moe_backward"},
+        "roofline": roof, "gpu_launches": launches * K, "clocks": nvml.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.backward:
+        return run_gpu_backward(args)
     return run_gpu(args)
 
 
