@@ -49,6 +49,9 @@ struct Layout {
     // relu: dZ1 only), shared-expert pre-activations and input gradient
     size_t off_bw_dgate, off_bw_dl, off_bw_dn, off_bw_dxr, off_bw_dyp, off_bw_z1, off_bw_z3, off_bw_zs1,
         off_bw_zs3, off_bw_dxs;
+    // router gradients on the tensor core: split gradients, paired weights, dW partials
+    int e8, r_nblk;
+    size_t off_bw_dcat, off_bw_wcat, off_bw_p;
     size_t total;
 };
 
@@ -155,6 +158,12 @@ Layout make_layout(const moe_params_t& p)
     L.off_bw_zs1 = bw(L.S > 0 ? L.esz * (size_t)L.T * L.S * L.F : 0);
     L.off_bw_zs3 = bw(L.S > 0 ? L.esz * (size_t)L.T * L.S * L.F : 0);
     L.off_bw_dxs = bw(L.S > 0 ? L.esz * (size_t)L.T * L.d : 0);
+    L.e8 = (L.E + 7) / 8 * 8;
+    L.r_nblk = noisy ? 8 : 4;
+    const bool tcr = train && L.tc_router;
+    L.off_bw_dcat = take(tcr ? sizeof(uint16_t) * (size_t)L.T * L.r_nblk * L.e8 : 0);
+    L.off_bw_wcat = take(tcr ? sizeof(uint16_t) * (size_t)L.r_nblk * L.e8 * L.d : 0);
+    L.off_bw_p = take(tcr ? sizeof(float) * 3 * (size_t)L.e8 * L.d * (noisy ? 2 : 1) : 0);
     L.total = o;
     return L;
 }
@@ -596,6 +605,61 @@ const void* offset_elems(const void* p, size_t n, size_t esz)
     return p == nullptr ? nullptr : static_cast<const char*>(p) + n * esz;
 }
 
+// Router weight and input gradients on the tensor core (bf16 layers): split the
+// fp32 logit gradients into exact bf16 terms, then one row-mode GEMM for the input
+// gradient and one token-reduction GEMM (fp32 partials, summed) per weight.
+cudaError_t router_bwd_tc(Ctx& c, const float* dl, const float* dn, float* dxr, const moe_grads_t* gr)
+{
+    const Layout& L = c.L;
+    const bool noisy = dn != nullptr;
+    void* dcat = c.at<void>(L.off_bw_dcat);
+    void* wcat = c.at<void>(L.off_bw_wcat);
+    float* P = c.at<float>(L.off_bw_p);
+    const int W = L.r_nblk * L.e8;
+    cudaError_t e = launch_split_grad(dl, dn, L.T, L.E, L.e8, L.r_nblk, dcat, c.sms, c.st, take_pdl(c));
+    if (e == cudaSuccess)
+        e = launch_split_wcat(c.in->W_gate, noisy ? c.in->W_noise : nullptr, L.E, L.e8, L.d, L.r_nblk, wcat, c.sms,
+                              c.st, take_pdl(c));
+    CUtensorMap kD, mD, mW, mX;
+    if (!encode_bf16_2d(&kD, dcat, L.T, W, 128) || !encode_bf16_2d(&mD, dcat, L.T, W, 64) ||
+        !encode_bf16_2d(&mW, wcat, W, L.d, 64) || !encode_bf16_2d(&mX, c.in->x, L.T, L.d, 64))
+        return cudaErrorInvalidValue;
+    auto grid_for = [&](long long tiles) { return (int)std::max(1ll, std::min(tiles, (long long)c.sms)); };
+    {
+        BwdTcArgs a{};  // dx_router = D Wcat
+        a.G = 1;
+        a.fixed_rows = L.T;
+        a.N = L.d;
+        a.K = W;
+        a.C = dxr;
+        a.ldc = L.d;
+        a.err = c.err();
+        const CUtensorMap maps[4] = {kD, mW, kD, mW};
+        if (e == cudaSuccess)
+            e = launch_gemm_bwd_tc(maps, a, kBwdRows, kEpiStoreF32,
+                                   grid_for((long long)ceil_div(L.T, 128) * ceil_div(L.d, 256)), c.st, take_pdl(c));
+    }
+    for (int which = 0; which < (noisy ? 2 : 1); ++which) {
+        BwdTcArgs a{};  // partials [3 E8, d] of dW = dl^T x (dn^T x), one per split term
+        a.G = 1;
+        a.fixed_rows = L.T;
+        a.M = 3 * L.e8;
+        a.N = L.d;
+        a.a_col0 = which * 4 * L.e8;
+        float* Pw = P + (size_t)which * 3 * L.e8 * L.d;
+        a.C = Pw;
+        a.ldc = L.d;
+        a.err = c.err();
+        const CUtensorMap maps[4] = {mD, mX, mD, mX};
+        if (e == cudaSuccess)
+            e = launch_gemm_bwd_tc(maps, a, kBwdReduce, kEpiStoreF32,
+                                   grid_for((long long)ceil_div(a.M, 128) * ceil_div(L.d, 256)), c.st, take_pdl(c));
+        if (e == cudaSuccess)
+            e = launch_sum3(Pw, L.E, L.e8, L.d, which ? gr->dW_noise : gr->dW_gate, c.sms, c.st, take_pdl(c));
+    }
+    return e;
+}
+
 // Routed and shared experts' backward on the tensor core (bf16 layers).
 cudaError_t experts_bwd_tc(Ctx& c, const void* dy, const moe_grads_t* gr)
 {
@@ -911,28 +975,51 @@ moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t
         rb.dn = dn;
     }
     if (e == cudaSuccess) e = launch_router_bwd(rb, c.sms, c.st, take_pdl(c));
-    {
-        BwdGemmArgs a{};  // dW_gate[e, i] = sum_t dl[t, e] x[t, i]
-        a.mode = kBwdFixed;
-        a.epi = kEpiStore;
-        a.A = dl;
-        a.a_sm = 1;
-        a.a_sk = L.E;
-        a.B = c.in->x;
-        a.b_sk = L.d;
-        a.b_sn = 1;
-        a.C = gr->dW_gate;
-        a.c_sm = L.d;
-        a.M = L.E;
-        a.N = L.d;
-        a.K = L.T;
-        const int ty = c.bf16 ? kBwdTypesF32xBf16 : kBwdTypesF32;
-        gemm(a, ty, tiles(a.M, a.N));
-        if (noisy) {
-            a.A = dn;
-            a.C = gr->dW_noise;
+    if (L.tc_router) {
+        if (e == cudaSuccess) e = router_bwd_tc(c, dl, dn, dxr, gr);
+    } else {
+        {
+            BwdGemmArgs a{};  // dW_gate[e, i] = sum_t dl[t, e] x[t, i]
+            a.mode = kBwdFixed;
+            a.epi = kEpiStore;
+            a.A = dl;
+            a.a_sm = 1;
+            a.a_sk = L.E;
+            a.B = c.in->x;
+            a.b_sk = L.d;
+            a.b_sn = 1;
+            a.C = gr->dW_gate;
+            a.c_sm = L.d;
+            a.M = L.E;
+            a.N = L.d;
+            a.K = L.T;
+            const int ty = c.bf16 ? kBwdTypesF32xBf16 : kBwdTypesF32;
             gemm(a, ty, tiles(a.M, a.N));
+            if (noisy) {
+                a.A = dn;
+                a.C = gr->dW_noise;
+                gemm(a, ty, tiles(a.M, a.N));
+            }
+            BwdGemmArgs r{};  // dx_router[t, i] = sum_e dl[t, e] W_gate[e, i] (+ dn W_noise)
+            r.mode = kBwdFixed;
+            r.epi = kEpiStore;
+            r.A = dl;
+            r.A2 = dn;
+            r.a_sm = L.E;
+            r.a_sk = 1;
+            r.B = c.in->W_gate;
+            r.B2 = noisy ? c.in->W_noise : nullptr;
+            r.b_sk = L.d;
+            r.b_sn = 1;
+            r.C = dxr;
+            r.c_sm = L.d;
+            r.M = L.T;
+            r.N = L.d;
+            r.K = L.E;
+            gemm(r, kBwdTypesF32, tiles(r.M, r.N));
         }
+    }
+    {
         ColsumArgs s{};
         s.lda = L.E;
         s.fixed_rows = L.T;
@@ -948,23 +1035,6 @@ moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t
             s.out = gr->db_noise;
             colsum(s, kBwdTypesF32);
         }
-        BwdGemmArgs r{};  // dx_router[t, i] = sum_e dl[t, e] W_gate[e, i] (+ dn W_noise)
-        r.mode = kBwdFixed;
-        r.epi = kEpiStore;
-        r.A = dl;
-        r.A2 = dn;
-        r.a_sm = L.E;
-        r.a_sk = 1;
-        r.B = c.in->W_gate;
-        r.B2 = noisy ? c.in->W_noise : nullptr;
-        r.b_sk = L.d;
-        r.b_sn = 1;
-        r.C = dxr;
-        r.c_sm = L.d;
-        r.M = L.T;
-        r.N = L.d;
-        r.K = L.E;
-        gemm(r, kBwdTypesF32, tiles(r.M, r.N));
     }
 
     void* dxs = L.S > 0 ? c.at<void>(L.off_bw_dxs) : nullptr;

@@ -29,30 +29,36 @@ __device__ __forceinline__ void st_round(T* p, size_t i, float v)
     else p[i] = v;
 }
 
-// One warp per token.
+// One warp per token; 16-byte vectors of the row per lane.
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_combine(BwdCombineArgs a)
 {
+    constexpr int V = Vec<T>::N;
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const T* dy = static_cast<const T*>(a.dy);
-    const T* yp = static_cast<const T*>(a.yp);
-    T* dyp = static_cast<T*>(a.dyp);
+    const int nvec = a.d / V;
+    const size_t row_bytes = (size_t)a.d * sizeof(T);
     for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
-        const T* dyr = dy + (size_t)t * a.d;
+        const char* dyr = static_cast<const char*>(a.dy) + (size_t)t * row_bytes;
         for (int j = 0; j < a.k; ++j) {
             const size_t s = (size_t)t * a.k + j;
             const int r = a.slot_row[s];
             float dot = 0.0f;
             if (r >= 0) {
                 const float g = a.gates[s];
-                const T* yr = yp + (size_t)r * a.d;
-                T* dr = dyp + (size_t)r * a.d;
-                for (int i = lane; i < a.d; i += 32) {
-                    const float v = ld_f32(dyr, i);
-                    dot = fmaf(v, ld_f32(yr, i), dot);
-                    st_round(dr, i, g * v);
+                const char* yr = static_cast<const char*>(a.yp) + (size_t)r * row_bytes;
+                char* dr = static_cast<char*>(a.dyp) + (size_t)r * row_bytes;
+                for (int v = lane; v < nvec; v += 32) {
+                    float u[V], y[V];
+                    Vec<T>::load(dyr + v * 16, u);
+                    Vec<T>::load(yr + v * 16, y);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
+                        dot = fmaf(u[i], y[i], dot);
+                        u[i] *= g;
+                    }
+                    Vec<T>::store(dr + v * 16, u);
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
@@ -142,51 +148,87 @@ __global__ void __launch_bounds__(256) k_router_bwd(RouterBwdArgs a)
     }
 }
 
-// out[g][n] = sum over the rows of segment g of A[row][n]; one thread per (g, n).
+// out[g][n] = sum over the rows of segment g of A[row][n].  A block covers (g, 32
+// columns): lane = column, the 8 warps take every 8th row, then the 8 partial sums
+// are added in warp order (deterministic).
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(256) k_colsum(ColsumArgs a)
 {
-    griddep_launch_dependents();
-    griddep_wait();
-    const TI* A = static_cast<const TI*>(a.A);
-    TO* out = static_cast<TO*>(a.out);
-    const long long total = (long long)a.G * a.N;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int g = (int)(i / a.N), n = (int)(i - (long long)g * a.N);
-        const long long r0 = a.row_off != nullptr ? a.row_off[g] : 0;
-        const int rows = a.rows != nullptr ? a.rows[g] : a.fixed_rows;
-        float s = 0.0f;
-        for (int r = 0; r < rows; ++r) s += to_f32(A[(r0 + r) * a.lda + n]);
-        st_round(out, (size_t)(a.out_g0 + g) * a.N + n, s);
-    }
-}
-
-// One warp per token, d elements per row, fp32 accumulation in a fixed order.
-template <typename T>
-__global__ void __launch_bounds__(256) k_bwd_unpermute(BwdUnpermuteArgs a)
-{
+    __shared__ float part[8][33];
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const T* dy = static_cast<const T*>(a.dy);
-    const T* dxp = static_cast<const T*>(a.dxp);
-    const T* dxs = static_cast<const T*>(a.dxs);
-    T* dx = static_cast<T*>(a.dx);
-    for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
-        int n_drop = 0;
-        for (int j = 0; j < a.k; ++j) n_drop += a.slot_row[(size_t)t * a.k + j] < 0 ? 1 : 0;
-        const bool pass = a.residual_mode == 1 || n_drop == a.k;
-        for (int i = lane; i < a.d; i += 32) {
-            float v = pass ? ld_f32(dy, (size_t)t * a.d + i) : 0.0f;
-            for (int j = 0; j < a.k; ++j) {
-                const int r = a.slot_row[(size_t)t * a.k + j];
-                if (r >= 0) v += ld_f32(dxp, (size_t)r * a.d + i);
-            }
-            if (dxs != nullptr) v += ld_f32(dxs, (size_t)t * a.d + i);
-            v += a.dxr[(size_t)t * a.d + i];
-            st_round(dx, (size_t)t * a.d + i, v);
+    const TI* A = static_cast<const TI*>(a.A);
+    TO* out = static_cast<TO*>(a.out);
+    const int chunks = ceil_div(a.N, 32);
+    for (int item = blockIdx.x; item < a.G * chunks; item += gridDim.x) {
+        const int g = item / chunks, n = (item - g * chunks) * 32 + lane;
+        const long long r0 = a.row_off != nullptr ? a.row_off[g] : 0;
+        const int rows = a.rows != nullptr ? a.rows[g] : a.fixed_rows;
+        float s = 0.0f;
+        if (n < a.N)
+            for (int r = warp; r < rows; r += 8) s += to_f32(A[(r0 + r) * a.lda + n]);
+        part[warp][lane] = s;
+        __syncthreads();
+        if (warp == 0 && n < a.N) {
+            float t = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) t += part[w][lane];
+            st_round(out, (size_t)(a.out_g0 + g) * a.N + n, t);
         }
+        __syncthreads();
+    }
+}
+
+// One warp per token, 16-byte vectors per lane, fp32 accumulation in a fixed order.
+template <typename T>
+__global__ void __launch_bounds__(256) k_bwd_unpermute(BwdUnpermuteArgs a)
+{
+    constexpr int V = Vec<T>::N;
+    __shared__ int s_row[8][kMaxTopK];
+    griddep_launch_dependents();
+    griddep_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = a.d / V;
+    const size_t row_bytes = (size_t)a.d * sizeof(T);
+    for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
+        const int r = lane < a.k ? a.slot_row[(size_t)t * a.k + lane] : -1;
+        if (lane < a.k) s_row[warp][lane] = r;
+        const unsigned dropped = __ballot_sync(0xffffffffu, lane < a.k && r < 0);
+        const unsigned all_k = a.k >= 32 ? 0xffffffffu : ((1u << a.k) - 1u);
+        const bool pass = a.residual_mode == 1 || dropped == all_k;
+        __syncwarp();  // s_row visible to the whole warp
+        const char* dyr = static_cast<const char*>(a.dy) + (size_t)t * row_bytes;
+        const char* dxsr = a.dxs ? static_cast<const char*>(a.dxs) + (size_t)t * row_bytes : nullptr;
+        const float* dxrr = a.dxr + (size_t)t * a.d;
+        char* dxo = static_cast<char*>(a.dx) + (size_t)t * row_bytes;
+        for (int v = lane; v < nvec; v += 32) {
+            float acc[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = dxrr[v * V + i];
+            if (pass) {
+                float u[V];
+                Vec<T>::load(dyr + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += u[i];
+            }
+            for (int j = 0; j < a.k; ++j) {
+                const int rj = s_row[warp][j];
+                if (rj < 0) continue;
+                float u[V];
+                Vec<T>::load(static_cast<const char*>(a.dxp) + (size_t)rj * row_bytes + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += u[i];
+            }
+            if (dxsr) {
+                float u[V];
+                Vec<T>::load(dxsr + v * 16, u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += u[i];
+            }
+            Vec<T>::store(dxo + v * 16, acc);
+        }
+        __syncwarp();  // s_row is rewritten for the warp's next token
     }
 }
 
@@ -209,6 +251,73 @@ __global__ void __launch_bounds__(256) k_zero_pad_rows(ZeroPadArgs a)
             for (int v = lane; v < a.row_bytes[b] / 16; v += 32) r[v] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
+}
+
+// Exact three-term bf16 split of an fp32 value (Henry, Tang and Heinecke 2019):
+// v = hi + mid + lo with hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid).
+__device__ __forceinline__ void split3(float v, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo)
+{
+    hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    mid = __float2bfloat16_rn(r1);
+    lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
+
+__global__ void __launch_bounds__(256) k_split_grad(const float* __restrict__ dl, const float* __restrict__ dn,
+                                                    int T, int E, int E8, int nblk, __nv_bfloat16* __restrict__ out)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int W = nblk * E8;
+    const long long total = (long long)T * W;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / W), c = (int)(i - (long long)t * W);
+        const int blk = c / E8, e = c - blk * E8;
+        const float* src = blk < 4 ? dl : dn;
+        const float v = e < E ? src[(size_t)t * E + e] : 0.0f;
+        __nv_bfloat16 hi, mid, lo;
+        split3(v, hi, mid, lo);
+        const int term = blk & 3;  // hi, mid, lo, hi
+        out[i] = term == 1 ? mid : (term == 2 ? lo : hi);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_split_wcat(const float* __restrict__ Wg, const float* __restrict__ Wn,
+                                                    int E, int E8, int d, int nblk, __nv_bfloat16* __restrict__ out)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const long long total = (long long)nblk * E8 * d;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / d), col = (int)(i - (long long)r * d);
+        const int blk = r / E8, e = r - blk * E8;
+        const float* src = blk < 4 ? Wg : Wn;
+        const float v = e < E ? src[(size_t)e * d + col] : 0.0f;
+        __nv_bfloat16 hi, mid, lo;
+        split3(v, hi, mid, lo);
+        out[i] = (blk & 3) == 3 ? mid : hi;  // hi, hi, hi, mid
+    }
+}
+
+__global__ void __launch_bounds__(256) k_sum3(const float* __restrict__ P, int E, int E8, int d,
+                                              float* __restrict__ out)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const long long total = (long long)E * d;
+    const long long blk = (long long)E8 * d;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = (P[2 * blk + i] + P[blk + i]) + P[i];  // smallest terms first
+}
+
+int elem_grid(long long n, int sms)
+{
+    long long g = (n + 255) / 256;
+    if (g > (long long)sms * 16) g = (long long)sms * 16;
+    return (int)(g < 1 ? 1 : g);
 }
 
 int warp_grid(int T, int sms)
@@ -238,8 +347,7 @@ cudaError_t launch_router_bwd(const RouterBwdArgs& a, int sms, cudaStream_t st, 
 
 cudaError_t launch_colsum(const ColsumArgs& a, int types, int sms, cudaStream_t st, bool pdl)
 {
-    const long long total = (long long)a.G * a.N;
-    long long grid = (total + 255) / 256;
+    long long grid = (long long)a.G * ceil_div(a.N, 32);
     if (grid > (long long)sms * 8) grid = (long long)sms * 8;
     if (grid < 1) grid = 1;
     const dim3 g((int)grid), b(256);
@@ -247,6 +355,25 @@ cudaError_t launch_colsum(const ColsumArgs& a, int types, int sms, cudaStream_t 
     case kBwdTypesBf16: return launch_kernel(k_colsum<__nv_bfloat16, __nv_bfloat16>, g, b, 0, st, pdl, a);
     default: return launch_kernel(k_colsum<float, float>, g, b, 0, st, pdl, a);
     }
+}
+
+cudaError_t launch_split_grad(const float* dl, const float* dn, int T, int E, int E8, int nblk, void* out,
+                              int sms, cudaStream_t st, bool pdl)
+{
+    return launch_kernel(k_split_grad, dim3(elem_grid((long long)T * nblk * E8, sms)), dim3(256), 0, st, pdl, dl, dn,
+                         T, E, E8, nblk, static_cast<__nv_bfloat16*>(out));
+}
+
+cudaError_t launch_split_wcat(const float* Wg, const float* Wn, int E, int E8, int d, int nblk, void* out,
+                              int sms, cudaStream_t st, bool pdl)
+{
+    return launch_kernel(k_split_wcat, dim3(elem_grid((long long)nblk * E8 * d, sms)), dim3(256), 0, st, pdl, Wg,
+                         Wn, E, E8, d, nblk, static_cast<__nv_bfloat16*>(out));
+}
+
+cudaError_t launch_sum3(const float* P, int E, int E8, int d, float* out, int sms, cudaStream_t st, bool pdl)
+{
+    return launch_kernel(k_sum3, dim3(elem_grid((long long)E * d, sms)), dim3(256), 0, st, pdl, P, E, E8, d, out);
 }
 
 cudaError_t launch_zero_pad_rows(const ZeroPadArgs& a, int sms, cudaStream_t st, bool pdl)

@@ -17,48 +17,6 @@ namespace moe {
 
 namespace {
 
-template <typename T>
-struct Vec;
-template <>
-struct Vec<__nv_bfloat16> {
-    static constexpr int N = 8;
-    __device__ static void load(const void* p, float (&v)[8])
-    {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-    __device__ static void store(void* p, const float (&v)[8])
-    {
-        uint4 u;
-        u.x = pack_bf16x2(v[0], v[1]);
-        u.y = pack_bf16x2(v[2], v[3]);
-        u.z = pack_bf16x2(v[4], v[5]);
-        u.w = pack_bf16x2(v[6], v[7]);
-        *reinterpret_cast<uint4*>(p) = u;
-    }
-};
-template <>
-struct Vec<float> {
-    static constexpr int N = 4;
-    __device__ static void load(const void* p, float (&v)[4])
-    {
-        const float4 u = *reinterpret_cast<const float4*>(p);
-        v[0] = u.x;
-        v[1] = u.y;
-        v[2] = u.z;
-        v[3] = u.w;
-    }
-    __device__ static void store(void* p, const float (&v)[4])
-    {
-        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-};
-
 template <typename T, bool SEG>
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
 {

@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kr = s_roff[g] + kb * kBK;  // token rows of this K block
 #pragma unroll
                         for (int j = 0; j < kBM / 64; ++j)
-                            tma_load_2d(dA + j * kMnBox, &tmA, &full[stage], m * kBM + j * 64, kr, pol_act);
+                            tma_load_2d(dA + j * kMnBox, &tmA, &full[stage], args.a_col0 + m * kBM + j * 64, kr,
+                                        pol_act);
 #pragma unroll
                         for (int j = 0; j < kBN / 64; ++j)
                             tma_load_2d(dB + j * kMnBox, &tmB, &full[stage], bx + j * 64, kr, pol_act);
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 off = (long long)(s_roff[g] + row) * args.ldc;
                 const bool valid = row < s_rows[g];
                 // pad rows of a routed segment get zeros from the act backward
-                store = valid || (EPI != kEpiStore && !fixed);
+                store = valid || (EPI != kEpiStore && EPI != kEpiStoreF32 && !fixed);
                 zero = !valid;
             } else {
                 off = (long long)(args.c_g0 + g) * args.c_gs + (long long)row * args.ldc;
@@ -304,6 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!store || col0 >= args.N) continue;
                 if constexpr (EPI == kEpiStore) {
                     store_row32(C + off, col0, args.N, v);
+                } else if constexpr (EPI == kEpiStoreF32) {
+                    float* crow = static_cast<float*>(args.C) + off;
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        if (col0 + q4 * 4 + 4 <= args.N)
+                            *reinterpret_cast<float4*>(crow + col0 + q4 * 4) =
+                                make_float4(v[q4 * 4], v[q4 * 4 + 1], v[q4 * 4 + 2], v[q4 * 4 + 3]);
                 } else if constexpr (EPI == kEpiSwigluBwd) {
                     float z1[32], z3[32], o3[32];
                     if (!zero) {
@@ -364,8 +372,12 @@ cudaError_t launch_t(const CUtensorMap* maps, const BwdTcArgs& a, int grid, cuda
 cudaError_t launch_gemm_bwd_tc(const CUtensorMap* maps, const BwdTcArgs& a, int mode, int epi, int grid,
                                cudaStream_t st, bool pdl)
 {
-    if (mode == kBwdReduce) return launch_t<kBwdReduce, kEpiStore>(maps, a, grid, st, pdl);
+    if (mode == kBwdReduce) {
+        if (epi == kEpiStoreF32) return launch_t<kBwdReduce, kEpiStoreF32>(maps, a, grid, st, pdl);
+        return launch_t<kBwdReduce, kEpiStore>(maps, a, grid, st, pdl);
+    }
     switch (epi) {
+    case kEpiStoreF32: return launch_t<kBwdRows, kEpiStoreF32>(maps, a, grid, st, pdl);
     case kEpiStore: return launch_t<kBwdRows, kEpiStore>(maps, a, grid, st, pdl);
     case kEpiReluBwd: return launch_t<kBwdRows, kEpiReluBwd>(maps, a, grid, st, pdl);
     case kEpiGeluTanhBwd: return launch_t<kBwdRows, kEpiGeluTanhBwd>(maps, a, grid, st, pdl);

@@ -147,7 +147,14 @@ constexpr int kFfmaTileN = 64;
 // (e1 = the pre-activation z); SwiGLU backward (e1 = z1, e2 = z3; writes
 // dz1 = v z3 silu'(z1) to C and dz3 = v silu(z1) to C2); e1, e2, C2 share C's indexing.
 enum BwdMode : int { kBwdFixed = 0, kBwdRows = 1, kBwdReduce = 2 };
-enum BwdEpi : int { kEpiStore = 0, kEpiReluBwd = 1, kEpiGeluTanhBwd = 2, kEpiGeluErfBwd = 3, kEpiSwigluBwd = 4 };
+enum BwdEpi : int {
+    kEpiStore = 0,
+    kEpiReluBwd = 1,
+    kEpiGeluTanhBwd = 2,
+    kEpiGeluErfBwd = 3,
+    kEpiSwigluBwd = 4,
+    kEpiStoreF32 = 5  // tensor-core kernel only: fp32 output
+};
 enum BwdTypes : int { kBwdTypesBf16 = 0, kBwdTypesF32 = 1, kBwdTypesF32xBf16 = 2 };  // (A,B,C) element types
 struct BwdGemmArgs {
     int mode, epi;
@@ -188,6 +195,7 @@ struct BwdTcArgs {
     int G, fixed_rows;
     int M, N, K;
     int b_g0, b_rows_per_group, b_col0;
+    int a_col0;           // kBwdReduce: first A column (M offset)
     int two_seg;
     void* C;
     void* C2;
@@ -210,6 +218,19 @@ struct ZeroPadArgs {
     int row_bytes[3];
 };
 cudaError_t launch_zero_pad_rows(const ZeroPadArgs& a, int sms, cudaStream_t st, bool pdl);
+
+// Router gradients on the tensor core.  The fp32 logit gradients dl (and dn) are
+// split exactly into bf16 terms hi + mid + lo; with E8 = E rounded up to 8:
+//   D [T, nblk * E8] = [dl_hi | dl_mid | dl_lo | dl_hi (| the same for dn)]
+//   B [nblk * E8, d] = [W_hi; W_hi; W_hi; W_mid (; the same for W_noise)]
+// so that D B = dl W_hi + dl_hi W_mid (+ dn ...) ~ dl W_gate (+ dn W_noise), and the
+// first three blocks of D reduce against x to three exact-product partials of dW.
+cudaError_t launch_split_grad(const float* dl, const float* dn, int T, int E, int E8, int nblk, void* out,
+                              int sms, cudaStream_t st, bool pdl);
+cudaError_t launch_split_wcat(const float* Wg, const float* Wn, int E, int E8, int d, int nblk, void* out,
+                              int sms, cudaStream_t st, bool pdl);
+// out[e, i] = (P[2 E8 + e, i] + P[E8 + e, i]) + P[e, i], e < E
+cudaError_t launch_sum3(const float* P, int E, int E8, int d, float* out, int sms, cudaStream_t st, bool pdl);
 
 // ---- backward: memory-bound kernels ---------------------------------------------
 struct BwdCombineArgs {

@@ -172,3 +172,13 @@ def test_tensor_core_and_ffma_backward_agree(name):
     for k, v in g_tc.items():
         if v is not None:
             assert rel_frobenius(v.double().numpy(), g_ff[k].double().numpy()) <= 1e-2, k
+
+
+@pytest.mark.parametrize("name", ["noisy_switch_capacity", "swiglu_renorm", "noisy_router_split_k"])
+def test_backward_ffma_router_matches_oracle(name):
+    # the CUDA-core router gradients (the tensor-core split-term path is the default)
+    cfg = CASES[name]
+    inp = _inputs(cfg)
+    dy = _dy(cfg)
+    out, grads, _ = run_backward(cfg, inp, dy, 0.37, flags=_lib.MOE_FLAG_FFMA_ROUTER)
+    compare(cfg, grads, oracle_grads(cfg, inp, out, dy, 0.37), out)
