@@ -219,7 +219,10 @@ typedef struct {
  * optional logits from `outputs`, and the permuted activations, hidden
  * activations and expert outputs from the workspace).  Gradients are computed
  * in fp32 and rounded once to the destination type; weight gradients are
- * written (not accumulated).  Validation happens before any launch. */
+ * written (not accumulated).  Under MOE_FLAG_TRAINING the forward also keeps
+ * the first layer's pre-activations in the workspace; the backward consumes
+ * them (overwrites them with their gradients), so each moe_backward needs its
+ * own preceding moe_forward.  Validation happens before any launch. */
 moe_status_t moe_backward(const moe_params_t* params, const moe_inputs_t* inputs,
                           const moe_outputs_t* outputs, const void* dy, float d_aux,
                           const moe_grads_t* grads, void* workspace, size_t workspace_bytes,

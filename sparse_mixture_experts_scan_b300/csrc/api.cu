@@ -477,6 +477,17 @@ moe_status_t stage_gemm(Ctx& c)
     const int mt_shared = L.t_pad / kSegRows;
     auto grid_for = [&](int tiles, int per_sm) { return std::max(1, std::min(tiles, c.sms * per_sm)); };
     cudaError_t e = cudaSuccess;
+    // training: the first layer also keeps its pre-activations for the backward pass
+    // (relu's derivative comes from H itself)
+    const bool save = (c.p.flags & MOE_FLAG_TRAINING) && c.p.act != MOE_ACT_RELU;
+    if (save && c.use_tc) {
+        g1.z1 = c.at<void>(L.off_bw_z1);
+        g1.z3 = gated ? c.at<void>(L.off_bw_z3) : nullptr;
+        if (L.S > 0) {
+            s1.z1 = c.at<void>(L.off_bw_zs1);
+            s1.z3 = c.at<void>(L.off_bw_zs3);
+        }
+    }
     if (c.use_tc) {
         const int out1 = gated ? c.bn1 / 2 : c.bn1;
         g1.n_tiles = ceil_div(L.F, out1);
@@ -501,6 +512,8 @@ moe_status_t stage_gemm(Ctx& c)
             f.ldy = L.d;
             f.bias1 = c.in->b1;
             f.bias2 = c.in->b2;
+            f.z1 = g1.z1;
+            f.z3 = g1.z3;
             unsigned* sync = c.at<unsigned>(L.off_ffn_sync);
             f.tile_ctr = sync;
             f.ctas_done = sync + 1;
@@ -726,31 +739,6 @@ cudaError_t experts_bwd_tc(Ctx& c, const void* dy, const moe_grads_t* gr)
         zp.row_bytes[2] = (int)(L.d * esz);
         e = launch_zero_pad_rows(zp, c.sms, c.st, take_pdl(c));
     }
-    if (c.p.act != MOE_ACT_RELU && mt_routed > 0) {
-        // recompute the pre-activations with the forward's grouped GEMM (no activation)
-        GroupedGemmArgs g{};
-        g.mtile_off = mtile;
-        g.row_off = row_off;
-        g.rows = kept;
-        g.G = L.E;
-        g.N = L.F;
-        g.K = L.d;
-        g.k_segments = 1;
-        g.b_rows_per_group = L.F;
-        g.out = z1;
-        g.ldo = L.F;
-        g.bias = c.in->b1;
-        g.a_rows_alloc = L.rows_cap;
-        g.err = c.err();
-        const int bn = swiglu ? c.bn1 / 2 : c.bn1;  // the B maps' box height
-        g.n_tiles = ceil_div(L.F, bn);
-        const int grid = std::max(1, std::min(mt_routed * g.n_tiles, c.sms));
-        if (e == cudaSuccess) e = launch_gemm_tc(c.mA1, c.mB1, c.mB1, g, kActNone, bn, grid, c.st, take_pdl(c));
-        if (swiglu) {
-            g.out = z3;
-            if (e == cudaSuccess) e = launch_gemm_tc(c.mA1, c.mB3, c.mB3, g, kActNone, bn, grid, c.st, take_pdl(c));
-        }
-    }
     {
         BwdTcArgs a = red;  // dW2_e = dYp_e^T H_e
         a.M = L.d;
@@ -846,24 +834,6 @@ cudaError_t experts_bwd_tc(Ctx& c, const void* dy, const moe_grads_t* gr)
              encode_bf16_2d(&mZs1, zs1, T, SF, 64) && encode_bf16_2d(&mZs3, zs3, T, SF, 64) &&
              encode_bf16_2d(&mHs, c.at<void>(L.off_hs), T, SF, 64) && encode_bf16_2d(&mX, c.in->x, T, L.d, 64);
         if (!ok) return cudaErrorInvalidValue;
-        GroupedGemmArgs g{};  // z = x W^T over the S*F concatenated rows
-        g.G = 1;
-        g.fixed_rows = L.T;
-        g.N = (int)SF;
-        g.K = L.d;
-        g.k_segments = 1;
-        g.b_rows_per_group = L.F;
-        g.b_group0 = L.E;
-        g.out = zs1;
-        g.ldo = (int)SF;
-        g.a_rows_alloc = L.T;
-        g.err = c.err();
-        const int bn = c.bn1 / 2;  // SwiGLU: the W1 / W3 maps' box height
-        g.n_tiles = ceil_div((int)SF, bn);
-        const int grid = std::max(1, std::min(ceil_div(L.T, 128) * g.n_tiles, c.sms));
-        if (e == cudaSuccess) e = launch_gemm_tc(c.mAs1, c.mB1, c.mB1, g, kActNone, bn, grid, c.st, take_pdl(c));
-        g.out = zs3;
-        if (e == cudaSuccess) e = launch_gemm_tc(c.mAs1, c.mB3, c.mB3, g, kActNone, bn, grid, c.st, take_pdl(c));
         BwdTcArgs f{};
         f.G = 1;
         f.fixed_rows = L.T;

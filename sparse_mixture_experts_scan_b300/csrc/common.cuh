@@ -478,6 +478,8 @@ struct GroupedGemmArgs {
     const void* bias;
     int a_rows_alloc;      // rows of A that exist (FFMA bounds)
     uint32_t* err;
+    void* z1;              // tcgen05 kernel, training: pre-activations of the output, [rows, ldo], or nullptr
+    void* z3;              // ... and the W3 half (SwiGLU)
 };
 
 }  // namespace moe

@@ -78,7 +78,7 @@ __device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target,
     }
 }
 
-template <int BN, int ACT1>
+template <int BN, int ACT1, bool SAVE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ffn_fused_tc(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
@@ -325,8 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             (size_t)g * args.b2_rows_per_group, 1, args.b2_rows_per_group);
             } else {
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.h) + (size_t)(s_roff[g] + row) * args.ldh;
-                epilogue_tile<BN, ACT1>(t_lane, orow, row_ok, n * OUT1, args.N1, bias1,
-                                        (size_t)g * args.b1_rows_per_group, 1, args.b1_rows_per_group);
+                const size_t zo = (size_t)(s_roff[g] + row) * args.ldh;
+                epilogue_tile<BN, ACT1, SAVE>(t_lane, orow, row_ok, n * OUT1, args.N1, bias1,
+                                              (size_t)g * args.b1_rows_per_group, 1, args.b1_rows_per_group,
+                                              SAVE ? static_cast<__nv_bfloat16*>(args.z1) + zo : nullptr,
+                                              SAVE && GATED ? static_cast<__nv_bfloat16*>(args.z3) + zo : nullptr);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -366,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int ACT1>
+template <int BN, int ACT1, bool SAVE>
 cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st, bool pdl)
 {
-    auto kern = k_ffn_fused_tc<BN, ACT1>;
+    auto kern = k_ffn_fused_tc<BN, ACT1, SAVE>;
     const size_t smem = FCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -382,11 +385,19 @@ cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, c
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
                                 cudaStream_t st, bool pdl)
 {
+    // with a.z1 set (training, GELU or SwiGLU) the GEMM1 epilogue also keeps the pre-activations
+    const bool save = a.z1 != nullptr;
     switch (act1) {
-    case kActRelu: return launch_t<256, kActRelu>(maps, a, grid, st, pdl);
-    case kActGeluTanh: return launch_t<256, kActGeluTanh>(maps, a, grid, st, pdl);
-    case kActGeluErf: return launch_t<256, kActGeluErf>(maps, a, grid, st, pdl);
-    default: return launch_t<256, kActSwiglu>(maps, a, grid, st, pdl);
+    case kActRelu: return launch_t<256, kActRelu, false>(maps, a, grid, st, pdl);
+    case kActGeluTanh:
+        return save ? launch_t<256, kActGeluTanh, true>(maps, a, grid, st, pdl)
+                    : launch_t<256, kActGeluTanh, false>(maps, a, grid, st, pdl);
+    case kActGeluErf:
+        return save ? launch_t<256, kActGeluErf, true>(maps, a, grid, st, pdl)
+                    : launch_t<256, kActGeluErf, false>(maps, a, grid, st, pdl);
+    default:
+        return save ? launch_t<256, kActSwiglu, true>(maps, a, grid, st, pdl)
+                    : launch_t<256, kActSwiglu, false>(maps, a, grid, st, pdl);
     }
 }
 

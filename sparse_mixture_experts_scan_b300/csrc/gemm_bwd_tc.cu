@@ -19,7 +19,8 @@
 // dH (relu mask from the saved output, GELU from the recomputed pre-activation,
 // SwiGLU pair dz1 = dh z3 silu'(z1), dz3 = dh silu(z1), in place).  In rows mode
 // the act-backward epilogue writes zeros on the pad rows of a segment, so the
-// wgrad that follows reduces over whole 64-row K blocks of finite zeros.
+// wgrad that follows reduces over whole 64-row K blocks of finite zeros.  The
+// pre-activations come from the forward, which keeps them under training.
 // Every wait is bounded; on expiry the CTA flags the error, drains and returns.
 #include "common.cuh"
 #include "kernels.h"
@@ -39,7 +40,8 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr size_t kBarBytes = 256;
 constexpr size_t kTableBytes = sizeof(int) * (3 * kMaxExperts + 1);
-constexpr size_t kSmem = 1024 + kStages * (size_t)kStageBytes + kBarBytes + kTableBytes;
+constexpr size_t kStageEpBytes = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16 columns
+constexpr size_t kSmem = 1024 + kStages * (size_t)kStageBytes + kBarBytes + kTableBytes + 4 * kStageEpBytes + 16;
 
 // Load 32 consecutive bf16 of a row as floats (only the 8-column groups below N).
 __device__ __forceinline__ void load_row32(const __nv_bfloat16* row, int col0, int N, float (&v)[32])
@@ -81,6 +83,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_mt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + kBarBytes);
     int* s_roff = s_mt + kMaxExperts + 1;
     int* s_rows = s_roff + kMaxExperts;
+    // bf16 store epilogue: per-warp staging of 32 rows x 64 columns (16-byte units
+    // XOR-swizzled by row), so that the global stores write whole 128-byte lines
+    uint8_t* s_ep = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(s_rows + kMaxExperts) + 15) & ~static_cast<uintptr_t>(15));
 
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -288,6 +294,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 zero = !have_k;
             }
             const uint32_t t_lane = tmem_base + acc * kBN + (static_cast<uint32_t>(q * 32) << 16);
+            if constexpr (EPI == kEpiStore) {
+                uint8_t* stg = s_ep + q * kStageEpBytes;
+                // the output row of staged row rr (0..31 of this warp) and whether it is written
+                const int row_base = m * kBM + q * 32;
+#pragma unroll 1
+                for (int c2 = 0; c2 < kBN / 64; ++c2) {
+                    uint4 u[8];
+                    if (have_k) {
+                        uint32_t ra[32], rb[32];
+                        tmem_ld_32cols(t_lane + c2 * 64, ra);
+                        tmem_ld_32cols(t_lane + c2 * 64 + 32, rb);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const float* fa = reinterpret_cast<const float*>(ra) + w * 8;
+                            const float* fb = reinterpret_cast<const float*>(rb) + w * 8;
+                            u[w] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                                        : make_uint4(pack_bf16x2(fa[0], fa[1]), pack_bf16x2(fa[2], fa[3]),
+                                                     pack_bf16x2(fa[4], fa[5]), pack_bf16x2(fa[6], fa[7]));
+                            u[4 + w] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                                            : make_uint4(pack_bf16x2(fb[0], fb[1]), pack_bf16x2(fb[2], fb[3]),
+                                                         pack_bf16x2(fb[4], fb[5]), pack_bf16x2(fb[6], fb[7]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) u[w] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();  // the previous pass's reads of the staging rows are done
+                    uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) srow[w ^ (lane & 7)] = u[w];
+                    __syncwarp();
+                    const int unit = lane & 7;
+                    const int col = n * kBN + c2 * 64 + unit * 8;
+#pragma unroll
+                    for (int it2 = 0; it2 < 8; ++it2) {
+                        const int rr = it2 * 4 + (lane >> 3);
+                        const int orow = row_base + rr;
+                        long long o2;
+                        bool ok_row;
+                        if constexpr (MODE == kBwdRows) {
+                            ok_row = orow < s_rows[g];
+                            o2 = (long long)(s_roff[g] + orow) * args.ldc;
+                        } else {
+                            ok_row = orow < args.M;
+                            o2 = (long long)(args.c_g0 + g) * args.c_gs + (long long)orow * args.ldc;
+                        }
+                        const uint4 val = reinterpret_cast<const uint4*>(stg + rr * 128)[unit ^ (rr & 7)];
+                        if (ok_row && col + 8 <= args.N) *reinterpret_cast<uint4*>(C + o2 + col) = val;
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {
                 const int col0 = n * kBN + c * 32;
@@ -303,9 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) v[i] = 0.0f;
                 }
                 if (!store || col0 >= args.N) continue;
-                if constexpr (EPI == kEpiStore) {
-                    store_row32(C + off, col0, args.N, v);
-                } else if constexpr (EPI == kEpiStoreF32) {
+                if constexpr (EPI == kEpiStoreF32) {
                     float* crow = static_cast<float*>(args.C) + off;
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
@@ -341,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     store_row32(C + off, col0, args.N, v);
                 }
+            }
             }
             tc_fence_before_sync();
             __syncwarp();

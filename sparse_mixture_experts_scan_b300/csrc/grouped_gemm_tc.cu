@@ -44,7 +44,7 @@ struct TcCfg {
     static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + BAR_BYTES + TABLE_BYTES;
 };
 
-template <int BN, int ACT>
+template <int BN, int ACT, bool SAVE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmB3, const GroupedGemmArgs args)
@@ -232,9 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = row < s_rows[tm.g];
             __nv_bfloat16* orow = out + (size_t)(s_roff[tm.g] + row) * args.ldo;
             const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            epilogue_tile<BN, ACT>(t_lane, orow, row_ok, n * OUT_COLS, args.N, bias,
-                                   (size_t)(args.b_group0 + tm.g) * args.b_rows_per_group, args.k_segments,
-                                   args.b_rows_per_group);
+            const size_t zo = (size_t)(s_roff[tm.g] + row) * args.ldo;
+            epilogue_tile<BN, ACT, SAVE>(t_lane, orow, row_ok, n * OUT_COLS, args.N, bias,
+                                         (size_t)(args.b_group0 + tm.g) * args.b_rows_per_group, args.k_segments,
+                                         args.b_rows_per_group,
+                                         SAVE ? static_cast<__nv_bfloat16*>(args.z1) + zo : nullptr,
+                                         SAVE && GATED ? static_cast<__nv_bfloat16*>(args.z3) + zo : nullptr);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -251,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int BN, int ACT>
+template <int BN, int ACT, bool SAVE = false>
 cudaError_t launch_tc_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                         const GroupedGemmArgs& args, int grid, cudaStream_t st, bool pdl)
 {
-    auto kern = k_grouped_gemm_tc<BN, ACT>;
+    auto kern = k_grouped_gemm_tc<BN, ACT, SAVE>;
     const size_t smem = TcCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -266,12 +269,20 @@ template <int BN>
 cudaError_t launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                          const GroupedGemmArgs& args, int act, int grid, cudaStream_t st, bool pdl)
 {
+    // with args.z1 set (training) the epilogue also keeps the pre-activations
+    const bool save = args.z1 != nullptr;
     switch (act) {
     case kActNone: return launch_tc_t<BN, kActNone>(a, b, b3, args, grid, st, pdl);
     case kActRelu: return launch_tc_t<BN, kActRelu>(a, b, b3, args, grid, st, pdl);
-    case kActGeluTanh: return launch_tc_t<BN, kActGeluTanh>(a, b, b3, args, grid, st, pdl);
-    case kActGeluErf: return launch_tc_t<BN, kActGeluErf>(a, b, b3, args, grid, st, pdl);
-    default: return launch_tc_t<BN, kActSwiglu>(a, b, b3, args, grid, st, pdl);
+    case kActGeluTanh:
+        return save ? launch_tc_t<BN, kActGeluTanh, true>(a, b, b3, args, grid, st, pdl)
+                    : launch_tc_t<BN, kActGeluTanh>(a, b, b3, args, grid, st, pdl);
+    case kActGeluErf:
+        return save ? launch_tc_t<BN, kActGeluErf, true>(a, b, b3, args, grid, st, pdl)
+                    : launch_tc_t<BN, kActGeluErf>(a, b, b3, args, grid, st, pdl);
+    default:
+        return save ? launch_tc_t<BN, kActSwiglu, true>(a, b, b3, args, grid, st, pdl)
+                    : launch_tc_t<BN, kActSwiglu>(a, b, b3, args, grid, st, pdl);
     }
 }
 

@@ -118,6 +118,8 @@ struct FusedFfnArgs {
     int ldy;
     const void* bias1;
     const void* bias2;
+    void* z1;              // training: GEMM1 pre-activations (W1 half, + bias), [rows, ldh], or nullptr
+    void* z3;              // training, SwiGLU: the W3 half
     unsigned* tile_ctr;    // tiles claimed so far (0 at launch)
     unsigned* ctas_done;   // CTAs finished (0 at launch)
     unsigned* mt_done;     // [mt_max] epilogue-warp arrivals per M-tile (0 at launch)

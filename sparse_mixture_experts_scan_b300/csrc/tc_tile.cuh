@@ -46,10 +46,13 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* orow, int col0, int N
 // [BN/2, BN) for SwiGLU) and stores bf16 outputs n0 .. n0 + OUT_COLS - 1 of the row.
 // The bias of column c is sum over K-segments sg of bias[bias_base + sg * seg_stride + c].
 // Every thread of the warp must call it (tcgen05.ld is warp-collective).
-template <int BN, int ACT>
+// SAVE: also store the pre-activations (training): z1 = the W1 half (+ bias), z3 =
+// the W3 half, rows laid out like orow.
+template <int BN, int ACT, bool SAVE = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_lane, __nv_bfloat16* orow, bool row_ok, int n0, int N,
                                               const __nv_bfloat16* bias, size_t bias_base, int k_segments,
-                                              int seg_stride)
+                                              int seg_stride, __nv_bfloat16* z1row = nullptr,
+                                              __nv_bfloat16* z3row = nullptr)
 {
     constexpr bool GATED = (ACT == kActSwiglu);
     constexpr int OUT_COLS = GATED ? BN / 2 : BN;
@@ -65,6 +68,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_lane, __nv_bfloat16* or
             for (int i = 0; i < 32; ++i)
                 o[i] = activate_bf16out<kActSwiglu>(__uint_as_float(va[i])) * __uint_as_float(vb[i]);
             if (row_ok) store_row32(orow, n0 + c * 32, N, o);
+            if constexpr (SAVE) {
+                if (row_ok) {
+                    store_row32(z1row, n0 + c * 32, N, reinterpret_cast<const float(&)[32]>(va));
+                    store_row32(z3row, n0 + c * 32, N, reinterpret_cast<const float(&)[32]>(vb));
+                }
+            }
         }
     } else if (bias == nullptr) {
 #pragma unroll 1
@@ -76,6 +85,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_lane, __nv_bfloat16* or
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = activate_bf16out<ACT>(__uint_as_float(va[i]));
             if (row_ok) store_row32(orow, n0 + c * 32, N, o);
+            if constexpr (SAVE) {
+                if (row_ok) store_row32(z1row, n0 + c * 32, N, reinterpret_cast<const float(&)[32]>(va));
+            }
         }
     } else {
 #pragma unroll 1
@@ -93,10 +105,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_lane, __nv_bfloat16* or
                 for (int i = 0; i < 32; ++i)
                     if (col0 + i < N) bsum[i] += __bfloat162float(bp[col0 + i]);
             }
-            float o[32];
+            float o[32], z[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = activate_bf16out<ACT>(__uint_as_float(va[i]) + bsum[i]);
+            for (int i = 0; i < 32; ++i) {
+                z[i] = __uint_as_float(va[i]) + bsum[i];
+                o[i] = activate_bf16out<ACT>(z[i]);
+            }
             if (row_ok) store_row32(orow, col0, N, o);
+            if constexpr (SAVE) {
+                if (row_ok) store_row32(z1row, col0, N, z);
+            }
         }
     }
 }
