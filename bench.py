@@ -613,10 +613,11 @@ def backward_work(cfg, out):
     """Minimum work of the backward's expert stage for this batch.
 
     Flops: dgrad and wgrad of every expert matrix on the kept rows (2 x the
-    forward's), plus the recomputed pre-activations (GELU: W1; SwiGLU: W1, W3).
-    Bytes: the weights of touched experts read once, every weight gradient
-    written once (untouched experts get zeros), and the row activations read or
-    written once: Xp, H, dYp, dXp (d, F, d, d per kept row)."""
+    forward's); the pre-activations the activation backward needs are kept by the
+    forward, not recomputed.  Bytes: the weights of touched experts read once,
+    every weight gradient written once (untouched experts get zeros), and the row
+    activations read or written once: Xp, H, dYp, dXp (d, F, d, d per kept row)
+    plus the saved pre-activations (GELU: F, SwiGLU: 2F per kept row)."""
     import torch
     kept = (out["dropped"] == 0)
     idx = out["expert_idx"].long()
@@ -627,9 +628,9 @@ def backward_work(cfg, out):
     esz = 2 if cfg.dtype == "bf16" else 4
     nmat = 3 if cfg.act == "swiglu" else 2
     n_pre = {"relu": 0, "swiglu": 2}.get(cfg.act, 1)
-    flops = 2.0 * rows * cfg.d * cfg.F * (2 * nmat + n_pre)
+    flops = 2.0 * rows * cfg.d * cfg.F * 2 * nmat
     w = nmat * cfg.d * cfg.F * esz
-    nbytes = touched * w + (cfg.E + cfg.S) * w + rows * esz * (3 * cfg.d + cfg.F)
+    nbytes = touched * w + (cfg.E + cfg.S) * w + rows * esz * (3 * cfg.d + (1 + n_pre) * cfg.F)
     return {"flops": flops, "bytes": nbytes, "rows": rows, "touched_experts": touched}
 
 
