@@ -43,15 +43,20 @@ constexpr size_t kTableBytes = sizeof(int) * (3 * kMaxExperts + 1);
 constexpr size_t kStageEpBytes = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16 columns
 constexpr size_t kSmem = 1024 + kStages * (size_t)kStageBytes + kBarBytes + kTableBytes + 4 * kStageEpBytes + 16;
 
-// Load 32 consecutive bf16 of a row as floats (only the 8-column groups below N).
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* row, int col0, int N, float (&v)[32])
+// Raw 32 bf16 of a row (four 16-byte groups; zeros for groups at or past N).
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* row, int col0, int N, uint4 (&u)[4])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        u[q] = (col0 + q * 8 + 8 <= N) ? *reinterpret_cast<const uint4*>(row + col0 + q * 8)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ void unpack32(const uint4 (&u)[4], float (&v)[32])
 {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const int col = col0 + q * 8;
-        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (col + 8 <= N) u = *reinterpret_cast<const uint4*>(row + col);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             v[q * 8 + 2 * i] = __uint_as_float(w[i] << 16);
@@ -273,11 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int g = tm.g;
             const int acc = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
-            if (!mbar_wait(&tfull[acc], acc_par, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
             const bool have_k = num_kb_of(g) > 0;
             const int row = m * kBM + r_in_tile;
             long long off;    // element offset of (row, column 0) in C (and e1, e2, C2)
@@ -293,6 +293,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 store = row < args.M;
                 zero = !have_k;
             }
+            // activation backward: the saved activations of the first 32 columns are
+            // fetched while the accumulator is still being computed
+            constexpr bool ACT_BWD = EPI == kEpiReluBwd || EPI == kEpiGeluTanhBwd || EPI == kEpiGeluErfBwd ||
+                                     EPI == kEpiSwigluBwd;
+            const bool fetch = ACT_BWD && store && !zero;
+            uint4 pa[4], pb[4];
+            if constexpr (ACT_BWD) {
+                if (fetch) {
+                    load_raw32(E1 + off, n * kBN, args.N, pa);
+                    if constexpr (EPI == kEpiSwigluBwd) load_raw32(E2 + off, n * kBN, args.N, pb);
+                }
+            }
+            if (!mbar_wait(&tfull[acc], acc_par, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
             const uint32_t t_lane = tmem_base + acc * kBN + (static_cast<uint32_t>(q * 32) << 16);
             if constexpr (EPI == kEpiStore) {
                 uint8_t* stg = s_ep + q * kStageEpBytes;
@@ -345,59 +362,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok_row && col + 8 <= args.N) *reinterpret_cast<uint4*>(C + o2 + col) = val;
                     }
                 }
-            } else {
+            } else if constexpr (EPI == kEpiStoreF32) {
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                const int col0 = n * kBN + c * 32;
-                float v[32];
-                if (have_k) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(t_lane + c * 32, r);
-                    tmem_ld_wait();
+                for (int c = 0; c < kBN / 32; ++c) {
+                    const int col0 = n * kBN + c * 32;
+                    float v[32];
+                    if (have_k) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(t_lane + c * 32, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = zero ? 0.0f : __uint_as_float(r[i]);
-                } else {
+                        for (int i = 0; i < 32; ++i) v[i] = zero ? 0.0f : __uint_as_float(r[i]);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                }
-                if (!store || col0 >= args.N) continue;
-                if constexpr (EPI == kEpiStoreF32) {
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+                    if (!store || col0 >= args.N) continue;
                     float* crow = static_cast<float*>(args.C) + off;
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
                         if (col0 + q4 * 4 + 4 <= args.N)
                             *reinterpret_cast<float4*>(crow + col0 + q4 * 4) =
                                 make_float4(v[q4 * 4], v[q4 * 4 + 1], v[q4 * 4 + 2], v[q4 * 4 + 3]);
-                } else if constexpr (EPI == kEpiSwigluBwd) {
-                    float z1[32], z3[32], o3[32];
-                    if (!zero) {
-                        load_row32(E1 + off, col0, args.N, z1);
-                        load_row32(E2 + off, col0, args.N, z3);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        if (zero) {
-                            o3[i] = 0.0f;
-                        } else {
-                            o3[i] = v[i] * silu_f32(z1[i]);
-                            v[i] = v[i] * z3[i] * silu_grad_f32(z1[i]);
-                        }
-                    }
-                    store_row32(C + off, col0, args.N, v);
-                    store_row32(C2 + off, col0, args.N, o3);
-                } else {
-                    float z[32];
-                    if (!zero) {
-                        load_row32(E1 + off, col0, args.N, z);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if constexpr (EPI == kEpiReluBwd) v[i] = z[i] > 0.0f ? v[i] : 0.0f;
-                            else v[i] *= act_grad_f32<EPI == kEpiGeluTanhBwd ? kActGeluTanh : kActGeluErf>(z[i]);
-                        }
-                    }
-                    store_row32(C + off, col0, args.N, v);
                 }
-            }
+            } else {
+                // activation backward (rows mode): the accumulator holds dH
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    const int col0 = n * kBN + c * 32;
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_lane + c * 32, r);
+                    uint4 qa[4], qb[4];  // the next chunk's saved activations, in flight meanwhile
+                    if (fetch && c + 1 < kBN / 32) {
+                        load_raw32(E1 + off, col0 + 32, args.N, qa);
+                        if constexpr (EPI == kEpiSwigluBwd) load_raw32(E2 + off, col0 + 32, args.N, qb);
+                    }
+                    tmem_ld_wait();
+                    if (store && col0 < args.N) {
+                        float v[32];
+                        if (zero) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                            store_row32(C + off, col0, args.N, v);
+                            if constexpr (EPI == kEpiSwigluBwd) store_row32(C2 + off, col0, args.N, v);
+                        } else if constexpr (EPI == kEpiSwigluBwd) {
+                            // dz1 = dh z3 silu'(z1), dz3 = dh silu(z1) (fast exp and divide: the
+                            // results are rounded to bf16)
+                            float z1[32], z3[32], o3[32];
+                            unpack32(pa, z1);
+                            unpack32(pb, z3);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float dh = __uint_as_float(r[i]);
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-z1[i]));
+                                o3[i] = dh * z1[i] * sg;
+                                v[i] = dh * z3[i] * sg * (1.0f + z1[i] * (1.0f - sg));
+                            }
+                            store_row32(C + off, col0, args.N, v);
+                            store_row32(C2 + off, col0, args.N, o3);
+                        } else {
+                            constexpr int kGeluKind = EPI == kEpiGeluTanhBwd ? kActGeluTanh : kActGeluErf;
+                            float z[32];
+                            unpack32(pa, z);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float dh = __uint_as_float(r[i]);
+                                if constexpr (EPI == kEpiReluBwd) v[i] = z[i] > 0.0f ? dh : 0.0f;
+                                else v[i] = dh * act_grad_f32<kGeluKind>(z[i]);
+                            }
+                            store_row32(C + off, col0, args.N, v);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        pa[q] = qa[q];
+                        pb[q] = qb[q];
+                    }
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
