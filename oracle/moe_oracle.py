@@ -85,6 +85,8 @@ def _lib():
         L.orc_backward.restype = None
         L.orc_backward.argtypes = ([i32] * 9 + [vp, i32, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, i32,
                                                 vp, vp, vp, i32, dbl, vp, vp, vp, dbl] + [vp] * 10)
+        L.orc_quantize_int8.restype = None
+        L.orc_quantize_int8.argtypes = [i32, i32, vp, i32, vp, vp]
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
         _lib_handle = L
@@ -317,6 +319,21 @@ def backward(x, Wg, bg, W1, W3, W2, b1, b2, *, idx, dropped, dy, d_aux: float, E
                         _ptr(o["dW3"]), _ptr(o["dW2"]), _ptr(o["db1"]), _ptr(o["db2"]),
                         _ptr(o["dW_noise"]), _ptr(o["db_noise"]))
     return out
+
+
+def quantize_int8(w):
+    """Per-row symmetric int8 quantisation of a 2-D array: (q int8, scale fp32)."""
+    wa, wc = _as_array(w)
+    rows, cols = wa.shape
+    q = np.empty((rows, cols), dtype=np.int8)
+    sc = np.empty(rows, dtype=np.float32)
+    _lib().orc_quantize_int8(rows, cols, _ptr(wa), wc, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def dequantize_int8(q, scale):
+    """q * scale per row, exactly, in fp64."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
 
 
 def num_threads() -> int:

@@ -535,3 +535,32 @@ def test_noisy_route_flips_choice_by_hand():
                   noise=(Wn, bn, np.array([[0.0, 0.0, 150.0]]), 0.01))
     assert r.idx.tolist() == [[0, 2]]
     # the second slot is expert 2 (0.5) ahead of expert 1 (0.0)
+
+
+# ---------------------------------------------------------------- int8 expert weights
+
+def test_quantize_int8_closed_form():
+    # amax 127 gives scale 1 exactly, so q = round-half-even(w); the all-zero row gets
+    # scale 0; a row with amax 0.5 gets scale 0.5/127 and its largest element maps to 127
+    w = np.array([[127.0, -63.5, 2.5, -0.49, 0.5, 1.5],
+                  [0.0, 0.0, 0.0, 0.0, 0.0, 0.0],
+                  [0.5, -0.5, 0.25, 0.0, -0.125, 0.0625]], dtype=np.float32)
+    q, s = orc.quantize_int8(w)
+    assert s[0] == 1.0 and s[1] == 0.0 and s[2] == np.float32(np.float32(0.5) / np.float32(127.0))
+    assert q[0].tolist() == [127, -64, 2, 0, 0, 2]
+    assert q[1].tolist() == [0] * 6
+    assert q[2, 0] == 127 and q[2, 1] == -127 and q[2, 3] == 0
+
+
+def test_quantize_int8_error_bound_and_range():
+    rng = np.random.default_rng(21)
+    w = (rng.standard_normal((37, 53)) * rng.uniform(0.01, 3.0, size=(37, 1))).astype(np.float32)
+    q, s = orc.quantize_int8(w)
+    assert q.dtype == np.int8 and np.abs(q.astype(int)).max() == 127
+    assert (np.abs(q.astype(int)).max(axis=1) == 127).all()  # every row reaches its scale
+    deq = orc.dequantize_int8(q, s)
+    # round to nearest: |w - q s| <= s / 2, with fp32 division slack
+    err = np.abs(w.astype(np.float64) - deq)
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-5)).all()
+    # scale is max|w| / 127 in fp32
+    np.testing.assert_array_equal(s, (np.abs(w).max(axis=1) / np.float32(127.0)).astype(np.float32))
