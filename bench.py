@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--noisy", action="store_true",
                     help="noisy top-k gating (training-mode router; noise floor 0.01)")
+    ap.add_argument("--int8", action="store_true",
+                    help="int8 expert weights with per-row scales (quantised by the library)")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step instead: moe_forward + moe_backward")
     ap.add_argument("--no-graph", action="store_true",
@@ -59,15 +61,19 @@ def workload_name(cfg) -> str:
     cap = "none" if cfg.cf is None else f"{cfg.cf:g}"
     shared = f"+{cfg.S}shared" if cfg.S else ""
     noisy = f", noisy top-k gating (noise floor {cfg.noise_min_std:g})" if cfg.noisy else ""
+    wq = " with int8 weights (per-row scales)" if cfg.weights == "int8" else ""
     return (f"{cfg.name} MoE FFN layer: T={cfg.T} d_model={cfg.d} E={cfg.E}{shared} k={cfg.k} "
-            f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts, fp32 router{noisy}")
+            f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts{wq}, fp32 router{noisy}")
 
 
 def bench_config(args):
     from sparse_mixture_experts_scan_b300 import config
+    kw = {}
     if args.noisy:
-        return config(args.config, noisy=True, noise_min_std=0.01)
-    return config(args.config)
+        kw.update(noisy=True, noise_min_std=0.01)
+    if args.int8:
+        kw.update(weights="int8")
+    return config(args.config, **kw)
 
 
 def peaks():
@@ -296,7 +302,10 @@ def algorithmic_gemm_work(cfg, out):
     rows = int(kept.sum())
     esz = 2 if cfg.dtype == "bf16" else 4
     nmat = 3 if cfg.act == "swiglu" else 2
-    w_bytes = touched * nmat * cfg.d * cfg.F * esz
+    if cfg.weights == "int8":  # 1-byte weights and one fp32 scale per output row
+        w_bytes = touched * (nmat * cfg.d * cfg.F + 4 * ((nmat - 1) * cfg.F + cfg.d))
+    else:
+        w_bytes = touched * nmat * cfg.d * cfg.F * esz
     srows = cfg.S * cfg.T
     act_bytes = (rows * (cfg.d + 2 * cfg.F + cfg.d) + cfg.T * cfg.d * (1 if cfg.S else 0)
                  + srows * (2 * cfg.F + cfg.d)) * esz
@@ -350,6 +359,9 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = bench_config(args)
     inp = make_inputs(cfg, seed=rank, device=dev)
+    if cfg.weights == "int8":
+        from sparse_mixture_experts_scan_b300 import quantize_expert_weights
+        inp = quantize_expert_weights(inp)
     layer = MoELayer(cfg, inp, device=dev)
     stream = torch.cuda.current_stream(dev)
     stages = ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
@@ -471,10 +483,15 @@ def run_gpu(args):
                 "frac": achieved / pk["bf16_tflops"]}
     wl_key = args.config + ("_noisy" if cfg.noisy else "")
     fused = cfg.dtype == "bf16"
-    tr = traffic_from_profiles("ffn_fused_tc.cu" if fused else "grouped_gemm_ffma.cu", wl_key)
-    kname = ("moe_grouped_gemm stage: k_ffn_fused_tc (both expert layers, one persistent tcgen05 launch)"
-             + (" + shared-expert k_grouped_gemm_tc launches" if cfg.S else "")) if fused else \
-        "moe_grouped_gemm stage: k_grouped_gemm_ffma (fp32)"
+    if cfg.weights == "int8":
+        wl_key += "_int8"
+        tr = traffic_from_profiles("grouped_gemm_q8.cu", wl_key)
+        kname = "moe_grouped_gemm stage: two k_grouped_gemm_q8 launches (int8 weights, tcgen05)"
+    else:
+        tr = traffic_from_profiles("ffn_fused_tc.cu" if fused else "grouped_gemm_ffma.cu", wl_key)
+        kname = ("moe_grouped_gemm stage: k_ffn_fused_tc (both expert layers, one persistent tcgen05 launch)"
+                 + (" + shared-expert k_grouped_gemm_tc launches" if cfg.S else "")) if fused else \
+            "moe_grouped_gemm stage: k_grouped_gemm_ffma (fp32)"
     roof.update({"traffic": tr, "kernel": kname,
                  "algorithmic_bytes": gemm["bytes"], "algorithmic_flops": gemm["flops"],
                  "touched_experts": gemm["touched_experts"], "kept_rows": gemm["kept_rows"],
@@ -570,6 +587,13 @@ def run_gpu(args):
     cpu_base = None
     if not args.no_cpu_baseline:
         cpu_inp = {k: (None if v is None else v.cpu()) for k, v in inp.items()}
+        if cfg.weights == "int8":  # the oracle runs on the exactly dequantised weights
+            from oracle import moe_oracle as orc
+            for k_ in ("W1", "W3", "W2"):
+                q_ = cpu_inp.get(k_)
+                if q_ is not None:
+                    cpu_inp[k_] = orc.dequantize_int8(q_.numpy().reshape(-1, q_.shape[-1]),
+                                                      cpu_inp[k_ + "_scale"].numpy().reshape(-1)).reshape(q_.shape)
         # about 10 G multiply-adds of expert work: ~10-30 s on the host cores
         per_tok = cfg.d * cfg.F * (3 if cfg.act == "swiglu" else 2) * (cfg.k + cfg.S)
         secs, desc, threads = oracle_step(cfg, cpu_inp, int(max(16, min(cfg.T, 1e10 / per_tok))))

@@ -94,7 +94,20 @@ typedef struct {
     uint32_t flags;     /* MOE_FLAG_* */
     int32_t noisy_gating;  /* 1: noisy top-k gating (training mode, see below); 0: off */
     float noise_min_std;   /* floor added to the noise scale; >= 0, finite */
+    int32_t weight_format; /* moe_weight_format_t */
 } moe_params_t;
+
+/* Expert weight storage ([Arch] §"部署实践": 8-bit expert weights; [Sparse]
+ * §"量化与PagedAttention结合": experts quantised, router kept precise).
+ * MOE_WEIGHTS_INT8: W1, W3, W2 hold int8 q with one fp32 scale per output row,
+ * W[e, n, :] = q[e, n, :] * scale[e, n] (moe_quantize_int8 makes them).  Needs
+ * dtype == MOE_BF16, the tensor-core expert path, n_shared == 0, no
+ * MOE_FLAG_TRAINING, and d_model and d_ff multiples of 16; otherwise
+ * MOE_ERR_UNSUPPORTED.  The router weights stay fp32. */
+typedef enum {
+    MOE_WEIGHTS_DTYPE = 0, /* expert weights in the layer dtype */
+    MOE_WEIGHTS_INT8 = 1   /* int8 expert weights + fp32 per-row scales */
+} moe_weight_format_t;
 
 /* Noisy top-k gating ([Arch] §2.1 noisy_top_k_gating; [Switch] §"代码实战"
  * NoisyTop1Gate).  With noisy_gating = 1 the router also computes
@@ -120,6 +133,9 @@ typedef struct {
     const float* W_noise;   /* [E, d] fp32 noise projection; required iff noisy_gating */
     const float* b_noise;   /* [E] fp32 noise projection bias, or NULL */
     const float* noise_eps; /* [T, E] fp32 standard normal draws; required iff noisy_gating */
+    const float* W1_scale;  /* [E, F] fp32; required iff weight_format == INT8, else NULL */
+    const float* W3_scale;  /* [E, F] fp32; iff INT8 and SwiGLU */
+    const float* W2_scale;  /* [E, d] fp32; iff INT8 */
 } moe_inputs_t;
 
 typedef struct {
@@ -268,6 +284,14 @@ moe_status_t moe_dispatch_positions_noalloc(const moe_params_t* params,
  * The difference across one call is the number of kernels that call enqueues.
  * Host-side counter; needs no device. */
 uint64_t moe_kernel_launches(void);
+
+/* Quantise `rows` rows of `cols` weights (device, `dtype` MOE_BF16 or MOE_F32,
+ * row-major) to int8 with one scale per row: scale = max |w| / 127 (IEEE fp32),
+ * q = round-half-even(w / scale) clamped to [-127, 127]; an all-zero row gets
+ * scale 0 and q 0.  For a layer's W1, W3 ([E, F, d]) call it with rows = E*F,
+ * cols = d; for W2 ([E, d, F]) with rows = E*d, cols = F.  Enqueues one kernel. */
+moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q,
+                               float* scale, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);

@@ -27,6 +27,7 @@ MOE_FLAG_FFMA_EXPERTS = 1
 MOE_FLAG_FFMA_ROUTER = 2
 MOE_FLAG_UNFUSED_EXPERTS = 4
 MOE_FLAG_TRAINING = 8
+MOE_WEIGHTS_DTYPE, MOE_WEIGHTS_INT8 = 0, 1
 MOE_MAX_EXPERTS = 512
 MOE_MAX_TOPK = 32
 MOE_NOALLOC_MAX_SLOTS = 131072
@@ -36,13 +37,13 @@ class moe_params_t(ctypes.Structure):
     _fields_ = [("T", _i32), ("d_model", _i32), ("d_ff", _i32), ("E", _i32), ("k", _i32),
                 ("n_shared", _i32), ("capacity_factor", _f32), ("renormalize", _i32),
                 ("residual_mode", _i32), ("act", _i32), ("dtype", _i32), ("flags", _u32),
-                ("noisy_gating", _i32), ("noise_min_std", _f32)]
+                ("noisy_gating", _i32), ("noise_min_std", _f32), ("weight_format", _i32)]
 
 
 class moe_inputs_t(ctypes.Structure):
     _fields_ = [("x", _vp), ("W_gate", _vp), ("b_gate", _vp), ("W1", _vp), ("W3", _vp),
                 ("W2", _vp), ("b1", _vp), ("b2", _vp), ("W_noise", _vp), ("b_noise", _vp),
-                ("noise_eps", _vp)]
+                ("noise_eps", _vp), ("W1_scale", _vp), ("W3_scale", _vp), ("W2_scale", _vp)]
 
 
 class moe_outputs_t(ctypes.Structure):
@@ -90,6 +91,8 @@ def load(build_if_stale: bool = True):
     L.moe_last_device_status.argtypes = [_vp, ctypes.c_size_t, _vp]
     L.moe_dispatch_positions_noalloc.restype = _i32
     L.moe_dispatch_positions_noalloc.argtypes = [_P(moe_params_t), _vp, _vp, _vp, _vp, _vp]
+    L.moe_quantize_int8.restype = _i32
+    L.moe_quantize_int8.argtypes = [_vp, _i32, ctypes.c_int64, _i32, _vp, _vp, _vp]
     L.moe_kernel_launches.restype = ctypes.c_uint64
     L.moe_kernel_launches.argtypes = []
     L.moe_status_string.restype = ctypes.c_char_p
@@ -153,6 +156,11 @@ def moe_dispatch_positions_noalloc(params, expert_idx, counts, dropped, perm_row
 
 def moe_last_device_status(workspace, workspace_bytes, stream):
     return load().moe_last_device_status(_vp(workspace), ctypes.c_size_t(workspace_bytes), _vp(stream))
+
+
+def moe_quantize_int8(w, dtype, rows, cols, q, scale, stream):
+    return load().moe_quantize_int8(_vp(w), _i32(dtype), ctypes.c_int64(rows), _i32(cols), _vp(q), _vp(scale),
+                                    _vp(stream))
 
 
 def moe_kernel_launches() -> int:

@@ -80,8 +80,13 @@ moe_status_t validate_params(const moe_params_t* p)
         return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (p->noisy_gating != 0 && p->noisy_gating != 1) return MOE_ERR_INVALID_ARG;
+    if (p->weight_format != MOE_WEIGHTS_DTYPE && p->weight_format != MOE_WEIGHTS_INT8) return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(p->noise_min_std) || p->noise_min_std < 0.0f) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    if (p->weight_format == MOE_WEIGHTS_INT8 &&
+        (p->dtype != MOE_BF16 || (p->flags & (MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_TRAINING)) || p->n_shared != 0 ||
+         p->d_model % 16 != 0 || p->d_ff % 16 != 0))
+        return MOE_ERR_UNSUPPORTED;
     // every index and row count below must fit in int32
     const long long slots = (long long)p->T * p->k;
     const long long rows = slots + (long long)p->E * kSegRows + kSegRows;
@@ -181,9 +186,13 @@ moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const mo
         return MOE_ERR_INVALID_ARG;
     if (p.noisy_gating == 1 ? (!in->W_noise || !in->noise_eps) : (in->W_noise || in->b_noise || in->noise_eps))
         return MOE_ERR_INVALID_ARG;
+    if (p.weight_format == MOE_WEIGHTS_INT8 ? (!in->W1_scale || !in->W2_scale || (swiglu != (in->W3_scale != nullptr)))
+                                            : (in->W1_scale || in->W3_scale || in->W2_scale))
+        return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
                           out->y, out->expert_idx, out->gates, out->counts, out->dropped, out->aux,
-                          out->logits, out->probs, out->perm_row, in->W_noise, in->b_noise, in->noise_eps};
+                          out->logits, out->probs, out->perm_row, in->W_noise, in->b_noise, in->noise_eps,
+                          in->W1_scale, in->W3_scale, in->W2_scale};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -221,6 +230,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
+// 2-D byte tensor map over a row-major [rows, cols] int8 matrix, box {64, box_rows},
+// no swizzle (64-byte rows in shared memory), zero fill out of bounds.
+bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, box {64, box_rows},
 // 128-byte swizzle, zero fill out of bounds.
 bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows)
@@ -248,6 +272,8 @@ struct Ctx {
     bool pdl = false;  // false until this call has launched its first kernel
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW, mWn;
+    bool q8 = false;              // int8 expert weights
+    CUtensorMap mQ1, mQ3, mQ2;    // their uint8 maps
     template <typename T>
     T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
     uint32_t* err() const { return reinterpret_cast<uint32_t*>(ws); }
@@ -293,7 +319,21 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
         if (c.p.noisy_gating == 1 && !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, L.r_bn))
             return MOE_ERR_UNSUPPORTED;
     }
-    if (c.use_tc) {
+    c.q8 = c.p.weight_format == MOE_WEIGHTS_INT8;
+    if (c.q8) {
+        const Layout& L = c.L;
+        const bool gated = c.p.act == MOE_ACT_SWIGLU;
+        const uint32_t r1 = gated ? 128 : 256;
+        bool ok = encode_u8_2d(&c.mQ1, in->W1, (uint64_t)L.E * L.F, L.d, r1) &&
+                  encode_u8_2d(&c.mQ3, gated ? in->W3 : in->W1, (uint64_t)L.E * L.F, L.d, r1) &&
+                  encode_u8_2d(&c.mQ2, in->W2, (uint64_t)L.E * L.d, L.F, 256);
+        if (L.rows_cap > 0)
+            ok = ok && encode_bf16_2d(&c.mA1, c.at<void>(L.off_xp), L.rows_cap, L.d, 128) &&
+                 encode_bf16_2d(&c.mA2, c.at<void>(L.off_h), L.rows_cap, L.F, 128);
+        if (!ok) return MOE_ERR_UNSUPPORTED;
+        c.use_tc = false;  // the int8 kernels replace the bf16 tensor-core path
+        c.fused = false;
+    } else if (c.use_tc) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
         c.bn1 = c.fused || gated ? 256 : pick_bn(L.F);
@@ -480,6 +520,39 @@ moe_status_t stage_gemm(Ctx& c)
     // training: the first layer also keeps its pre-activations for the backward pass
     // (relu's derivative comes from H itself)
     const bool save = (c.p.flags & MOE_FLAG_TRAINING) && c.p.act != MOE_ACT_RELU;
+    if (c.q8) {
+        if (mt_routed == 0) return MOE_OK;
+        GroupedGemmQ8Args q1{};
+        q1.mtile_off = g1.mtile_off;
+        q1.row_off = g1.row_off;
+        q1.rows = g1.rows;
+        q1.G = L.E;
+        q1.N = L.F;
+        q1.n_tiles = ceil_div(L.F, gated ? 128 : 256);
+        q1.K = L.d;
+        q1.b_rows_per_group = L.F;
+        q1.out = g1.out;
+        q1.ldo = L.F;
+        q1.bias = c.in->b1;
+        q1.scale = c.in->W1_scale;
+        q1.scale3 = c.in->W3_scale;
+        q1.err = c.err();
+        GroupedGemmQ8Args q2 = q1;
+        q2.N = L.d;
+        q2.n_tiles = ceil_div(L.d, 256);
+        q2.K = L.F;
+        q2.b_rows_per_group = L.d;
+        q2.out = g2.out;
+        q2.ldo = L.d;
+        q2.bias = c.in->b2;
+        q2.scale = c.in->W2_scale;
+        q2.scale3 = nullptr;
+        e = launch_gemm_q8(c.mA1, c.mQ1, c.mQ3, q1, act1, grid_for(mt_routed * q1.n_tiles, 1), c.st, take_pdl(c));
+        if (e == cudaSuccess)
+            e = launch_gemm_q8(c.mA2, c.mQ2, c.mQ2, q2, kActNone, grid_for(mt_routed * q2.n_tiles, 1), c.st,
+                               take_pdl(c));
+        return cuda_status(e);
+    }
     if (save && c.use_tc) {
         g1.z1 = c.at<void>(L.off_bw_z1);
         g1.z3 = gated ? c.at<void>(L.off_bw_z3) : nullptr;
@@ -1346,6 +1419,18 @@ moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, voi
 }
 
 uint64_t moe_kernel_launches(void) { return moe::launch_counter().load(std::memory_order_relaxed); }
+
+moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q, float* scale,
+                               void* stream)
+{
+    if (w == nullptr || q == nullptr || scale == nullptr || rows < 0 || cols < 1) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    return cuda_status(launch_quantize_int8(w, dtype == MOE_BF16, rows, cols, q, scale, sms,
+                                            static_cast<cudaStream_t>(stream)));
+}
 
 const char* moe_status_string(moe_status_t status)
 {

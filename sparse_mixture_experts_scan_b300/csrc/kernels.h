@@ -130,6 +130,31 @@ struct FusedFfnArgs {
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
                                 cudaStream_t st, bool pdl);
 
+// int8 expert weights (bf16 activations): tcgen05 grouped GEMM with the int8 B tile
+// converted to bf16 in shared memory and the per-output-row scales applied in the
+// epilogue.  maps: A (bf16, box {64, 128}), Q and Q3 (uint8 [groups * rows, K], box
+// {64, 256} or {64, 128} for the two SwiGLU halves).
+struct GroupedGemmQ8Args {
+    const int* mtile_off;  // [G+1]
+    const int* row_off;    // [G]
+    const int* rows;       // [G]
+    int G;
+    int N, n_tiles, K;
+    int b_rows_per_group;  // weight rows (and scales) per group
+    void* out;
+    int ldo;
+    const void* bias;      // [G, b_rows_per_group] bf16 or nullptr
+    const float* scale;    // [G, b_rows_per_group] (W1 or W2 rows)
+    const float* scale3;   // SwiGLU: the W3 rows' scales
+    uint32_t* err;
+};
+cudaError_t launch_gemm_q8(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& q3,
+                           const GroupedGemmQ8Args& args, int act, int grid, cudaStream_t st, bool pdl);
+size_t gemm_q8_smem();
+// Per-row symmetric int8 quantisation (scale = max|w| / 127, q = rint(w / scale)).
+cudaError_t launch_quantize_int8(const void* w, bool bf16, long long rows, int cols, int8_t* q, float* scale,
+                                 int sms, cudaStream_t st);
+
 // FFMA kernel over fp32 or bf16 operands (A [a_rows_alloc, lda], B [*, ldb]).
 cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
                              const GroupedGemmArgs& args, int act, bool bf16, int grid,

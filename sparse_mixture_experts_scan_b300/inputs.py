@@ -20,10 +20,15 @@ Configurations (shapes and distributions of the workloads the pages discuss):
   decode    the first 64 tokens of skewed with the same weights (capacity 1.0 -> C = 0)
   decode_nocap  the same without a capacity limit
 
+Int8 expert weights (weights="int8"): the tensors above are drawn as usual; the
+layer quantises W1, W3, W2 itself (moe_quantize_int8), so the inputs carry no
+quantisation arithmetic.
+
 Noisy top-k gating (any config with noisy=True): after the tensors above, W_noise
-is drawn like W_gate, b_noise ~ N(0,1) (noise scales softplus(b) from about 0.1 to
-2.1) and noise_eps ~ N(0,1) of shape [T, E] (the standard normal draws the gate
-scales); for a config with a parent, the first T rows of the parent's draws.
+and b_noise ~ U(-1/sqrt(d), 1/sqrt(d)) (nn.Linear's default initialisation of the
+noise projection; noise scales softplus(x W_noise + b) around 0.4-1.1) and
+noise_eps ~ N(0,1) of shape [T, E] (the standard normal draws the gate scales); for
+a config with a parent, the first T rows of the parent's draws.
 """
 from __future__ import annotations
 
@@ -53,6 +58,7 @@ class LayerConfig:
     parent: str | None = None    # take the first T tokens of this config's inputs
     noisy: bool = False          # noisy top-k gating (training mode)
     noise_min_std: float = 0.0   # floor added to the softplus noise scale
+    weights: str = "dtype"       # dtype | int8 (expert weights quantised per output row)
 
     @property
     def torch_dtype(self):
@@ -138,9 +144,11 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> dict:
     out["b1"] = torch.zeros(ES, F, device=device, dtype=dt) if cfg.bias else None
     out["b2"] = torch.zeros(ES, d, device=device, dtype=dt) if cfg.bias else None
     if cfg.noisy:
-        out["W_noise"] = (_trunc((E, d), math.sqrt(0.1 / d), g, device) if wg_std is None
-                          else _normal((E, d), wg_std, g, device))
-        out["b_noise"] = _normal((E,), 1.0, g, device)
+        # the noise projection as nn.Linear initialises it (U(-1/sqrt(d), 1/sqrt(d)) for the
+        # weight and the bias), as in the NoisyTop1Gate listing
+        bound = 1.0 / math.sqrt(d)
+        out["W_noise"] = (torch.rand((E, d), generator=g, device=device) * 2.0 - 1.0) * bound
+        out["b_noise"] = (torch.rand((E,), generator=g, device=device) * 2.0 - 1.0) * bound
         out["noise_eps"] = _normal((T, E), 1.0, g, device)
     else:
         out["W_noise"] = out["b_noise"] = out["noise_eps"] = None

@@ -33,7 +33,8 @@ def make_params(cfg: LayerConfig, *, flags: int = 0, residual_mode: int | None =
         renormalize=int(cfg.renormalize),
         residual_mode=cfg.residual_mode if residual_mode is None else residual_mode,
         act=ACT_CODES[cfg.act], dtype=_lib.MOE_BF16 if cfg.dtype == "bf16" else _lib.MOE_F32,
-        flags=flags, noisy_gating=int(cfg.noisy), noise_min_std=float(cfg.noise_min_std))
+        flags=flags, noisy_gating=int(cfg.noisy), noise_min_std=float(cfg.noise_min_std),
+        weight_format=_lib.MOE_WEIGHTS_INT8 if cfg.weights == "int8" else _lib.MOE_WEIGHTS_DTYPE)
 
 
 def _ptr(t):
@@ -81,7 +82,8 @@ class MoELayer:
             x=_ptr(w["x"]), W_gate=_ptr(w["W_gate"]), b_gate=_ptr(w.get("b_gate")), W1=_ptr(w["W1"]),
             W3=_ptr(w.get("W3")), W2=_ptr(w["W2"]), b1=_ptr(w.get("b1")), b2=_ptr(w.get("b2")),
             W_noise=_ptr(w.get("W_noise")), b_noise=_ptr(w.get("b_noise")),
-            noise_eps=_ptr(w.get("noise_eps")))
+            noise_eps=_ptr(w.get("noise_eps")), W1_scale=_ptr(w.get("W1_scale")),
+            W3_scale=_ptr(w.get("W3_scale")), W2_scale=_ptr(w.get("W2_scale")))
         o = self.out
         self.outputs = _lib.moe_outputs_t(
             y=_ptr(o["y"]), expert_idx=_ptr(o["expert_idx"]), gates=_ptr(o["gates"]),
@@ -137,6 +139,29 @@ class MoELayer:
     def device_status(self, stream=None) -> int:
         return _lib.moe_last_device_status(self.workspace.data_ptr(), self.workspace_bytes,
                                            _stream_handle(stream))
+
+
+def quantize_int8(w: torch.Tensor, stream=None):
+    """Per-row int8 quantisation of a [..., cols] device tensor (moe_quantize_int8):
+    returns (q int8 of the same shape, scale fp32 of shape [...])."""
+    w = w.contiguous()
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
+    scale = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    dt = _lib.MOE_BF16 if w.dtype == torch.bfloat16 else _lib.MOE_F32
+    check(_lib.moe_quantize_int8(w.data_ptr(), dt, rows, cols, q.data_ptr(), scale.data_ptr(),
+                                 _stream_handle(stream)), "moe_quantize_int8")
+    return q, scale
+
+
+def quantize_expert_weights(weights: dict, stream=None) -> dict:
+    """The layer's inputs with W1, W3, W2 replaced by int8 + per-row scales."""
+    out = dict(weights)
+    for k in ("W1", "W3", "W2"):
+        if weights.get(k) is not None:
+            out[k], out[k + "_scale"] = quantize_int8(weights[k], stream)
+    return out
 
 
 def forward(cfg: LayerConfig, weights: dict, **kw) -> dict:

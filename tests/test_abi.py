@@ -12,7 +12,7 @@ def test_library_exports_every_header_function():
     assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
                           "moe_status_string", "moe_dispatch_positions_noalloc",
-                          "moe_kernel_launches", "moe_backward"}
+                          "moe_kernel_launches", "moe_backward", "moe_quantize_int8"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -25,9 +25,9 @@ def test_status_strings():
 
 
 def test_struct_layouts_match_header():
-    # moe_params_t: 11 int32/float fields, uint32 flags, noisy_gating, noise_min_std
-    assert ctypes.sizeof(_lib.moe_params_t) == 14 * 4
-    assert ctypes.sizeof(_lib.moe_inputs_t) == 11 * 8
+    # moe_params_t: 11 int32/float fields, uint32 flags, noisy_gating, noise_min_std, weight_format
+    assert ctypes.sizeof(_lib.moe_params_t) == 15 * 4
+    assert ctypes.sizeof(_lib.moe_inputs_t) == 14 * 8
     assert ctypes.sizeof(_lib.moe_outputs_t) == 9 * 8
 
 
@@ -221,3 +221,41 @@ def test_backward_validation_happens_before_any_launch():
     assert _lib.moe_backward(p, ins, outs, dy, 0.0, _fake_grads(cfg, ins), 1 << 44, need - 1,
                              None) == _lib.MOE_ERR_WORKSPACE
     assert _lib.moe_kernel_launches() == n0
+
+
+@pytest.mark.parametrize("base,over,expect", [
+    ("switch", {}, _lib.MOE_OK),
+    ("mixtral", {}, _lib.MOE_OK),
+    ("tiny", {}, _lib.MOE_ERR_UNSUPPORTED),                     # fp32 layer
+    ("deepseek", {}, _lib.MOE_ERR_UNSUPPORTED),                 # shared experts
+    ("switch", {"flags": 1}, _lib.MOE_ERR_UNSUPPORTED),          # FFMA experts
+    ("switch", {"flags": 8}, _lib.MOE_ERR_UNSUPPORTED),          # training
+    ("switch", {"d_model": 776}, _lib.MOE_ERR_UNSUPPORTED),      # d not a multiple of 16
+    ("switch", {"weight_format": 2}, _lib.MOE_ERR_INVALID_ARG),
+])
+def test_int8_weight_combinations(base, over, expect):
+    p = make_params(config(base, weights="int8"))
+    for k, v in over.items():
+        setattr(p, k, v)
+    assert _lib.moe_workspace_size(p)[0] == expect
+
+
+def test_int8_scales_must_match_the_format():
+    base = 1 << 40
+    for fmt in ("int8", "dtype"):
+        cfg = config("mixtral", weights=fmt)
+        p = make_params(cfg)
+        _, need = _lib.moe_workspace_size(p)
+        ins, outs = _fake_io(cfg)
+        if fmt == "int8":
+            ins.W1_scale, ins.W2_scale = base + 30 * (1 << 30), base + 31 * (1 << 30)  # W3_scale missing
+        else:
+            ins.W2_scale = base + 31 * (1 << 30)  # a scale with bf16 weights
+        assert _lib.moe_forward(p, ins, outs, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_quantize_rejects_bad_arguments():
+    assert _lib.moe_quantize_int8(None, _lib.MOE_BF16, 4, 8, 1 << 40, 1 << 41, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_quantize_int8(1 << 40, 7, 4, 8, 1 << 40, 1 << 41, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_quantize_int8(1 << 40, _lib.MOE_BF16, 4, 0, 1 << 40, 1 << 41, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_quantize_int8(1 << 40, _lib.MOE_BF16, 0, 8, 1 << 40, 1 << 41, None) == _lib.MOE_OK  # nothing to do
