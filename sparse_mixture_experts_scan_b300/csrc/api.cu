@@ -50,7 +50,7 @@ struct Layout {
     size_t off_bw_dgate, off_bw_dl, off_bw_dn, off_bw_dxr, off_bw_dyp, off_bw_z1, off_bw_z3, off_bw_zs1,
         off_bw_zs3, off_bw_dxs;
     // router gradients on the tensor core: split gradients, paired weights, dW partials
-    int e8, r_nblk;
+    int e8, r_nblk, r_dw_splits;
     size_t off_bw_dcat, off_bw_wcat, off_bw_p;
     size_t total;
 };
@@ -168,7 +168,8 @@ Layout make_layout(const moe_params_t& p)
     const bool tcr = train && L.tc_router;
     L.off_bw_dcat = take(tcr ? sizeof(uint16_t) * (size_t)L.T * L.r_nblk * L.e8 : 0);
     L.off_bw_wcat = take(tcr ? sizeof(uint16_t) * (size_t)L.r_nblk * L.e8 * L.d : 0);
-    L.off_bw_p = take(tcr ? sizeof(float) * 3 * (size_t)L.e8 * L.d * (noisy ? 2 : 1) : 0);
+    L.r_dw_splits = router_dw_splits(L.T, L.e8, L.d);
+    L.off_bw_p = take(tcr ? sizeof(float) * 3 * (size_t)L.e8 * L.d * L.r_dw_splits * (noisy ? 2 : 1) : 0);
     L.total = o;
     return L;
 }
@@ -726,22 +727,30 @@ cudaError_t router_bwd_tc(Ctx& c, const float* dl, const float* dn, float* dxr, 
                                    grid_for((long long)ceil_div(L.T, 128) * ceil_div(L.d, 256)), c.st, take_pdl(c));
     }
     for (int which = 0; which < (noisy ? 2 : 1); ++which) {
-        BwdTcArgs a{};  // partials [3 E8, d] of dW = dl^T x (dn^T x), one per split term
+        // partials [3 E8, d] of dW = dl^T x (dn^T x), one per split term and per token split
+        const int splits = L.r_dw_splits;
+        BwdTcArgs a{};
         a.G = 1;
         a.fixed_rows = L.T;
+        // split boundaries on 64-row K blocks, so no block reads into the next split
+        a.split_rows = splits > 1 ? ceil_div(ceil_div(L.T, splits), 64) * 64 : 0;
         a.M = 3 * L.e8;
         a.N = L.d;
         a.a_col0 = which * 4 * L.e8;
-        float* Pw = P + (size_t)which * 3 * L.e8 * L.d;
+        float* Pw = P + (size_t)which * 3 * L.e8 * L.d * splits;
         a.C = Pw;
+        a.c_gs = 3ll * L.e8 * L.d;
         a.ldc = L.d;
         a.err = c.err();
+        const int n_split = splits > 1 ? ceil_div(L.T, a.split_rows) : 1;
         const CUtensorMap maps[4] = {mD, mX, mD, mX};
         if (e == cudaSuccess)
             e = launch_gemm_bwd_tc(maps, a, kBwdReduce, kEpiStoreF32,
-                                   grid_for((long long)ceil_div(a.M, 128) * ceil_div(L.d, 256)), c.st, take_pdl(c));
+                                   grid_for((long long)n_split * ceil_div(a.M, 128) * ceil_div(L.d, 256)), c.st,
+                                   take_pdl(c));
         if (e == cudaSuccess)
-            e = launch_sum3(Pw, L.E, L.e8, L.d, which ? gr->dW_noise : gr->dW_gate, c.sms, c.st, take_pdl(c));
+            e = launch_sum3(Pw, n_split, L.E, L.e8, L.d, which ? gr->dW_noise : gr->dW_gate, c.sms, c.st,
+                            take_pdl(c));
     }
     return e;
 }

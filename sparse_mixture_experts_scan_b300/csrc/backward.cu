@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(256) k_split_wcat(const float* __restrict__ Wg
     }
 }
 
-__global__ void __launch_bounds__(256) k_sum3(const float* __restrict__ P, int E, int E8, int d,
+__global__ void __launch_bounds__(256) k_sum3(const float* __restrict__ P, int splits, int E, int E8, int d,
                                               float* __restrict__ out)
 {
     griddep_launch_dependents();
@@ -309,8 +309,14 @@ __global__ void __launch_bounds__(256) k_sum3(const float* __restrict__ P, int E
     const long long total = (long long)E * d;
     const long long blk = (long long)E8 * d;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x)
-        out[i] = (P[2 * blk + i] + P[blk + i]) + P[i];  // smallest terms first
+         i += (long long)gridDim.x * blockDim.x) {
+        float acc = 0.0f;
+        for (int sp = 0; sp < splits; ++sp) {
+            const float* p = P + (long long)sp * 3 * blk;
+            acc += (p[2 * blk + i] + p[blk + i]) + p[i];  // smallest terms first
+        }
+        out[i] = acc;
+    }
 }
 
 int elem_grid(long long n, int sms)
@@ -371,9 +377,19 @@ cudaError_t launch_split_wcat(const float* Wg, const float* Wn, int E, int E8, i
                          Wn, E, E8, d, nblk, static_cast<__nv_bfloat16*>(out));
 }
 
-cudaError_t launch_sum3(const float* P, int E, int E8, int d, float* out, int sms, cudaStream_t st, bool pdl)
+cudaError_t launch_sum3(const float* P, int splits, int E, int E8, int d, float* out, int sms, cudaStream_t st,
+                        bool pdl)
 {
-    return launch_kernel(k_sum3, dim3(elem_grid((long long)E * d, sms)), dim3(256), 0, st, pdl, P, E, E8, d, out);
+    return launch_kernel(k_sum3, dim3(elem_grid((long long)E * d, sms)), dim3(256), 0, st, pdl, P, splits, E, E8, d,
+                         out);
+}
+
+int router_dw_splits(int T, int E8, int d)
+{
+    const int tiles = ceil_div(3 * E8, 128) * ceil_div(d, 256);
+    int s = 1;
+    while (s < 16 && tiles * s * 2 <= 148 && ceil_div(T, s * 2) >= 256) s *= 2;
+    return s;
 }
 
 cudaError_t launch_zero_pad_rows(const ZeroPadArgs& a, int sms, cudaStream_t st, bool pdl)

@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool fixed = args.row_off == nullptr;
-    const int G = fixed ? 1 : args.G;
+    const bool split = MODE == kBwdReduce && fixed && args.split_rows > 0;
+    const int G = split ? ceil_div(args.fixed_rows, args.split_rows) : (fixed ? 1 : args.G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -136,8 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_mt[i] = i * ceil_div(args.M, kBM);
     }
     for (int i = threadIdx.x; i < G; i += kThreads) {
-        s_roff[i] = fixed ? 0 : args.row_off[i];
-        s_rows[i] = fixed ? args.fixed_rows : args.rows[i];
+        if (split) {
+            s_roff[i] = i * args.split_rows;
+            s_rows[i] = min(args.split_rows, args.fixed_rows - i * args.split_rows);
+        } else {
+            s_roff[i] = fixed ? 0 : args.row_off[i];
+            s_rows[i] = fixed ? args.fixed_rows : args.rows[i];
+        }
     }
     __syncthreads();
 

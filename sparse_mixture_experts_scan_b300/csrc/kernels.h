@@ -223,6 +223,9 @@ struct BwdTcArgs {
     int M, N, K;
     int b_g0, b_rows_per_group, b_col0;
     int a_col0;           // kBwdReduce: first A column (M offset)
+    int split_rows;       // kBwdReduce with one fixed group: > 0 splits the rows into groups of
+                          // this many (group g -> output block c_g0 + g), a split-K over rows;
+                          // a multiple of 64 (K blocks never cross into the next group)
     int two_seg;
     void* C;
     void* C2;
@@ -256,8 +259,12 @@ cudaError_t launch_split_grad(const float* dl, const float* dn, int T, int E, in
                               int sms, cudaStream_t st, bool pdl);
 cudaError_t launch_split_wcat(const float* Wg, const float* Wn, int E, int E8, int d, int nblk, void* out,
                               int sms, cudaStream_t st, bool pdl);
-// out[e, i] = (P[2 E8 + e, i] + P[E8 + e, i]) + P[e, i], e < E
-cudaError_t launch_sum3(const float* P, int E, int E8, int d, float* out, int sms, cudaStream_t st, bool pdl);
+// out[e, i] = sum over splits s (in order) of (P_s[2 E8 + e, i] + P_s[E8 + e, i]) + P_s[e, i], e < E;
+// P_s = P + s * 3 E8 d
+cudaError_t launch_sum3(const float* P, int splits, int E, int E8, int d, float* out, int sms, cudaStream_t st,
+                        bool pdl);
+// K splits of the router's dW reduction over T tokens (about one CTA per SM)
+int router_dw_splits(int T, int E8, int d);
 
 // ---- backward: memory-bound kernels ---------------------------------------------
 struct BwdCombineArgs {
