@@ -87,6 +87,26 @@ def peaks():
                 "source": "fallback"}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of `value` over all ranks (the value itself without a process group).
+
+    Works with any torch.distributed backend: NCCL on the GPU machine (device = the rank's
+    GPU), gloo on CPU (device None)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job tokens/s of `world` replicas that each process `tokens_per_rank` tokens in
+    `ms` milliseconds (the max over ranks)."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -457,10 +477,8 @@ def run_gpu(args):
     stage_ms = {k_: v / K for k_, v in stage_ms.items()}
     ms_step = sum(a.elapsed_time(b) for a, b in ev_step) / K
     if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * cfg.T / (ms_step * 1e-3)
+        ms_step = max_over_ranks(ms_step, dev)
+    value = replica_throughput(world, cfg.T, ms_step)
 
     out = layer.out
     gemm = algorithmic_gemm_work(cfg, out)
@@ -563,11 +581,9 @@ def run_gpu(args):
         torch.cuda.synchronize()
         e_ms = t0.elapsed_time(t1) / K
         if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+            e_ms = max_over_ranks(e_ms, dev)
         esz = x_host.element_size()
-        e2e = {"value": world * cfg.T / (e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": replica_throughput(world, cfg.T, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": x_host.numel() * esz,
                "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size() + 4,
                "ms_per_step": e_ms,
@@ -709,9 +725,7 @@ def run_gpu_backward(args):
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     ms = fwd_ms + bwd_ms
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
     status = layer.device_status()
     if status != 0:
         print(f"device status {status}", file=sys.stderr)
@@ -732,7 +746,7 @@ def run_gpu_backward(args):
                  "counted)", "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"],
                  "peak_source": pk["source"] + " (burst)"})
     line = {
-        "metric": "MoE layer training step (fwd + bwd) tokens/s on 1 B300", "value": world * cfg.T / (ms * 1e-3),
+        "metric": "MoE layer training step (fwd + bwd) tokens/s on 1 B300", "value": replica_throughput(world, cfg.T, ms),
         "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded; shapes and distributions of the workload; random-init weights)",

@@ -273,3 +273,29 @@ def test_noisy_gating_moves_the_selection():
     clean = run_device(clean_cfg, {k: v for k, v in inp.items() if k not in _NOISE_KEYS})
     moved = (noisy["expert_idx"] != clean["expert_idx"]).any(dim=1).float().mean().item()
     assert 0.05 < moved < 1.0, moved
+
+
+@pytest.mark.parametrize("name", ["swiglu_renorm", "gelu_tanh_bias", "shared_experts", "relu_capacity"])
+def test_training_flag_leaves_forward_outputs_unchanged(name):
+    # MOE_FLAG_TRAINING only adds stores (logits, pre-activations): every output is bit-identical
+    cfg = SMALL[name]
+    inp = _inputs(cfg, random_bias=True)
+    a = run_device(cfg, inp)
+    b = run_device(cfg, inp, flags=_lib.MOE_FLAG_TRAINING)
+    for key, v in a.items():
+        if v is not None:
+            assert torch.equal(v, b[key]), key
+
+
+def test_stage_entry_points_equal_forward_with_noise_and_int8():
+    from sparse_mixture_experts_scan_b300 import quantize_expert_weights
+    for cfg, quant in ((NOISY["noisy_top2_renorm"], False),
+                       (config("mixtral", T=300, d=256, E=8, k=2, F=512, weights="int8"), True)):
+        inp = _inputs(cfg)
+        if quant:
+            inp = quantize_expert_weights(inp)
+        a = run_device(cfg, inp)
+        b = run_device(cfg, inp, stages=["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"])
+        for key, v in a.items():
+            if v is not None:
+                assert torch.equal(v, b[key]), key
