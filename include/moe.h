@@ -29,6 +29,7 @@
  *   - Validation happens before any launch.  On a non-OK status nothing was
  *     enqueued.  Asynchronous device faults surface at the caller's next
  *     synchronisation as usual.
+ *   - For an empty batch (T == 0) the arrays with T rows may be NULL.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -79,7 +80,8 @@ typedef enum {
 #define MOE_MAX_TOPK 32     /* k */
 
 typedef struct {
-    int32_t T;          /* tokens (rows of x) >= 1 */
+    int32_t T;          /* tokens (rows of x) >= 0; T == 0 (an empty batch) launches no kernel:
+                           the forward writes counts = 0 and aux = 0, the backward zero gradients */
     int32_t d_model;    /* d, multiple of 8 */
     int32_t d_ff;       /* F, hidden width of one expert, multiple of 8 */
     int32_t E;          /* routed experts, 1..MOE_MAX_EXPERTS */

@@ -66,7 +66,7 @@ long long capacity_of(const moe_params_t& p)
 moe_status_t validate_params(const moe_params_t* p)
 {
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
-    if (p->T < 1 || p->d_model < 8 || p->d_ff < 8) return MOE_ERR_INVALID_ARG;
+    if (p->T < 0 || p->d_model < 8 || p->d_ff < 8) return MOE_ERR_INVALID_ARG;
     if (p->d_model % 8 != 0 || p->d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
     if (p->E < 1 || p->E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
     if (p->k < 1 || p->k > p->E || p->k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
@@ -180,12 +180,15 @@ moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const mo
 {
     if (in == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
     const bool swiglu = p.act == MOE_ACT_SWIGLU;
-    if (!in->x || !in->W_gate || !in->W1 || !in->W2) return MOE_ERR_INVALID_ARG;
+    // arrays with T rows may be NULL for an empty batch (an empty tensor has no storage)
+    const bool rows = p.T > 0;
+    if ((rows && !in->x) || !in->W_gate || !in->W1 || !in->W2) return MOE_ERR_INVALID_ARG;
     if (swiglu != (in->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
     if (swiglu && (in->b1 || in->b2)) return MOE_ERR_INVALID_ARG;
-    if (!out->y || !out->expert_idx || !out->gates || !out->counts || !out->dropped || !out->aux)
+    if ((rows && (!out->y || !out->expert_idx || !out->gates || !out->dropped)) || !out->counts || !out->aux)
         return MOE_ERR_INVALID_ARG;
-    if (p.noisy_gating == 1 ? (!in->W_noise || !in->noise_eps) : (in->W_noise || in->b_noise || in->noise_eps))
+    if (p.noisy_gating == 1 ? (!in->W_noise || (rows && !in->noise_eps))
+                            : (in->W_noise || in->b_noise || in->noise_eps))
         return MOE_ERR_INVALID_ARG;
     if (p.weight_format == MOE_WEIGHTS_INT8 ? (!in->W1_scale || !in->W2_scale || (swiglu != (in->W3_scale != nullptr)))
                                             : (in->W1_scale || in->W3_scale || in->W2_scale))
@@ -310,6 +313,7 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     c.sms = sm_count();
     if (c.sms <= 0) return MOE_ERR_CUDA;
     c.bf16 = c.p.dtype == MOE_BF16;
+    if (c.L.T == 0) return MOE_OK;  // an empty batch: no kernel, no tensor map
     c.use_tc = c.bf16 && !(c.p.flags & MOE_FLAG_FFMA_EXPERTS);
     c.fused = c.use_tc && !(c.p.flags & MOE_FLAG_UNFUSED_EXPERTS);
     if (c.L.tc_router) {
@@ -359,6 +363,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 moe_status_t stage_router(Ctx& c)
 {
+    if (c.L.T == 0) return MOE_OK;
     RouterArgs a{};
     a.x = c.in->x;
     a.Wg = c.in->W_gate;
@@ -430,6 +435,11 @@ moe_status_t stage_router(Ctx& c)
 
 moe_status_t stage_dispatch(Ctx& c)
 {
+    if (c.L.T == 0) {  // an empty batch: no expert receives a token, the statistic is 0
+        cudaError_t e = cudaMemsetAsync(c.out->counts, 0, sizeof(int32_t) * c.L.E, c.st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c.out->aux, 0, sizeof(float), c.st);
+        return cuda_status(e);
+    }
     DispatchArgs a{};
     a.idx = c.out->expert_idx;
     a.gates = c.out->gates;
@@ -464,6 +474,7 @@ moe_status_t stage_dispatch(Ctx& c)
 
 moe_status_t stage_gemm(Ctx& c)
 {
+    if (c.L.T == 0) return MOE_OK;
     const Layout& L = c.L;
     const bool gated = c.p.act == MOE_ACT_SWIGLU;
     const int act1 = c.p.act;  // moe_act_t values equal the kernels' ActKind values
@@ -638,6 +649,7 @@ moe_status_t stage_gemm(Ctx& c)
 
 moe_status_t stage_combine(Ctx& c)
 {
+    if (c.L.T == 0) return MOE_OK;
     CombineArgs a{};
     a.yp = c.at<void>(c.L.off_yp);
     a.ys = c.L.S > 0 ? c.at<void>(c.L.off_ys) : nullptr;
@@ -673,8 +685,9 @@ moe_status_t run_stages(const moe_params_t* params, const moe_inputs_t* in, moe_
 moe_status_t validate_grads(const moe_params_t& p, const moe_inputs_t* in, const void* dy, float d_aux,
                             const moe_grads_t* g)
 {
-    if (g == nullptr || dy == nullptr || !aligned16(dy) || !std::isfinite(d_aux)) return MOE_ERR_INVALID_ARG;
-    if (!g->dx || !g->dW_gate || !g->dW1 || !g->dW2) return MOE_ERR_INVALID_ARG;
+    const bool rows = p.T > 0;  // dy and dx may be NULL for an empty batch
+    if (g == nullptr || (rows && dy == nullptr) || !aligned16(dy) || !std::isfinite(d_aux)) return MOE_ERR_INVALID_ARG;
+    if ((rows && !g->dx) || !g->dW_gate || !g->dW1 || !g->dW2) return MOE_ERR_INVALID_ARG;
     const bool swiglu = p.act == MOE_ACT_SWIGLU, noisy = p.noisy_gating == 1;
     if ((g->dW3 != nullptr) != swiglu || (g->db_gate != nullptr) != (in->b_gate != nullptr) ||
         (g->db1 != nullptr) != (in->b1 != nullptr) || (g->db2 != nullptr) != (in->b2 != nullptr) ||
@@ -968,6 +981,16 @@ cudaError_t experts_bwd_tc(Ctx& c, const void* dy, const moe_grads_t* gr)
 moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t* gr)
 {
     const Layout& L = c.L;
+    if (L.T == 0) {  // an empty batch: every gradient is zero
+        const size_t ES = (size_t)(L.E + L.S), w = ES * L.F * L.d * L.esz;
+        const std::pair<void*, size_t> z[] = {{gr->dW_gate, 4ull * L.E * L.d}, {gr->db_gate, 4ull * L.E},
+                                              {gr->dW1, w}, {gr->dW3, w}, {gr->dW2, w},
+                                              {gr->db1, ES * L.F * L.esz}, {gr->db2, ES * L.d * L.esz},
+                                              {gr->dW_noise, 4ull * L.E * L.d}, {gr->db_noise, 4ull * L.E}};
+        for (const auto& q : z)
+            if (q.first != nullptr && cudaMemsetAsync(q.first, 0, q.second, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     const size_t esz = L.esz;
     const int types = c.bf16 ? kBwdTypesBf16 : kBwdTypesF32;
     const bool swiglu = c.p.act == MOE_ACT_SWIGLU, noisy = c.p.noisy_gating == 1;

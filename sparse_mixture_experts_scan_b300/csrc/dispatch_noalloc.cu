@@ -98,10 +98,14 @@ extern "C" moe_status_t moe_dispatch_positions_noalloc(const moe_params_t* param
         perm_row == nullptr)
         return MOE_ERR_INVALID_ARG;
     const moe_params_t& p = *params;
-    if (p.T < 1 || p.E < 1 || p.E > MOE_MAX_EXPERTS || p.k < 1 || p.k > p.E || p.k > MOE_MAX_TOPK)
+    if (p.T < 0 || p.E < 1 || p.E > MOE_MAX_EXPERTS || p.k < 1 || p.k > p.E || p.k > MOE_MAX_TOPK)
         return MOE_ERR_INVALID_ARG;
     if ((long long)p.T * p.k > kNoallocMaxSlots) return MOE_ERR_INVALID_ARG;  // scratch too small
     if (p.capacity_factor != p.capacity_factor) return MOE_ERR_INVALID_ARG;
+    if (p.T == 0)  // an empty batch: no expert receives a token
+        return cudaMemsetAsync(counts, 0, sizeof(int32_t) * p.E, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
 
     unsigned char* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;

@@ -323,7 +323,7 @@ cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGe
 int router_tc_bn(int T, int E)
 {
     // Aim for about 128 CTAs (m-tiles x expert tiles), BN a power of two in [16, 128].
-    const int m_tiles = ceil_div(T, kRBM);
+    const int m_tiles = T > 0 ? ceil_div(T, kRBM) : 1;
     const int want_tiles = ceil_div(128, m_tiles);
     const int per_tile = ceil_div(E, want_tiles);
     int bn = 16;

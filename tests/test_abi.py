@@ -48,7 +48,7 @@ def test_workspace_grows_with_tokens():
 
 
 @pytest.mark.parametrize("field,value", [
-    ("k", 0), ("k", 9), ("E", 0), ("E", 513), ("d_model", 12), ("d_ff", 20), ("T", 0),
+    ("k", 0), ("k", 9), ("E", 0), ("E", 513), ("d_model", 12), ("d_ff", 20), ("T", -1),
     ("renormalize", 2), ("residual_mode", 5), ("act", 7), ("dtype", 3), ("flags", 16),
     ("n_shared", -1)])
 def test_invalid_params_rejected(field, value):
@@ -259,3 +259,10 @@ def test_quantize_rejects_bad_arguments():
     assert _lib.moe_quantize_int8(1 << 40, 7, 4, 8, 1 << 40, 1 << 41, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_quantize_int8(1 << 40, _lib.MOE_BF16, 4, 0, 1 << 40, 1 << 41, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_quantize_int8(1 << 40, _lib.MOE_BF16, 0, 8, 1 << 40, 1 << 41, None) == _lib.MOE_OK  # nothing to do
+
+
+def test_empty_batch_is_valid():
+    for name in ("switch", "mixtral", "tiny"):
+        p = make_params(config(name), T=0)
+        st, n = _lib.moe_workspace_size(p)
+        assert st == _lib.MOE_OK and n > 0

@@ -299,3 +299,30 @@ def test_stage_entry_points_equal_forward_with_noise_and_int8():
         for key, v in a.items():
             if v is not None:
                 assert torch.equal(v, b[key]), key
+
+
+def test_empty_batch_forward_and_backward():
+    # T = 0: no kernel; counts and aux are zero, gradients are zero
+    cfg = config("mixtral", T=0, d=64, E=8, k=2, F=64)
+    inp = make_inputs(config("mixtral", T=1, d=64, E=8, k=2, F=64), 0, device="cuda")
+    inp["x"] = inp["x"][:0]
+    layer = MoELayer(cfg, inp, flags=_lib.MOE_FLAG_TRAINING)
+    layer.out["counts"].fill_(7)
+    layer.out["aux"].fill_(7.0)
+    n0 = _lib.moe_kernel_launches()
+    layer.run()
+    grads = layer.backward(torch.zeros(0, cfg.d, dtype=cfg.torch_dtype, device="cuda"), 0.5)
+    torch.cuda.synchronize()
+    assert _lib.moe_kernel_launches() == n0
+    assert layer.device_status() == _lib.MOE_OK
+    assert int(layer.out["counts"].abs().sum()) == 0 and float(layer.out["aux"][0]) == 0.0
+    for k, v in grads.items():
+        if v is not None:
+            assert int(torch.count_nonzero(v)) == 0, k
+
+
+def test_maximum_top_k():
+    # k = MOE_MAX_TOPK = 32 of E = 64 (and of E = 512) experts
+    for cfg in (config("mixtral", T=200, d=64, E=64, k=32, F=64),
+                config("mixtral", T=100, d=64, E=512, k=32, F=64, cf=1.0)):
+        _full_check(cfg, _inputs(cfg))
