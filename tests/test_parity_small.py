@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as orc
-from sparse_mixture_experts_scan_b300 import _lib, config, make_inputs
+from sparse_mixture_experts_scan_b300 import MoELayer, _lib, config, make_inputs
 from parity_utils import (check_dropped_tokens_pass_x, check_output, check_router_vs_fp64,
                           check_routing_bitexact, run_device, to_cpu)
 
