@@ -35,6 +35,7 @@ struct Layout {
     int t_pad;         // T rounded up to 128 (shared-expert buffers)
     size_t esz;        // element size of the activation dtype
     bool tc_router;    // bf16 router logits on the tensor core
+    bool tc_rbwd;      // router gradients on the tensor core (bf16 layers)
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
     int r_ksplits;             // router GEMM K splits
     size_t off_wsplit, off_logits;
@@ -117,6 +118,7 @@ Layout make_layout(const moe_params_t& p)
     L.t_pad = (p.T + kSegRows - 1) / kSegRows * kSegRows;
     L.esz = (p.dtype == MOE_BF16) ? 2 : 4;
     L.tc_router = p.dtype == MOE_BF16 && !(p.flags & MOE_FLAG_FFMA_ROUTER);
+    L.tc_rbwd = L.tc_router;
     L.r_bn = router_tc_bn(p.T, p.E);
     L.r_tiles = (p.E + L.r_bn - 1) / L.r_bn;
     L.e_pad = L.r_tiles * L.r_bn;
@@ -165,7 +167,7 @@ Layout make_layout(const moe_params_t& p)
     L.off_bw_dxs = bw(L.S > 0 ? L.esz * (size_t)L.T * L.d : 0);
     L.e8 = (L.E + 7) / 8 * 8;
     L.r_nblk = noisy ? 8 : 4;
-    const bool tcr = train && L.tc_router;
+    const bool tcr = train && L.tc_rbwd;
     L.off_bw_dcat = take(tcr ? sizeof(uint16_t) * (size_t)L.T * L.r_nblk * L.e8 : 0);
     L.off_bw_wcat = take(tcr ? sizeof(uint16_t) * (size_t)L.r_nblk * L.e8 * L.d : 0);
     L.r_dw_splits = router_dw_splits(L.T, L.e8, L.d);
@@ -1050,7 +1052,7 @@ moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t
         rb.dn = dn;
     }
     if (e == cudaSuccess) e = launch_router_bwd(rb, c.sms, c.st, take_pdl(c));
-    if (L.tc_router) {
+    if (L.tc_rbwd) {
         if (e == cudaSuccess) e = router_bwd_tc(c, dl, dn, dxr, gr);
     } else {
         {

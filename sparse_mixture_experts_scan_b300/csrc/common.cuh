@@ -13,6 +13,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -82,15 +83,18 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 // launches (including ones recorded into CUDA graphs) make no attribute call.
 inline cudaError_t ensure_smem_limit(const void* kernel, size_t bytes)
 {
+    // the largest limit set so far per (kernel, device): kernels whose shared memory
+    // depends on the layer's sizes raise it again when a later layer needs more
     static std::mutex mu;
-    static std::set<std::pair<const void*, int>> done;
+    static std::map<std::pair<const void*, int>, size_t> done;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    if (done.count({kernel, dev})) return cudaSuccess;
+    auto it = done.find({kernel, dev});
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) done.insert({kernel, dev});
+    if (e == cudaSuccess) done[{kernel, dev}] = bytes;
     return e;
 }
 __host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -120,6 +124,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 16-byte read-only load through the non-coherent path (data written by an earlier kernel).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
 }
 
 // 16-byte vectors of a row as fp32: 8 bf16 or 4 fp32 elements.

@@ -226,14 +226,6 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
     if (tid == 0) *a.scan_done = 0u;  // re-arm for the next call
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
 
 __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
 {

@@ -42,6 +42,7 @@ cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st, bool 
 // Softmax / top-k / gates of logits already in a.logits.
 cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st);
 
+
 // Tensor-core router logits (bf16 x, W_gate split into three bf16 terms).
 struct RouterGemmArgs {
     int T, d, E;

@@ -12,7 +12,7 @@
 // The tensor core adds each MMA's partial products into the TMEM accumulator
 // with less than IEEE fp32 precision, so the error of one long accumulation
 // chain grows with its length (3 d / 16 MMAs).  The K loop is therefore cut
-// into chunks of kChunkKB K-blocks: each chunk accumulates in one of two TMEM
+// into chunks of a few K-blocks: each chunk accumulates in one of two TMEM
 // accumulators (alternating, so the MMAs of chunk c+1 overlap the drain of
 // chunk c), and the epilogue warps add every finished chunk into fp32
 // registers with round-to-nearest additions.  The error is then bounded by the
@@ -35,7 +35,11 @@ namespace {
 constexpr int kRBM = 128;
 constexpr int kRBK = 64;
 constexpr int kRThreads = 192;
-constexpr int kChunkKB = 2;  // K-blocks (of 64) per TMEM accumulation chunk
+// K-blocks (of 64) per TMEM accumulation chunk: 2 for wide expert tiles; 4 for
+// BN <= 32, where a chunk's MMAs are short and the per-chunk promotion would
+// dominate (the error bound doubles and stays below the fp32 FFMA router's)
+template <int BN>
+constexpr int chunk_kb() { return BN <= 32 ? 4 : 2; }
 
 template <int BN>
 struct RCfg {
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                 const int ks = tile / (m_tiles * a.n_tiles);
                 const int kbeg = ks * kb_per_split;
                 const int num_kb = min(kbeg + kb_per_split, num_kb_all);
-                for (int kb0 = kbeg; kb0 < num_kb && ok; kb0 += kChunkKB, ++ci) {
+                for (int kb0 = kbeg; kb0 < num_kb && ok; kb0 += chunk_kb<BN>(), ++ci) {
                     const int acc = ci & 1;
                     if (!mbar_wait(&tempty[acc], ((ci >> 1) & 1) ^ 1u, abort_flag)) {
                         ok = false;
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + acc * BN;
-                    const int kb1 = kb0 + kChunkKB < num_kb ? kb0 + kChunkKB : num_kb;
+                    const int kb1 = kb0 + chunk_kb<BN>() < num_kb ? kb0 + chunk_kb<BN>() : num_kb;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag)) {
                             ok = false;
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             float sum[BN];
 #pragma unroll
             for (int i = 0; i < BN; ++i) sum[i] = 0.0f;
-            for (int kb0 = kbeg; kb0 < num_kb; kb0 += kChunkKB, ++ci) {
+            for (int kb0 = kbeg; kb0 < num_kb; kb0 += chunk_kb<BN>(), ++ci) {
                 const int acc = ci & 1;
                 if (!mbar_wait(&tfull[acc], (ci >> 1) & 1, abort_flag)) {
                     ok = false;

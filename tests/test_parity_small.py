@@ -326,3 +326,11 @@ def test_maximum_top_k():
     for cfg in (config("mixtral", T=200, d=64, E=64, k=32, F=64),
                 config("mixtral", T=100, d=64, E=512, k=32, F=64, cf=1.0)):
         _full_check(cfg, _inputs(cfg))
+
+
+def test_layers_of_growing_size_in_one_process():
+    # kernels whose dynamic shared memory depends on the layer (router for few experts,
+    # dispatch scan) raise their limit when a later layer needs more
+    for cfg in (config("mixtral", T=64, d=64, E=8, k=2, F=64), config("mixtral", T=64, d=4096, E=8, k=2, F=64),
+                config("skewed", T=64, d=64, E=64, k=4, F=64), config("skewed", T=64, d=64, E=512, k=4, F=64)):
+        _full_check(cfg, _inputs(cfg))
