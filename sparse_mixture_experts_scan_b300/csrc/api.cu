@@ -321,9 +321,10 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.L.tc_router) {
         const Layout& L = c.L;
         if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) ||
-            !encode_bf16_2d(&c.mW, c.at<void>(L.off_wsplit), 3ull * L.e_pad, L.d, L.r_bn))
+            !encode_bf16_2d(&c.mW, c.at<void>(L.off_wsplit), 3ull * L.e_pad, L.d, 3 * L.r_bn))
             return MOE_ERR_UNSUPPORTED;
-        if (c.p.noisy_gating == 1 && !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, L.r_bn))
+        if (c.p.noisy_gating == 1 &&
+            !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, 3 * L.r_bn))
             return MOE_ERR_UNSUPPORTED;
     }
     c.q8 = c.p.weight_format == MOE_WEIGHTS_INT8;
@@ -419,7 +420,7 @@ moe_status_t stage_router(Ctx& c)
     g.bg = c.in->b_gate;
     g.logits = split ? parts : a.logits;
     g.err = c.err();
-    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
+    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.r_bn, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
                                        take_pdl(c));
     if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
     if (noisy) {  // the same GEMM on W_noise, without bias, into the noise-logit partials
@@ -427,7 +428,7 @@ moe_status_t stage_router(Ctx& c)
         gn.bg = nullptr;
         gn.logits = c.at<float>(c.L.off_nlogits);
         if (e == cudaSuccess)
-            e = launch_split_wgate(c.in->W_noise, c.L.E, c.L.e_pad, c.L.d, c.at<void>(c.L.off_nsplit), c.sms, c.st,
+            e = launch_split_wgate(c.in->W_noise, c.L.E, c.L.e_pad, c.L.r_bn, c.L.d, c.at<void>(c.L.off_nsplit), c.sms, c.st,
                                    take_pdl(c));
         if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mWn, gn, c.L.r_bn, c.sms, c.st);
     }

@@ -53,9 +53,9 @@ struct RouterGemmArgs {
     float* logits;        // [T, E] fp32 when k_splits == 1, else [k_splits, T, E] partial sums
     uint32_t* err;
 };
-int router_tc_bn(int T, int E);  // MMA N of the router GEMM (16..128), ~128 CTAs
+int router_tc_bn(int T, int E);  // experts per router GEMM tile (16..64; MMA N = 3x), ~128 CTAs
 int router_tc_ksplits(int T, int E, int d);  // K splits so that small batches still fill ~128 CTAs
-cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms,
+cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d, void* out, int sms,
                                cudaStream_t st, bool pdl);
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
                                     int bn, int sms, cudaStream_t st);

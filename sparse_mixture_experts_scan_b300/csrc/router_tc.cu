@@ -18,12 +18,13 @@
 // registers with round-to-nearest additions.  The error is then bounded by the
 // chunk length, independent of d, and comparable to an fp32 FFMA dot product.
 //
-// k_split_wgate writes [3, E_pad, d] bf16 (rows >= E zero) into the workspace.
-// k_router_logits_tc: persistent, one CTA per SM, warp-specialised like the
-// grouped GEMM: warp 0 TMA (x tile 128 x 64 + the three W tiles BN x 64 of one
-// K-block per stage), warp 1 tcgen05.mma (M = 128, N = BN, three splits, lo
-// first, one accumulator per chunk), warps 2-5 epilogue (chunk promotion into
-// fp32 registers, bias add, fp32 logits to global).  Softmax,
+// k_split_wgate writes the three terms tile by tile, [E_pad / BN][3][BN][d] bf16
+// (rows >= E zero), into the workspace.  k_router_logits_tc: persistent, one CTA
+// per SM, warp-specialised like the grouped GEMM: warp 0 TMA (x tile 128 x 64 and
+// one box of the tile's 3 BN term rows per stage), warp 1 tcgen05.mma (M = 128,
+// N = 3 BN: the hi, mid and lo products of a K-step in one instruction, each in
+// its own column group of the accumulator), warps 2-5 epilogue (chunk promotion
+// (lo + mid) + hi into fp32 registers, bias add, fp32 logits to global).  Softmax,
 // top-k and gates follow in k_router_topk (router.cu).
 #include "common.cuh"
 #include "kernels.h"
@@ -41,33 +42,40 @@ constexpr int kRThreads = 192;
 template <int BN>
 constexpr int chunk_kb() { return BN <= 32 ? 4 : 2; }
 
+// BN = experts per tile; the three split terms of the tile's experts are stacked
+// along the MMA's N dimension (N = 3 BN): one MMA per K-step covers all three.
 template <int BN>
 struct RCfg {
+    static constexpr int N = 3 * BN;
     static constexpr uint32_t A_BYTES = kRBM * kRBK * 2;
-    static constexpr uint32_t B_BYTES = BN * kRBK * 2;  // one split
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+    static constexpr uint32_t B_BYTES = N * kRBK * 2;  // the three splits
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_FIT = 196608 / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+    static constexpr uint32_t TMEM_COLS = 2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 2 * N <= 256 ? 256 : 512;
     static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 256;
 };
 
-__global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int d,
+// out is [E_pad / BN][3][BN][d]: for each tile of BN experts, its hi, mid and lo rows
+// (rows >= E zero), so one TMA box of 3 BN rows holds a tile's three terms.
+__global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int BN, int d,
                                                      __nv_bfloat16* __restrict__ out)
 {
     griddep_launch_dependents();
     griddep_wait();
     const size_t n = (size_t)E_pad * d;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const int e = (int)(i / d);
+        const int e = (int)(i / d), col = (int)(i - (size_t)e * d);
         const float w = e < E ? Wg[i] : 0.0f;  // Wg is [E, d]: the same flat index for e < E
         const __nv_bfloat16 hi = __float2bfloat16_rn(w);
         const float r1 = w - __bfloat162float(hi);  // exact
         const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
         const float r2 = r1 - __bfloat162float(mid);  // exact
-        out[i] = hi;
-        out[n + i] = mid;
-        out[2 * n + i] = __float2bfloat16_rn(r2);
+        const int tile = e / BN, el = e - tile * BN;
+        const size_t r0 = (size_t)tile * 3 * BN + el;  // hi row; mid and lo rows BN and 2 BN further
+        out[r0 * d + col] = hi;
+        out[(r0 + BN) * d + col] = mid;
+        out[(r0 + 2 * BN) * d + col] = __float2bfloat16_rn(r2);
     }
 }
 
@@ -97,14 +105,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
                        const RouterGemmArgs a)
 {
     using C = RCfg<BN>;
-    constexpr uint32_t IDESC = idesc_bf16_f32(kRBM, BN);
+    constexpr uint32_t IDESC = idesc_bf16_f32(kRBM, C::N);
     constexpr int CHUNK = BN < 32 ? BN : 32;  // TMEM columns per epilogue load
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sA = base;
     uint8_t* sB = base + C::STAGES * C::A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * 3 * C::B_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
     uint64_t* empty = full + C::STAGES;
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
@@ -164,11 +172,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                     }
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     tma_load_2d(sA + stage * C::A_BYTES, &tmX, &full[stage], kb * kRBK, m * kRBM, pol);
-                    uint8_t* dB = sB + stage * 3 * C::B_BYTES;
-#pragma unroll
-                    for (int s = 0; s < 3; ++s)
-                        tma_load_2d(dB + s * C::B_BYTES, &tmW, &full[stage], kb * kRBK,
-                                    s * a.E_pad + n * BN, pol);
+                    tma_load_2d(sB + stage * C::B_BYTES, &tmW, &full[stage], kb * kRBK, n * C::N, pol);
                     filled |= 1u << stage;
                     fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    const uint32_t d_tmem = tmem_base + acc * C::N;
                     const int kb1 = kb0 + chunk_kb<BN>() < num_kb ? kb0 + chunk_kb<BN>() : num_kb;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -210,14 +214,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
                         }
                         tc_fence_after_sync();
                         const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
-                        const uint32_t b0 = smem_u32(sB + stage * 3 * C::B_BYTES);
+                        const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+                        // hi, mid and lo terms land in column groups [0, BN), [BN, 2 BN), [2 BN, 3 BN)
 #pragma unroll
-                        for (int s = 2; s >= 0; --s)  // smallest split first
-#pragma unroll
-                            for (int k = 0; k < kRBK / 16; ++k)
-                                mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32),
-                                            sdesc_kmajor_sw128(b0 + s * C::B_BYTES + k * 32), IDESC,
-                                            (kb == kb0 && s == 2 && k == 0) ? 0u : 1u);
+                        for (int k = 0; k < kRBK / 16; ++k)
+                            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32),
+                                        IDESC, (kb == kb0 && k == 0) ? 0u : 1u);
                         mma_commit(&empty[stage]);
                         if (++stage == C::STAGES) {
                             stage = 0;
@@ -254,21 +256,30 @@ __global__ void __launch_bounds__(kRThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+                const uint32_t t_lane = tmem_base + acc * C::N + (static_cast<uint32_t>(q * 32) << 16);
+                // promote the chunk: (lo + mid) + hi per expert, added to the fp32 running sums
 #pragma unroll
                 for (int c = 0; c < BN / CHUNK; ++c) {
                     if constexpr (CHUNK == 32) {
-                        uint32_t r[32];
-                        tmem_ld_32cols(t_lane + c * 32, r);
+                        uint32_t rh[32], rm[32], rl[32];
+                        tmem_ld_32cols(t_lane + c * 32, rh);
+                        tmem_ld_32cols(t_lane + BN + c * 32, rm);
+                        tmem_ld_32cols(t_lane + 2 * BN + c * 32, rl);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(r[i]);
+                        for (int i = 0; i < 32; ++i)
+                            sum[c * 32 + i] +=
+                                (__uint_as_float(rl[i]) + __uint_as_float(rm[i])) + __uint_as_float(rh[i]);
                     } else {
-                        uint32_t r[16];
-                        tmem_ld_16cols(t_lane + c * 16, r);
+                        uint32_t rh[16], rm[16], rl[16];
+                        tmem_ld_16cols(t_lane + c * 16, rh);
+                        tmem_ld_16cols(t_lane + BN + c * 16, rm);
+                        tmem_ld_16cols(t_lane + 2 * BN + c * 16, rl);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) sum[c * 16 + i] += __uint_as_float(r[i]);
+                        for (int i = 0; i < 16; ++i)
+                            sum[c * 16 + i] +=
+                                (__uint_as_float(rl[i]) + __uint_as_float(rm[i])) + __uint_as_float(rh[i]);
                     }
                 }
                 tc_fence_before_sync();
@@ -331,7 +342,7 @@ int router_tc_bn(int T, int E)
     const int want_tiles = ceil_div(128, m_tiles);
     const int per_tile = ceil_div(E, want_tiles);
     int bn = 16;
-    while (bn < per_tile && bn < 128) bn *= 2;
+    while (bn < per_tile && bn < 64) bn *= 2;  // 3 bn <= 256 columns per MMA
     return bn;
 }
 
@@ -345,13 +356,13 @@ int router_tc_ksplits(int T, int E, int d)
     return ks;
 }
 
-cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int d, void* out, int sms, cudaStream_t st,
+cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d, void* out, int sms, cudaStream_t st,
                                bool pdl)
 {
     const size_t n = (size_t)E_pad * d;
     size_t grid = (n + 255) / 256;
     if (grid > (size_t)sms * 8) grid = (size_t)sms * 8;
-    return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, d,
+    return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, bn, d,
                          static_cast<__nv_bfloat16*>(out));
 }
 
@@ -361,8 +372,7 @@ cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, 
     switch (bn) {
     case 16: return launch_bn<16>(x, w, a, sms, st);
     case 32: return launch_bn<32>(x, w, a, sms, st);
-    case 64: return launch_bn<64>(x, w, a, sms, st);
-    default: return launch_bn<128>(x, w, a, sms, st);
+    default: return launch_bn<64>(x, w, a, sms, st);
     }
 }
 
