@@ -252,16 +252,16 @@ __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
         const uint4* src =
             reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)t * a.row_bytes);
         uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)row * a.row_bytes);
-        int v = lane;
-        for (; v + 96 < nvec; v += 128) {
-            const uint4 r0 = ld_stream(src + v), r1 = ld_stream(src + v + 32);
-            const uint4 r2 = ld_stream(src + v + 64), r3 = ld_stream(src + v + 96);
-            dst[v] = r0;
-            dst[v + 32] = r1;
-            dst[v + 64] = r2;
-            dst[v + 96] = r3;
+        // up to four 16-byte vectors per lane in flight before any store
+        for (int v = lane; v < nvec; v += 128) {
+            uint4 r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + 32 * u < nvec) r[u] = ld_stream(src + v + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + 32 * u < nvec) dst[v + 32 * u] = r[u];
         }
-        for (; v < nvec; v += 32) dst[v] = ld_stream(src + v);
     }
 }
 
