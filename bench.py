@@ -583,10 +583,11 @@ def run_gpu(args):
         if world > 1:
             e_ms = max_over_ranks(e_ms, dev)
         esz = x_host.element_size()
+        h2d = x_host.numel() * esz
+        d2h = y_host[0].numel() * y_host[0].element_size() + 4
         e2e = {"value": replica_throughput(world, cfg.T, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": x_host.numel() * esz,
-               "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size() + 4,
-               "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms, "pcie_GB/s": (h2d + d2h) / (e_ms * 1e-3) / 1e9,
                "method": "moe_forward per step (its CUDA graph) on pinned host buffers; upload, "
                          "compute and download of consecutive steps overlap on three streams"}
         layer = layers[0]
