@@ -420,6 +420,17 @@ moe_status_t stage_router(Ctx& c)
     g.bg = c.in->b_gate;
     g.logits = split ? parts : a.logits;
     g.err = c.err();
+    // one expert tile and no K split: the GEMM's epilogue finishes the router
+    g.fuse = (!noisy && c.L.r_tiles == 1 && c.L.r_ksplits == 1 && c.L.r_bn <= 32) ? 1 : 0;
+    if (g.fuse) {
+        g.k = a.k;
+        g.renormalize = a.renormalize;
+        g.idx = a.idx;
+        g.gates = a.gates;
+        g.probs = a.probs;
+        g.psum_part = a.psum_part;
+        g.scan_done = a.scan_done;
+    }
     cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.r_bn, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
                                        take_pdl(c));
     if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
@@ -432,7 +443,7 @@ moe_status_t stage_router(Ctx& c)
                                    take_pdl(c));
         if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mWn, gn, c.L.r_bn, c.sms, c.st);
     }
-    if (e == cudaSuccess) e = launch_router_topk(a, c.st);
+    if (e == cudaSuccess && !g.fuse) e = launch_router_topk(a, c.st);
     return cuda_status(e);
 }
 

@@ -52,6 +52,14 @@ struct RouterGemmArgs {
     const float* bg;      // [E] or nullptr (added here only when k_splits == 1)
     float* logits;        // [T, E] fp32 when k_splits == 1, else [k_splits, T, E] partial sums
     uint32_t* err;
+    // fuse != 0 (one tile of at most 32 experts, no K split): softmax, top-k, gates and the
+    // per-32-token column sums of p are computed in the epilogue (no separate top-k kernel)
+    int fuse, k, renormalize;
+    int32_t* idx;         // [T, k]
+    float* gates;         // [T, k]
+    float* probs;         // [T, E] or nullptr
+    float* psum_part;     // [ceil(T / 32), E]
+    unsigned* scan_done;  // dispatch-scan arrival counter, reset here
 };
 int router_tc_bn(int T, int E);  // experts per router GEMM tile (16..64; MMA N = 3x), ~128 CTAs
 int router_tc_ksplits(int T, int E, int d);  // K splits so that small batches still fill ~128 CTAs

@@ -99,7 +99,78 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
         : "r"(taddr));
 }
 
+// The rest of the router for one token per thread when a tile holds every expert:
+// logits (+ bias) written out, softmax, the k largest logits (ties to the lower expert
+// index, a NaN logit competing as -inf), gates (renormalised over the k when asked),
+// probabilities if asked, and the column sums of p over the warp's 32 tokens (one
+// psum_part row per 32-token group, as the top-k kernel writes them).  Every lane of
+// the warp must call it (the column sums are warp reductions); rows >= T add nothing.
 template <int BN>
+__device__ __forceinline__ void route_rows(const float (&sum)[BN], int row, int group, const RouterGemmArgs& a)
+{
+    const bool valid = row < a.T;
+    const int E = a.E;
+    float l[BN];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < BN; ++e) {
+        l[e] = e < E ? sum[e] + (a.bg != nullptr ? a.bg[e] : 0.0f) : -INFINITY;
+        mx = fmaxf(mx, l[e]);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int e = 0; e < BN; ++e) s += e < E ? expf(l[e] - mx) : 0.0f;
+    const float inv = 1.0f / s;
+    if (valid) {
+        float* lrow = a.logits + (size_t)row * E;
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+            if (e < E) lrow[e] = l[e];
+        // top-k rounds over (logit desc, expert asc)
+        uint64_t taken = 0;
+        float gsum = 0.0f;
+        for (int r = 0; r < a.k; ++r) {
+            float bv = -INFINITY;
+            int be = -1;
+#pragma unroll
+            for (int e = 0; e < BN; ++e) {
+                const float v = (l[e] != l[e]) ? -INFINITY : l[e];
+                if (e < E && !((taken >> e) & 1ull) && (be < 0 || v > bv)) {
+                    bv = v;
+                    be = e;
+                }
+            }
+            taken |= 1ull << be;
+            float le = 0.0f;
+#pragma unroll
+            for (int e = 0; e < BN; ++e)
+                if (e == be) le = l[e];
+            const float pe = expf(le - mx) * inv;
+            a.idx[(size_t)row * a.k + r] = be;
+            a.gates[(size_t)row * a.k + r] = pe;
+            gsum += pe;
+        }
+        if (a.renormalize)
+            for (int r = 0; r < a.k; ++r) a.gates[(size_t)row * a.k + r] /= gsum;
+    }
+    // probabilities and their column sums over the warp's rows
+    const int lane = threadIdx.x & 31;
+    float mine = 0.0f;  // lane e ends with expert e's sum (lanes 0..31), the rest in a loop
+#pragma unroll
+    for (int e = 0; e < BN; ++e) {
+        float pe = (valid && e < E) ? expf(l[e] - mx) * inv : 0.0f;
+        if (valid && e < E && a.probs != nullptr) a.probs[(size_t)row * E + e] = pe;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+        if ((e & 31) == lane) mine = pe;
+        if ((e & 31) == 31 || e == BN - 1) {  // a batch of 32 experts is complete
+            const int e0 = e & ~31;
+            if (group * 32 < a.T && e0 + lane < E && e0 + lane <= e) a.psum_part[(size_t)group * E + e0 + lane] = mine;
+        }
+    }
+}
+
+template <int BN, bool FUSE>
 __global__ void __launch_bounds__(kRThreads, 1)
     k_router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const RouterGemmArgs a)
@@ -148,6 +219,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     griddep_wait();  // the W_gate splits come from the previous kernel
+    if (FUSE && blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
 
     const int m_tiles = ceil_div(a.T, kRBM);
     const int total = m_tiles * a.n_tiles * a.k_splits;
@@ -288,6 +360,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
             if (!ok) break;
             const int row = m * kRBM + q * 32 + lane;
+            if constexpr (FUSE) {
+                route_rows<BN>(sum, row, m * 4 + q, a);
+                continue;
+            }
             if (row < a.T) {
                 // one K range: partial sums without bias, summed by the top-k kernel
                 const bool split = a.k_splits > 1;
@@ -321,11 +397,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int BN>
+template <int BN, bool FUSE>
 cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a, int sms,
                       cudaStream_t st)
 {
-    auto kern = k_router_logits_tc<BN>;
+    auto kern = k_router_logits_tc<BN, FUSE>;
     const size_t smem = RCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -369,10 +445,12 @@ cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d,
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
                                     int bn, int sms, cudaStream_t st)
 {
+    // a.fuse is set only for tiles of at most 32 experts (one tile, no K split): there the
+    // epilogue's per-token softmax and top-k are short; wider tiles keep the top-k kernel
     switch (bn) {
-    case 16: return launch_bn<16>(x, w, a, sms, st);
-    case 32: return launch_bn<32>(x, w, a, sms, st);
-    default: return launch_bn<64>(x, w, a, sms, st);
+    case 16: return a.fuse ? launch_bn<16, true>(x, w, a, sms, st) : launch_bn<16, false>(x, w, a, sms, st);
+    case 32: return a.fuse ? launch_bn<32, true>(x, w, a, sms, st) : launch_bn<32, false>(x, w, a, sms, st);
+    default: return launch_bn<64, false>(x, w, a, sms, st);
     }
 }
 
