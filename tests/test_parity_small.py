@@ -334,3 +334,27 @@ def test_layers_of_growing_size_in_one_process():
     for cfg in (config("mixtral", T=64, d=64, E=8, k=2, F=64), config("mixtral", T=64, d=4096, E=8, k=2, F=64),
                 config("skewed", T=64, d=64, E=64, k=4, F=64), config("skewed", T=64, d=64, E=512, k=4, F=64)):
         _full_check(cfg, _inputs(cfg))
+
+
+def _random_config(seed):
+    rng = np.random.default_rng(1000 + seed)
+    act = ["relu", "gelu_tanh", "swiglu", "gelu_erf", "swiglu", "swiglu"][seed % 6]
+    E = [1, 3, 8, 16, 31, 64, 100, 300, 24, 130, 7, 48][seed % 12]
+    k = int(rng.integers(1, min(E, 8) + 1))
+    S = int(rng.integers(1, 3)) if act == "swiglu" and seed % 2 == 0 else 0
+    dtype = "f32" if rng.random() < 0.2 else "bf16"
+    cf = None if rng.random() < 0.4 else float(rng.choice([0.5, 1.0, 1.25, 2.0]))
+    return config("mixtral", T=int(rng.integers(1, 700)), d=8 * int(rng.integers(1, 48)),
+                  F=8 * int(rng.integers(1, 64)), E=E, k=k, S=S, act=act, dtype=dtype, cf=cf,
+                  renormalize=bool(rng.integers(2)), bias=act != "swiglu" and bool(rng.integers(2)),
+                  residual_mode=int(rng.integers(2)), noisy=bool(rng.random() < 0.25),
+                  noise_min_std=0.01)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_layers_match_oracle(seed):
+    # seeded random shapes and options: every combination of router tile width, K split,
+    # fused top-k, combine segmentation and expert path that the heuristics can pick
+    cfg = _random_config(seed)
+    out, _ = _full_check(cfg, _inputs(cfg, seed=seed, random_bias=True), residual_mode=cfg.residual_mode)
+    assert out["expert_idx"].shape == (cfg.T, cfg.k)
