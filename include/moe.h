@@ -295,6 +295,15 @@ uint64_t moe_kernel_launches(void);
 moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q,
                                float* scale, void* stream);
 
+/* Diagnostic: enqueues one kernel whose bounded wait (on a barrier that nothing
+ * arrives at) expires after timeout_us microseconds (1 .. 1e6) and records the
+ * expiry in the workspace's error word, exactly as the layer's kernels do when a
+ * wait of theirs expires.  The next moe_last_device_status on this workspace then
+ * returns MOE_ERR_DEVICE_TIMEOUT (and clears the word); the CUDA context stays
+ * usable.  For testing the failure-detection path; not needed otherwise. */
+moe_status_t moe_check_bounded_wait(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                    void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 

@@ -93,6 +93,8 @@ def load(build_if_stale: bool = True):
     L.moe_dispatch_positions_noalloc.argtypes = [_P(moe_params_t), _vp, _vp, _vp, _vp, _vp]
     L.moe_quantize_int8.restype = _i32
     L.moe_quantize_int8.argtypes = [_vp, _i32, ctypes.c_int64, _i32, _vp, _vp, _vp]
+    L.moe_check_bounded_wait.restype = _i32
+    L.moe_check_bounded_wait.argtypes = [_vp, ctypes.c_size_t, _u32, _vp]
     L.moe_kernel_launches.restype = ctypes.c_uint64
     L.moe_kernel_launches.argtypes = []
     L.moe_status_string.restype = ctypes.c_char_p
@@ -161,6 +163,11 @@ def moe_last_device_status(workspace, workspace_bytes, stream):
 def moe_quantize_int8(w, dtype, rows, cols, q, scale, stream):
     return load().moe_quantize_int8(_vp(w), _i32(dtype), ctypes.c_int64(rows), _i32(cols), _vp(q), _vp(scale),
                                     _vp(stream))
+
+
+def moe_check_bounded_wait(workspace, workspace_bytes, timeout_us, stream):
+    return load().moe_check_bounded_wait(_vp(workspace), ctypes.c_size_t(workspace_bytes), _u32(timeout_us),
+                                         _vp(stream))
 
 
 def moe_kernel_launches() -> int:

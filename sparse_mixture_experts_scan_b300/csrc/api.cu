@@ -1466,6 +1466,16 @@ moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, voi
 
 uint64_t moe_kernel_launches(void) { return moe::launch_counter().load(std::memory_order_relaxed); }
 
+moe_status_t moe_check_bounded_wait(void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream)
+{
+    if (workspace == nullptr || workspace_bytes < sizeof(uint32_t) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return MOE_ERR_WORKSPACE;
+    if (timeout_us < 1 || timeout_us > 1000000) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_expires(static_cast<uint32_t*>(workspace), 1000ull * timeout_us,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q, float* scale,
                                void* stream)
 {

@@ -328,6 +328,11 @@ struct BwdUnpermuteArgs {
 };
 cudaError_t launch_bwd_unpermute(const BwdUnpermuteArgs& a, bool bf16, int sms, cudaStream_t st, bool pdl);
 
+// ---- diagnostics ------------------------------------------------------------
+// One kernel whose bounded wait on a barrier nobody arrives at expires after
+// timeout_ns and sets an error bit in *err, as the layer's kernels do on expiry.
+cudaError_t launch_wait_expires(uint32_t* err, unsigned long long timeout_ns, cudaStream_t st);
+
 // ---- stage 4: combine ------------------------------------------------------
 struct CombineArgs {
     const void* yp;       // [rows_cap, d]

@@ -12,7 +12,8 @@ def test_library_exports_every_header_function():
     assert set(names) == {"moe_workspace_size", "moe_forward", "moe_router", "moe_dispatch",
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
                           "moe_status_string", "moe_dispatch_positions_noalloc",
-                          "moe_kernel_launches", "moe_backward", "moe_quantize_int8"}
+                          "moe_kernel_launches", "moe_backward", "moe_quantize_int8",
+                          "moe_check_bounded_wait"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -266,3 +267,13 @@ def test_empty_batch_is_valid():
         p = make_params(config(name), T=0)
         st, n = _lib.moe_workspace_size(p)
         assert st == _lib.MOE_OK and n > 0
+
+
+def test_bounded_wait_check_validates_before_launch():
+    n0 = _lib.moe_kernel_launches()
+    assert _lib.moe_check_bounded_wait(None, 1024, 1000, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.moe_check_bounded_wait(1 << 40, 2, 1000, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.moe_check_bounded_wait((1 << 40) + 16, 1024, 1000, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.moe_check_bounded_wait(1 << 40, 1024, 0, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_check_bounded_wait(1 << 40, 1024, 2000000, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0

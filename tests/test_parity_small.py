@@ -358,3 +358,21 @@ def test_random_layers_match_oracle(seed):
     cfg = _random_config(seed)
     out, _ = _full_check(cfg, _inputs(cfg, seed=seed, random_bias=True), residual_mode=cfg.residual_mode)
     assert out["expert_idx"].shape == (cfg.T, cfg.k)
+
+
+def test_expired_device_wait_is_reported_and_the_context_stays_usable():
+    # a bounded wait that runs out (a barrier nothing arrives at, 20 ms) sets the
+    # workspace's error word; moe_last_device_status reports it once, then the layer runs
+    cfg = SMALL["swiglu_renorm"]
+    inp = _inputs(cfg)
+    layer = MoELayer(cfg, inp, want_logits=True, want_probs=True)
+    st = torch.cuda.current_stream().cuda_stream
+    assert _lib.moe_check_bounded_wait(layer.workspace.data_ptr(), layer.workspace_bytes, 20000, st) == _lib.MOE_OK
+    assert layer.device_status() == _lib.MOE_ERR_DEVICE_TIMEOUT
+    assert layer.device_status() == _lib.MOE_OK  # read and cleared
+    layer.run()
+    torch.cuda.synchronize()
+    assert layer.device_status() == _lib.MOE_OK
+    out = to_cpu(layer.out)
+    r = check_routing_bitexact(cfg, out)
+    check_output(cfg, to_cpu(inp), out, r)
