@@ -4,7 +4,7 @@
 // ("混合专家 MOE 是什么" §"公式：三步走": g = softmax(W_g x); the router is
 // computed in fp32 as "MoE 混合专家模型串讲" §"选择性精度" prescribes).
 // p = softmax over the E routed experts; the k largest logits are selected
-// with a warp-shuffle argmax, ties to the lower expert index ("混合专家模型MoE
+// with warp reductions (redux.sync max/min), ties to the lower expert index ("混合专家模型MoE
 // 入门实战" §3.3 torch.topk; "MoE架构解析" §2.1 top_k on the logits - the same
 // experts, softmax being monotone).  Gates are p, or p divided by the sum of
 // the k selected p ("混合专家模型MoE入门实战" §3.3 重新归一化).
@@ -26,16 +26,40 @@ constexpr int kTokPerWarp = kRouterTokens / 8;
 // lane, lane+32, ...; -inf beyond E), executed by a whole warp.  Adds the token's
 // probabilities to the lane's running column sums.  write_logits = false when
 // the logits row already sits in a.logits.
+// Order-preserving 32-bit key of a logit for the top-k: a larger float gets a larger
+// key, NaN competes as -inf and -0 as +0 (so equal logits tie and the lower expert
+// index wins).  Every key of a real candidate is >= key(-inf) = 0x007fffff > 0, so 0
+// marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    v = (v != v) ? -INFINITY : (v == 0.0f ? 0.0f : v);
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Softmax, top-k and gates of one token from its logit row l (lane owns experts
+// lane, lane+32, ...; -inf beyond E), executed by a whole warp.  Adds the token's
+// probabilities to the lane's running column sums.  write_logits = false when
+// the logits row already sits in a.logits.
 template <int EJ>
 __device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const RouterArgs& a,
                                             bool write_logits, float (&psum)[EJ])
 {
     const int lane = threadIdx.x & 31;
-    float m = -INFINITY;
+    uint32_t key[EJ];
+    uint32_t kmax = 0;
 #pragma unroll
-    for (int j = 0; j < EJ; ++j) m = fmaxf(m, l[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int j = 0; j < EJ; ++j) {
+        key[j] = (lane + 32 * j < a.E) ? order_key(l[j]) : 0u;
+        kmax = max(kmax, key[j]);
+    }
+    // the row maximum (NaN ignored) by one warp reduction of the keys
+    const float m = key_value(__reduce_max_sync(0xffffffffu, kmax));
     float p[EJ];
     float s = 0.0f;
 #pragma unroll
@@ -58,40 +82,34 @@ __device__ __forceinline__ void route_token(const float (&l)[EJ], int t, const R
         }
     }
 
-    // top-k: k rounds of a warp argmax over (logit desc, expert asc).  A NaN logit
-    // competes as -inf, so every comparison is ordered and the winner of each round
-    // is always one of the E experts (k <= E), whatever the inputs hold.
-    float ls[EJ];
-#pragma unroll
-    for (int j = 0; j < EJ; ++j) ls[j] = (l[j] != l[j]) ? -INFINITY : l[j];
-    uint32_t taken = 0;
+    // top-k: k rounds of a warp argmax over (logit desc, expert asc), each two warp
+    // reductions: the largest key among the lanes' best untaken candidates, then the
+    // lowest expert holding it.  A lane's best is its first (lowest-index) maximum, so
+    // the lowest expert with the round's key is the lowest of those lanes' bests.
+    // k <= E, so every round finds an expert.
     int my_e = 0;
     float my_p = 0.0f, gsum = 0.0f;
     for (int r = 0; r < a.k; ++r) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-        float bp = 0.0f;
+        uint32_t lk = 0u, le = 0xffffffffu;
 #pragma unroll
-        for (int j = 0; j < EJ; ++j) {
-            const int e = lane + 32 * j;
-            if (e < a.E && !((taken >> j) & 1u) && (ls[j] > bv || be == 0x7fffffff)) {
-                bv = ls[j];
-                be = e;
-                bp = p[j];
+        for (int j = 0; j < EJ; ++j)
+            if (key[j] > lk) {
+                lk = key[j];
+                le = (uint32_t)(lane + 32 * j);
             }
-        }
+        const uint32_t rk = __reduce_max_sync(0xffffffffu, lk);
+        const int be = (int)__reduce_min_sync(0xffffffffu, lk == rk ? le : 0xffffffffu);
+        const int bj = be >> 5;
+        float pj = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-                bp = op;
-            }
+        for (int j = 0; j < EJ; ++j)
+            if (j == bj) pj = p[j];
+        const float bp = __shfl_sync(0xffffffffu, pj, be & 31);
+        if ((be & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < EJ; ++j)
+                if (j == bj) key[j] = 0u;  // taken
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
         if (lane == r) {
             my_e = be;
             my_p = bp;
@@ -249,16 +267,30 @@ __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
             l[i][j] = in ? (a.logit_parts == nullptr ? a.logits[(size_t)t * a.E + e] : 0.0f) : -INFINITY;
         }
     if (a.logit_parts != nullptr) {
-        // split-K: add the partial sums in K order (each round's loads are independent)
-        for (int ks = 0; ks < a.k_splits; ++ks) {
-            const float* part = a.logit_parts + (size_t)ks * a.T * a.E;
+        // split-K: add the partial sums in K order; the loads of PF splits are issued
+        // before their additions
+        constexpr int PF = TPW * EJ <= 16 ? 4 : 1;
+        for (int ks0 = 0; ks0 < a.k_splits; ks0 += PF) {
+            float v[PF][TPW][EJ];
 #pragma unroll
-            for (int i = 0; i < TPW; ++i)
+            for (int u = 0; u < PF; ++u) {
+                const float* part = a.logit_parts + (size_t)(ks0 + u) * a.T * a.E;
 #pragma unroll
-                for (int j = 0; j < EJ; ++j) {
-                    const int t = t0 + warp * TPW + i, e = lane + 32 * j;
-                    if (t < a.T && e < a.E) l[i][j] += part[(size_t)t * a.E + e];
-                }
+                for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                    for (int j = 0; j < EJ; ++j) {
+                        const int t = t0 + warp * TPW + i, e = lane + 32 * j;
+                        v[u][i][j] = (ks0 + u < a.k_splits && t < a.T && e < a.E) ? __ldcg(&part[(size_t)t * a.E + e])
+                                                                                  : 0.0f;
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < PF; ++u)
+#pragma unroll
+                for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                    for (int j = 0; j < EJ; ++j)
+                        if (ks0 + u < a.k_splits) l[i][j] += v[u][i][j];
         }
 #pragma unroll
         for (int i = 0; i < TPW; ++i)

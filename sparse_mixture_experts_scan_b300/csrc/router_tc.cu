@@ -56,26 +56,62 @@ struct RCfg {
     static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 256;
 };
 
+// The three bf16 terms of one fp32 weight: hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid); both differences are exact in fp32.
+__device__ __forceinline__ void split3(float w, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo)
+{
+    hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    mid = __float2bfloat16_rn(r1);
+    lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
+
 // out is [E_pad / BN][3][BN][d]: for each tile of BN experts, its hi, mid and lo rows
-// (rows >= E zero), so one TMA box of 3 BN rows holds a tile's three terms.
+// (rows >= E zero), so one TMA box of 3 BN rows holds a tile's three terms.  With d a
+// multiple of 8 and W_gate 16-byte aligned every thread splits 8 consecutive weights
+// of a row (two 16-byte loads, three 16-byte stores); otherwise one weight.
 __global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int BN, int d,
                                                      __nv_bfloat16* __restrict__ out)
 {
     griddep_launch_dependents();
     griddep_wait();
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    if ((d & 7) == 0 && (reinterpret_cast<uintptr_t>(Wg) & 15u) == 0) {
+        const size_t n8 = (size_t)E_pad * d / 8;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+            const int e = (int)(i * 8 / d), col = (int)(i * 8 - (size_t)e * d);
+            float w[8];
+            if (e < E) {
+                const float4 u0 = __ldg(reinterpret_cast<const float4*>(Wg + (size_t)e * d + col));
+                const float4 u1 = __ldg(reinterpret_cast<const float4*>(Wg + (size_t)e * d + col + 4));
+                w[0] = u0.x, w[1] = u0.y, w[2] = u0.z, w[3] = u0.w;
+                w[4] = u1.x, w[5] = u1.y, w[6] = u1.z, w[7] = u1.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = 0.0f;
+            }
+            __align__(16) __nv_bfloat16 h[8], m[8], lo[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) split3(w[q], h[q], m[q], lo[q]);
+            const int tile = e / BN, el = e - tile * BN;
+            const size_t r0 = (size_t)tile * 3 * BN + el;  // hi row; mid and lo rows BN and 2 BN further
+            *reinterpret_cast<uint4*>(out + r0 * d + col) = *reinterpret_cast<const uint4*>(h);
+            *reinterpret_cast<uint4*>(out + (r0 + BN) * d + col) = *reinterpret_cast<const uint4*>(m);
+            *reinterpret_cast<uint4*>(out + (r0 + 2 * BN) * d + col) = *reinterpret_cast<const uint4*>(lo);
+        }
+        return;
+    }
     const size_t n = (size_t)E_pad * d;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int e = (int)(i / d), col = (int)(i - (size_t)e * d);
         const float w = e < E ? Wg[i] : 0.0f;  // Wg is [E, d]: the same flat index for e < E
-        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        const float r1 = w - __bfloat162float(hi);  // exact
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const float r2 = r1 - __bfloat162float(mid);  // exact
+        __nv_bfloat16 h, m, lo;
+        split3(w, h, m, lo);
         const int tile = e / BN, el = e - tile * BN;
-        const size_t r0 = (size_t)tile * 3 * BN + el;  // hi row; mid and lo rows BN and 2 BN further
-        out[r0 * d + col] = hi;
-        out[(r0 + BN) * d + col] = mid;
-        out[(r0 + 2 * BN) * d + col] = __float2bfloat16_rn(r2);
+        const size_t r0 = (size_t)tile * 3 * BN + el;
+        out[r0 * d + col] = h;
+        out[(r0 + BN) * d + col] = m;
+        out[(r0 + 2 * BN) * d + col] = lo;
     }
 }
 
@@ -228,7 +264,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol = policy_evict_last();  // x and W are re-read by other CTAs
+            // W is re-read by every M-tile and x by every expert tile; with one expert
+            // tile x streams through once and is marked evict-first
+            const uint64_t pol = policy_evict_last();
+            const uint64_t pol_x = a.n_tiles > 1 ? pol : policy_evict_first();
             int stage = 0;
             uint32_t phase = 0, filled = 0, fill_par = 0;
             bool ok = true;
@@ -243,7 +282,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    tma_load_2d(sA + stage * C::A_BYTES, &tmX, &full[stage], kb * kRBK, m * kRBM, pol);
+                    tma_load_2d(sA + stage * C::A_BYTES, &tmX, &full[stage], kb * kRBK, m * kRBM, pol_x);
                     tma_load_2d(sB + stage * C::B_BYTES, &tmW, &full[stage], kb * kRBK, n * C::N, pol);
                     filled |= 1u << stage;
                     fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
@@ -435,7 +474,7 @@ int router_tc_ksplits(int T, int E, int d)
 cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d, void* out, int sms, cudaStream_t st,
                                bool pdl)
 {
-    const size_t n = (size_t)E_pad * d;
+    const size_t n = (d % 8 == 0) ? (size_t)E_pad * d / 8 : (size_t)E_pad * d;
     size_t grid = (n + 255) / 256;
     if (grid > (size_t)sms * 8) grid = (size_t)sms * 8;
     return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, bn, d,
