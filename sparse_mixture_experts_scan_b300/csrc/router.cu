@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
     if (a.logit_parts != nullptr) {
         // split-K: add the partial sums in K order; the loads of PF splits are issued
         // before their additions
-        constexpr int PF = TPW * EJ <= 16 ? 4 : 1;
+        constexpr int PF = TPW * EJ <= 8 ? 8 : TPW * EJ <= 16 ? 4 : 1;
         for (int ks0 = 0; ks0 < a.k_splits; ks0 += PF) {
             float v[PF][TPW][EJ];
 #pragma unroll
