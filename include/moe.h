@@ -169,7 +169,7 @@ moe_status_t moe_forward(const moe_params_t* params, const moe_inputs_t* inputs,
 /* Stage 1, router.  logits[t,e] = sum_i x[t,i] W_gate[e,i] + b_gate[e] in fp32
  * ([Basic] §"公式：三步走"; the router runs in fp32 as [Switch] §"选择性精度"
  * prescribes), p = softmax over the E routed experts ([Basic] §"一个小算例"),
- * the k largest logits per token (warp-shuffle top-k; [Intro] §3.3, [Arch]
+ * the k largest logits per token (warp-reduction top-k; [Intro] §3.3, [Arch]
  * §2.1), gates = p or p renormalised over the k ([Intro] §3.3), and per-block
  * column sums of p for the balance statistic.  Writes expert_idx, gates and the
  * optional logits/probs; the rest lives in the workspace. */

@@ -11,7 +11,7 @@
 //
 // One block = 32 tokens = 8 warps x 4 tokens; lane l of a warp owns experts
 // l, l+32, ... (EJ of them), so after the d-loop every warp holds full logit
-// rows of its tokens in registers and finishes softmax/top-k with shuffles.
+// rows of its tokens in registers and finishes softmax/top-k with warp reductions.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
     float psum[EJ];
 #pragma unroll
     for (int j = 0; j < EJ; ++j) psum[j] = 0.0f;
-    // all loads of the warp's tokens first, then the dependent shuffle chains
+    // all loads of the warp's tokens first, then the dependent reduction chains
     float l[TPW][EJ];
 #pragma unroll
     for (int i = 0; i < TPW; ++i)
