@@ -22,10 +22,6 @@ namespace {
 constexpr int kRouterBK = 16;  // d-chunk staged in shared memory
 constexpr int kTokPerWarp = kRouterTokens / 8;
 
-// Softmax, top-k and gates of one token from its logit row l (lane owns experts
-// lane, lane+32, ...; -inf beyond E), executed by a whole warp.  Adds the token's
-// probabilities to the lane's running column sums.  write_logits = false when
-// the logits row already sits in a.logits.
 // Order-preserving 32-bit key of a logit for the top-k: a larger float gets a larger
 // key, NaN competes as -inf and -0 as +0 (so equal logits tie and the lower expert
 // index wins).  Every key of a real candidate is >= key(-inf) = 0x007fffff > 0, so 0
