@@ -38,6 +38,7 @@ struct Layout {
     bool tc_rbwd;      // router gradients on the tensor core (bf16 layers)
     int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
     int r_ksplits;             // router GEMM K splits
+    bool r_fuse;               // top-k in the router GEMM's epilogue
     size_t off_wsplit, off_logits;
     size_t off_nsplit, off_nlogits;  // noisy gating: W_noise splits, noise logits [ks, T, E]
     size_t off_psum_chunk;
@@ -109,7 +110,6 @@ Layout make_layout(const moe_params_t& p)
     L.S = p.n_shared;
     L.k = p.k;
     L.C = (int)capacity_of(p);
-    L.n_rblk = router_blocks(p.T);
     const long long slots = (long long)p.T * p.k;
     L.nchunks = (int)((slots + kScanChunk - 1) / kScanChunk);
     long long cap = slots + (long long)p.E * (kSegRows - 1);
@@ -123,6 +123,10 @@ Layout make_layout(const moe_params_t& p)
     L.r_tiles = (p.E + L.r_bn - 1) / L.r_bn;
     L.e_pad = L.r_tiles * L.r_bn;
     L.r_ksplits = L.tc_router ? router_tc_ksplits(p.T, p.E, p.d_model) : 1;
+    // one expert tile and no K split: the router GEMM's epilogue finishes the router;
+    // otherwise (tensor-core logits) k_router_topk does, with its own column-sum rows
+    L.r_fuse = L.tc_router && p.noisy_gating != 1 && L.r_tiles == 1 && L.r_ksplits == 1 && L.r_bn <= 32;
+    L.n_rblk = (L.tc_router && !L.r_fuse) ? router_topk_blocks(p.T) : router_blocks(p.T);
 
     size_t o = kRegionAlign;  // header: [0] device error word, [1] scan arrival counter
     auto take = [&](size_t bytes) {
@@ -420,8 +424,7 @@ moe_status_t stage_router(Ctx& c)
     g.bg = c.in->b_gate;
     g.logits = split ? parts : a.logits;
     g.err = c.err();
-    // one expert tile and no K split: the GEMM's epilogue finishes the router
-    g.fuse = (!noisy && c.L.r_tiles == 1 && c.L.r_ksplits == 1 && c.L.r_bn <= 32) ? 1 : 0;
+    g.fuse = c.L.r_fuse ? 1 : 0;
     if (g.fuse) {
         g.k = a.k;
         g.renormalize = a.renormalize;

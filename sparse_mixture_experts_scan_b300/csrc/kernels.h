@@ -24,7 +24,7 @@ struct RouterArgs {
     float* gates;         // [T, k]
     float* logits;        // [T, E] or nullptr
     float* probs;         // [T, E] or nullptr
-    float* psum_part;     // [router_blocks(T), E] per-block column sums of p
+    float* psum_part;     // [router_blocks(T) or router_topk_blocks(T), E] per-block column sums of p
     unsigned* scan_done;  // dispatch-scan arrival counter, reset here
     const float* logit_parts;  // k_router_topk with split-K logits: [k_splits, T, E], else nullptr
     int k_splits;
@@ -36,7 +36,11 @@ struct RouterArgs {
     float min_std;
     float* raw_out;       // k_router only: write x W^T (no bias, no routing) here and stop
 };
+// Rows of per-block column sums of p: k_router and the fused tensor-core router write
+// one per 32 tokens (router_blocks), k_router_topk one per kTopkTokens tokens.
 int router_blocks(int T);
+constexpr int kTopkTokens = 8;
+int router_topk_blocks(int T);
 // CUDA-core router: fp32 logits by FFMA, then softmax / top-k / gates.
 cudaError_t launch_router(const RouterArgs& a, bool bf16, cudaStream_t st, bool pdl);
 // Softmax / top-k / gates of logits already in a.logits.

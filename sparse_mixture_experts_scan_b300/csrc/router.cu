@@ -236,18 +236,18 @@ __global__ void __launch_bounds__(256) k_router(RouterArgs a)
 // NOISY: the noise of noisy top-k gating is added first ("MoE架构解析" §2.1
 // noisy_top_k_gating; "MoE 混合专家模型串讲" §"代码实战" NoisyTop1Gate), so softmax,
 // top-k, gates and the column sums all see the noisy logits, which are written out.
-// A block covers 32 tokens (the column-sum layout of k_router), WARPS warps with
-// 32 / WARPS tokens each: one token per warp when the registers allow it (E <= 256),
-// so a small batch still runs many independent warps.
+// A block covers kTopkTokens tokens, one per warp, and writes one row of column
+// sums of p (router_topk_blocks(T) rows in all): a small batch still spreads over
+// many SMs.
 template <int EJ, int WARPS, bool NOISY>
 __global__ void __launch_bounds__(WARPS * 32) k_router_topk(RouterArgs a)
 {
-    constexpr int TPW = kRouterTokens / WARPS;  // tokens per warp
+    constexpr int TPW = kTopkTokens / WARPS;  // tokens per warp
     __shared__ float scratch[WARPS * 32 * EJ];
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * kRouterTokens;
+    const int t0 = blockIdx.x * kTopkTokens;
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
     float psum[EJ];
 #pragma unroll
@@ -347,8 +347,8 @@ cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t st, bool pdl)
 template <int EJ>
 cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
 {
-    constexpr int WARPS = EJ <= 8 ? 32 : 8;
-    const dim3 grid(ceil_div(a.T, kRouterTokens)), block(WARPS * 32);
+    constexpr int WARPS = kTopkTokens;
+    const dim3 grid(router_topk_blocks(a.T)), block(WARPS * 32);
     if (a.eps != nullptr) return launch_kernel(k_router_topk<EJ, WARPS, true>, grid, block, 0, st, true, a);
     return launch_kernel(k_router_topk<EJ, WARPS, false>, grid, block, 0, st, true, a);
 }
@@ -356,6 +356,8 @@ cudaError_t launch_topk_ej(const RouterArgs& a, cudaStream_t st)
 }  // namespace
 
 int router_blocks(int T) { return ceil_div(T, kRouterTokens); }
+
+int router_topk_blocks(int T) { return ceil_div(T, kTopkTokens); }
 
 cudaError_t launch_router_topk(const RouterArgs& a, cudaStream_t st)
 {
