@@ -139,7 +139,7 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
 // logits (+ bias) written out, softmax, the k largest logits (ties to the lower expert
 // index, a NaN logit competing as -inf), gates (renormalised over the k when asked),
 // probabilities if asked, and the column sums of p over the warp's 32 tokens (one
-// psum_part row per 32-token group, as the top-k kernel writes them).  Every lane of
+// psum_part row per 32-token group, router_blocks(T) rows in all).  Every lane of
 // the warp must call it (the column sums are warp reductions); rows >= T add nothing.
 template <int BN>
 __device__ __forceinline__ void route_rows(const float (&sum)[BN], int row, int group, const RouterGemmArgs& a)
