@@ -3,8 +3,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
-Default workload: the Switch top-1 layer (T=8192, d=768, E=128, k=1, d_ff=3072,
-capacity factor 1.25, bf16 experts, fp32 router) on seeded synthetic inputs.
+Default workload: the Mixtral-shaped top-2 layer (T=16384, d=4096, E=8, k=2,
+SwiGLU d_ff=14336, renormalised gates, no capacity limit, bf16 experts, fp32
+router), the largest of the layer configurations, on seeded synthetic inputs;
+--config switch|deepseek|skewed|decode|decode_nocap|tiny selects another.
 A step is one pass of the whole layer (router, dispatch, grouped GEMM,
 combine) through the C ABI, timed with CUDA events on the launching stream;
 L2 is flushed (a 2x-L2 buffer is written) between steps, outside the timed
@@ -42,7 +44,16 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="switch")
+    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (a smaller case of the same layer shape, e.g. for ncu captures)")
+    ap.add_argument("--d-ff", type=int, default=None,
+                    help="override d_ff (router, dispatch and combine do not depend on it)")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="only run warm-up + steps forwards through moe_forward (direct launches, no "
+                         "timing, no e2e, no CPU baseline): the command ncu captures")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where the nvidia-smi clock samples of the timed region go (default: a temp file)")
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -73,6 +84,10 @@ def bench_config(args):
         kw.update(noisy=True, noise_min_std=0.01)
     if args.int8:
         kw.update(weights="int8")
+    if args.tokens is not None:
+        kw.update(T=args.tokens)
+    if args.d_ff is not None:
+        kw.update(F=args.d_ff)
     return config(args.config, **kw)
 
 
@@ -105,6 +120,13 @@ def replica_throughput(world: int, tokens_per_rank: int, ms: float) -> float:
     """Whole-job tokens/s of `world` replicas that each process `tokens_per_rank` tokens in
     `ms` milliseconds (the max over ranks)."""
     return world * tokens_per_rank / (ms * 1e-3)
+
+
+def clocks_path(args, rank: int) -> str:
+    if args.clocks_csv:
+        return args.clocks_csv if rank == 0 else f"{args.clocks_csv}.rank{rank}"
+    import tempfile
+    return os.path.join(tempfile.gettempdir(), f"moe_bench_clocks_rank{rank}.csv")
 
 
 def dist_env():
@@ -288,16 +310,21 @@ def run_reference(args):
         s, descs, threads = oracle_step(cfg, inp, n_sample)
         secs.append(s)
     wall = time.perf_counter() - t_wall
-    per_step = sum(secs) / len(secs)
+    per_step = sum(secs) / len(secs)  # seconds the whole batch would take (extrapolated)
     value = cfg.T / per_step
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "steps": args.steps, "warmup": args.warmup,
+        # wall time each step actually spent (routing of all T tokens + the expert sample)
+        "ms_per_step": wall / max(args.steps, 1) * 1e3,
+        # the whole batch's time, the expert part extrapolated per kept slot: value = T / this
+        "extrapolated_ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": descs + f"; {args.steps} steps in {wall:.1f} s wall"},
+                         "sample": descs + f"; {args.steps} steps in {wall:.1f} s wall; value = T / "
+                                           "extrapolated_ms_per_step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -385,6 +412,17 @@ def run_gpu(args):
     layer = MoELayer(cfg, inp, device=dev)
     stream = torch.cuda.current_stream(dev)
     stages = ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
+    if args.profile_only:
+        # the command ncu captures: warm-up + steps forwards, direct launches, nothing else
+        for _ in range(max(args.warmup, 0) + args.steps):
+            layer.run("moe_forward", stream)
+        torch.cuda.synchronize()
+        status = layer.device_status()
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": workload_name(cfg),
+                              "forwards": max(args.warmup, 0) + args.steps, "device_status": status}),
+                  flush=True)
+        return 0 if status == 0 else 1
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
@@ -445,8 +483,7 @@ def run_gpu(args):
     K = args.steps
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
-    clk = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                       if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clk = ClockSampler(dev.index, clocks_path(args, rank))
     nvml = NvmlSampler(dev.index)
     if world > 1:
         dist.barrier()
@@ -498,8 +535,13 @@ def run_gpu(args):
     else:
         achieved = gemm["flops"] / (g_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"]}
+                "frac": achieved / pk["bf16_tflops"],
+                # the same kernel against the power-capped, seconds-long cuBLAS figure
+                "peak_sustained": pk["bf16_tflops_sustained"],
+                "frac_sustained": achieved / pk["bf16_tflops_sustained"]}
     wl_key = args.config + ("_noisy" if cfg.noisy else "")
+    if args.tokens is not None or args.d_ff is not None:
+        wl_key += f"_T{cfg.T}_F{cfg.F}"
     fused = cfg.dtype == "bf16"
     if cfg.weights == "int8":
         wl_key += "_int8"

@@ -271,8 +271,11 @@ moe_status_t moe_last_device_status(void* workspace, size_t workspace_bytes, voi
  * that loads the library, held until the process exits.  Limits: T * k <=
  * MOE_NOALLOC_MAX_SLOTS and E <= MOE_MAX_EXPERTS; larger problems return
  * MOE_ERR_INVALID_ARG and enqueue nothing.  The first call on a device looks up
- * the array's device address (once, with that device current); make that first
- * call before starting any stream capture.  All calls on a device share the array:
+ * the array's device address (with that device current) and keeps it; make that
+ * first call before starting any stream capture.  A lookup that fails returns
+ * MOE_ERR_CUDA, enqueues nothing and is tried again by the next call.  Every call
+ * clears the scan's arrival counter before its kernels run, and overwrites every
+ * other scratch word it reads.  All calls on a device share the array:
  * calls whose work overlaps on the GPU (e.g. on two streams) race; calls ordered on
  * one stream are safe.  Allocates nothing; all pointers are device pointers. */
 #define MOE_NOALLOC_MAX_SLOTS 131072

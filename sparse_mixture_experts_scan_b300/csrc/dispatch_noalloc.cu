@@ -42,12 +42,14 @@ constexpr size_t kScratchBytes = kOffAux + 256;  // about 1.03 MB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Per device: the device address of g_noalloc_scratch, looked up once with
-// that device current (the host-side symbol is not a device address).
+// Per device: the device address of g_noalloc_scratch, looked up with that
+// device current (the host-side symbol is not a device address).  Only a
+// successful lookup is kept: a lookup that failed (for example one attempted
+// during a stream capture, where loading the module is not allowed) is retried
+// by the next call.
 struct ScratchSlot {
-    std::once_flag once;
+    std::mutex mu;
     unsigned char* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
 };
 ScratchSlot g_slots[64];
 
@@ -58,12 +60,16 @@ cudaError_t scratch_for_current_device(unsigned char** out)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     ScratchSlot& s = g_slots[dev];
-    std::call_once(s.once, [&] {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (s.ptr == nullptr) {
         void* p = nullptr;
-        s.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();  // the failed lookup leaves no sticky error behind
+            return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+        }
         s.ptr = static_cast<unsigned char*>(p);
-    });
-    if (s.err != cudaSuccess) return s.err;
+    }
     *out = s.ptr;
     return cudaSuccess;
 }

@@ -3,13 +3,16 @@
 It serves callers that cannot allocate device memory while routing (an engine
 that owns all device memory, a path that cannot pay cudaMalloc's implicit
 synchronisation).  Its output must equal what the workspace-based entry points
-(moe_router + moe_dispatch) produce for the same router selection, on two
-calls in a row (the second call reuses the static scratch the first one left
-behind).  This file is collected last on purpose.
+(moe_router + moe_dispatch) produce for the same router selection, and the
+fp64 oracle's counts, capacity drops and permutation rows for the same expert
+indices, on two calls in a row (the second call reuses the static scratch the
+first one left behind).  This file is collected last on purpose.
 """
+import numpy as np
 import pytest
 import torch
 
+from oracle import moe_oracle as orc
 from sparse_mixture_experts_scan_b300 import MoELayer, _lib, config, make_inputs, make_params
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +35,9 @@ def _reference(cfg):
 ], ids=["switch_like", "deepseek_like", "skewed_like"])
 def test_noalloc_dispatch_matches_workspace_path_twice(cfg):
     ref = _reference(cfg)
+    # the oracle's token-order capacity on the same selection (bit-exact bar)
+    idx_cpu = ref["expert_idx"].cpu().numpy()
+    want = orc.dispatch(idx_cpu, cfg.E, orc.capacity(cfg.T, cfg.E, cfg.cf))
     params = make_params(cfg)
     stream = torch.cuda.current_stream().cuda_stream
     for _ in range(2):
@@ -46,6 +52,9 @@ def test_noalloc_dispatch_matches_workspace_path_twice(cfg):
         assert torch.equal(counts, ref["counts"])
         assert torch.equal(dropped, ref["dropped"])
         assert torch.equal(perm, ref["perm_row"])
+        np.testing.assert_array_equal(counts.cpu().numpy(), want.counts)
+        np.testing.assert_array_equal(dropped.cpu().numpy(), want.dropped)
+        np.testing.assert_array_equal(perm.cpu().numpy(), want.perm_row)
 
 
 def test_noalloc_dispatch_rejects_oversized_problems():
