@@ -681,3 +681,157 @@ void orc_quantize_int8(int rows, int cols, const void* w, int w_code, int8_t* q,
         }
     }
 }
+
+/* ======================================================================== */
+/* Expert parallelism over G ranks.  [Arch] §3.2 "分布式训练优化": experts are
+ * placed on different devices; in the mixed data + expert parallel mode the
+ * data is sharded over the workers, every worker holds a part of the experts,
+ * and tokens are sent between devices.  [Sparse] §4.2 "专家分片": 64 experts
+ * cut over 4 cards, 16 on each.  [Arch] §5 (问题3) names the exchange: an
+ * AllToAll.  [Intro] §4 (第四): every token may be sent to another device.
+ *
+ * Readings (the pages give no layout):
+ *   - rank r holds the tokens [floor(r T / G), floor((r+1) T / G)) and the
+ *     experts [r E/G, (r+1) E/G); E is a multiple of G;
+ *   - routing is per token, so a rank routes its own tokens exactly as the
+ *     whole layer would;
+ *   - capacity is the pages' rule applied to each shard on its own:
+ *     C_r = floor(T_r cf / E), positions counted in the shard's token order;
+ *   - every kept slot is sent to the rank that owns its expert; a rank's
+ *     receive buffer holds its experts in ascending order and, inside one
+ *     expert, the rows sent by rank 0, 1, ..., each in token order;
+ *   - the expert outputs return to the token's rank, which combines them;
+ *     shared experts are applied by each rank to its own tokens;
+ *   - the balance statistic is reduced over all ranks: f_e and P_e are sums
+ *     over every rank's tokens divided by T k and T. */
+
+/* The exchange.  idx [T,k]; C_rank [G] (-1 = no limit).  Writes
+ *   counts_rank [G,E]  slots of rank r's tokens that chose e (before drops)
+ *   dropped [T,k]      per-shard capacity drops
+ *   recv_row [T,k]     row of the slot in the concatenated receive buffers
+ *                      (rank 0's rows first), -1 if dropped
+ *   recv_rows [G]      rows each rank receives
+ *   recv_slot [...]    for each row of the concatenated receive buffers, the
+ *                      slot t*k + j it holds (sum of recv_rows entries). */
+void orc_ep_exchange(int T, int E, int k, int G, const int32_t* idx, const long long* C_rank,
+                     int32_t* counts_rank, uint8_t* dropped, int32_t* recv_row, int32_t* recv_rows,
+                     int32_t* recv_slot)
+{
+    long long* seen = (long long*)calloc((size_t)E, sizeof(long long));
+    const int E_loc = E / G;
+    for (int r = 0; r < G; ++r) {
+        const long t0 = (long)((long long)r * T / G), t1 = (long)((long long)(r + 1) * T / G);
+        for (int e = 0; e < E; ++e) {
+            seen[e] = 0;
+            counts_rank[(size_t)r * E + e] = 0;
+        }
+        for (long t = t0; t < t1; ++t) {
+            for (int j = 0; j < k; ++j) {
+                const size_t s = (size_t)t * k + j;
+                const int e = idx[s];
+                counts_rank[(size_t)r * E + e] += 1;
+                const long long p = seen[e]++;
+                dropped[s] = (uint8_t)(C_rank[r] >= 0 && p >= C_rank[r]);
+                recv_row[s] = -1;
+            }
+        }
+    }
+    long long row = 0;
+    for (int q = 0; q < G; ++q) {
+        long long n_q = 0;
+        for (int e = q * E_loc; e < (q + 1) * E_loc; ++e) {
+            for (int src = 0; src < G; ++src) {
+                const long t0 = (long)((long long)src * T / G), t1 = (long)((long long)(src + 1) * T / G);
+                for (long t = t0; t < t1; ++t) {
+                    for (int j = 0; j < k; ++j) {
+                        const size_t s = (size_t)t * k + j;
+                        if (idx[s] != e || dropped[s]) continue;
+                        recv_row[s] = (int32_t)row;
+                        recv_slot[row] = (int32_t)s;
+                        ++row;
+                        ++n_q;
+                    }
+                }
+            }
+        }
+        recv_rows[q] = (int32_t)n_q;
+    }
+    free(seen);
+}
+
+/* The owners' expert computation on a list of rows: out[r] = FFN_{expert[r]}(x[token[r]])
+ * ([Intro] §3.2 two-layer MLP; shared experts are experts E..E+S-1).  out is
+ * [n_rows, d]. */
+void orc_expert_apply(int d, int F, int act, const void* x, int x_code,
+                      const void* W1, const void* W3, const void* W2, int w_code,
+                      const void* b1, const void* b2, int b_code,
+                      int n_rows, const int32_t* token, const int32_t* expert, double* out)
+{
+    #pragma omp parallel
+    {
+        double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+        double* h = (double*)malloc(sizeof(double) * (size_t)F);
+        #pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < n_rows; ++r) {
+            for (int i = 0; i < d; ++i) xr[i] = rd(x, x_code, (size_t)token[r] * d + i);
+            expert_ffn(d, F, act, expert[r], W1, W3, W2, w_code, b1, b2, b_code, xr, h,
+                       out + (size_t)r * d);
+        }
+        free(xr);
+        free(h);
+    }
+}
+
+/* The combine at the token's own rank after the return exchange, for the
+ * tokens listed in `tokens` (y is [n_tok, d]):
+ *   y[t] = sum over kept slots j (slot order) of gates[t,j] * o[row_of[t,j]]
+ *        + sum over shared experts s of ys[s, t] + pass(t) x[t]
+ * with row_of[t,j] the slot's row in o (the concatenated receive buffers'
+ * outputs), ys [S, T, d] the shared experts' outputs (may be NULL when S = 0),
+ * and pass(t) as in orc_output_rows. */
+void orc_ep_combine(int T, int d, int k, int S, int residual_mode, const void* x, int x_code,
+                    const double* gates, const uint8_t* dropped, const int32_t* row_of, const double* o,
+                    const double* ys, int n_tok, const int32_t* tokens, double* y)
+{
+    for (long r = 0; r < n_tok; ++r) {
+        const long t = tokens[r];
+        double* yr = y + (size_t)r * d;
+        for (int i = 0; i < d; ++i) yr[i] = 0.0;
+        int n_dropped = 0;
+        for (int j = 0; j < k; ++j) {
+            const size_t s = (size_t)t * k + j;
+            if (dropped[s]) {
+                ++n_dropped;
+                continue;
+            }
+            const double* orow = o + (size_t)row_of[s] * d;
+            for (int i = 0; i < d; ++i) yr[i] += gates[s] * orow[i];
+        }
+        for (int sh = 0; sh < S; ++sh)
+            for (int i = 0; i < d; ++i) yr[i] += ys[((size_t)sh * T + t) * d + i];
+        if (residual_mode == 1 || (k >= 1 && n_dropped == k))
+            for (int i = 0; i < d; ++i) yr[i] += rd(x, x_code, (size_t)t * d + i);
+    }
+}
+
+/* The balance statistic reduced over the ranks (an all-reduce of each rank's
+ * counts and probability sums): E * sum_e f_e P_e with
+ * f_e = (sum_r counts_rank[r,e]) / (T k) and P_e = (sum_r sum_{t in shard r} p[t,e]) / T
+ * ([Intro] §3.4, [Switch] §"负载均衡损失函数"). */
+double orc_ep_aux(int T, int E, int k, int G, const int32_t* counts_rank, const double* probs)
+{
+    double aux = 0.0;
+    for (int e = 0; e < E; ++e) {
+        long long c = 0;
+        double P = 0.0;
+        for (int r = 0; r < G; ++r) {
+            c += counts_rank[(size_t)r * E + e];
+            const long t0 = (long)((long long)r * T / G), t1 = (long)((long long)(r + 1) * T / G);
+            double Pr = 0.0;
+            for (long t = t0; t < t1; ++t) Pr += probs[(size_t)t * E + e];
+            P += Pr;
+        }
+        aux += ((double)c / ((double)T * (double)k)) * (P / (double)T);
+    }
+    return (double)E * aux;
+}

@@ -89,6 +89,14 @@ def _lib():
         L.orc_quantize_int8.argtypes = [i32, i32, vp, i32, vp, vp]
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
+        L.orc_ep_exchange.restype = None
+        L.orc_ep_exchange.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_expert_apply.restype = None
+        L.orc_expert_apply.argtypes = [i32, i32, i32, vp, i32, vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp]
+        L.orc_ep_combine.restype = None
+        L.orc_ep_combine.argtypes = [i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp]
+        L.orc_ep_aux.restype = dbl
+        L.orc_ep_aux.argtypes = [i32, i32, i32, i32, vp, vp]
         _lib_handle = L
     return _lib_handle
 
@@ -394,3 +402,130 @@ def forward(x, Wg, bg, W1, W3, W2, b1, b2, *, E: int, S: int, k: int, act_name: 
     y = output_rows(x, W1, W3, W2, b1, b2, r.idx, r.gates, r.dropped, E=E, S=S,
                     act_name=act_name, residual_mode=residual_mode, tokens=tokens)
     return y, r
+
+
+# --------------------------------------------------------------------------
+# expert parallelism over G ranks (host-side emulation of the exchange)
+
+def shard_bounds(T: int, G: int) -> list:
+    """Token shard of each rank: rank r holds [b[r], b[r+1]), b[r] = floor(r T / G)."""
+    return [r * T // G for r in range(G + 1)]
+
+
+@dataclass
+class EPExchange:
+    counts_rank: np.ndarray  # [G, E] int32, each rank's slots per expert before drops
+    dropped: np.ndarray      # [T, k] uint8, per-shard capacity drops
+    recv_row: np.ndarray     # [T, k] int32, row in the concatenated receive buffers or -1
+    recv_rows: np.ndarray    # [G] int32, rows each rank receives
+    recv_slot: np.ndarray    # [sum recv_rows] int32, slot t*k+j held by each received row
+
+
+def ep_exchange(idx, E: int, G: int, C_rank) -> EPExchange:
+    ia = _i32(idx)
+    T, k = ia.shape
+    if G < 1 or E % G != 0:
+        raise ValueError("need E to be a multiple of G")
+    cr = np.ascontiguousarray(np.asarray(C_rank, dtype=np.int64))
+    if cr.shape != (G,):
+        raise ValueError("one capacity per rank")
+    counts_rank = np.empty((G, E), dtype=np.int32)
+    dropped = np.empty((T, k), dtype=np.uint8)
+    recv_row = np.empty((T, k), dtype=np.int32)
+    recv_rows = np.empty(G, dtype=np.int32)
+    recv_slot = np.full(max(T * k, 1), -1, dtype=np.int32)
+    _lib().orc_ep_exchange(T, E, k, G, _ptr(ia), _ptr(cr), _ptr(counts_rank), _ptr(dropped),
+                           _ptr(recv_row), _ptr(recv_rows), _ptr(recv_slot))
+    return EPExchange(counts_rank, dropped, recv_row, recv_rows, recv_slot[: int(recv_rows.sum())])
+
+
+def expert_apply(x, W1, W3, W2, b1, b2, tokens, experts, *, act_name: str) -> np.ndarray:
+    """out[r] = FFN_{experts[r]}(x[tokens[r]]) in fp64."""
+    xa, xc = _as_array(x)
+    w1, wc = _as_array(W1)
+    w3, _ = _as_array(W3)
+    w2, _ = _as_array(W2)
+    ba1, bc = _as_array(b1)
+    ba2, bc2 = _as_array(b2)
+    if b1 is None:
+        bc = bc2
+    d = xa.shape[1]
+    F = w1.shape[1]
+    tok = _i32(tokens)
+    exp = _i32(experts)
+    out = np.empty((tok.shape[0], d), dtype=np.float64)
+    if tok.shape[0]:
+        _lib().orc_expert_apply(d, F, ACTS[act_name], _ptr(xa), xc, _ptr(w1), _ptr(w3), _ptr(w2), wc,
+                                _ptr(ba1), _ptr(ba2), bc, tok.shape[0], _ptr(tok), _ptr(exp), _ptr(out))
+    return out
+
+
+def ep_aux(counts_rank, probs, k: int) -> float:
+    ca = _i32(counts_rank)
+    pa = np.ascontiguousarray(np.asarray(probs, dtype=np.float64))
+    T, E = pa.shape
+    return float(_lib().orc_ep_aux(T, E, k, ca.shape[0], _ptr(ca), _ptr(pa)))
+
+
+@dataclass
+class EPResult:
+    logits: np.ndarray
+    probs: np.ndarray
+    idx: np.ndarray
+    gates: np.ndarray
+    counts: np.ndarray       # [E] all ranks' slots per expert before drops
+    ex: EPExchange
+    C_rank: list
+    aux: float
+    y: np.ndarray | None     # rows of the listed tokens
+
+
+def ep_forward(x, Wg, bg, W1, W3, W2, b1, b2, *, E: int, S: int, k: int, G: int, act_name: str,
+               renormalize: bool, cf, residual_mode: int = 0, tokens=None, noise=None,
+               logits=None) -> EPResult:
+    """The layer computed rank by rank over G ranks, in fp64.
+
+    Each rank routes its token shard (the router is per token, so ``logits`` --
+    e.g. the device's -- may be given for all T tokens at once), applies the
+    capacity rule to its shard alone, sends its kept slots to the experts'
+    owners, the owners run their experts on the rows they received, the
+    outputs return, and each rank combines its tokens.  ``tokens`` limits the
+    expert work and y to the listed tokens (None: all)."""
+    xa, _ = _as_array(x)
+    T = xa.shape[0]
+    if logits is None:
+        la = router_logits(x, Wg, bg)
+        if noise is not None:
+            Wn, bn, eps, min_std = noise
+            la = noisy_logits(la, router_logits(x, Wn, bn), eps, min_std)
+    else:
+        la = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
+    probs = softmax(la)
+    idx = topk(la, k)
+    g = gates(probs, idx, renormalize)
+    b = shard_bounds(T, G)
+    C_rank = [capacity(b[r + 1] - b[r], E, cf) for r in range(G)]
+    ex = ep_exchange(idx, E, G, C_rank)
+    tok = np.arange(T, dtype=np.int32) if tokens is None else _i32(tokens)
+    # the owners compute the received rows that the listed tokens need
+    rows_needed = ex.recv_row[tok].reshape(-1)
+    rows_needed = np.unique(rows_needed[rows_needed >= 0])
+    o = np.zeros((max(int(ex.recv_rows.sum()), 1), xa.shape[1]), dtype=np.float64)
+    if rows_needed.size:
+        slot = ex.recv_slot[rows_needed]
+        o[rows_needed] = expert_apply(x, W1, W3, W2, b1, b2, slot // k, idx.reshape(-1)[slot],
+                                      act_name=act_name)
+    ys = None
+    if S > 0:  # each rank applies the shared experts to its own tokens
+        ys = np.zeros((S, T, xa.shape[1]), dtype=np.float64)
+        for sh in range(S):
+            ys[sh, tok] = expert_apply(x, W1, W3, W2, b1, b2, tok, np.full(tok.shape, E + sh),
+                                       act_name=act_name)
+    xa2, xc = _as_array(x)
+    y = np.empty((tok.shape[0], xa.shape[1]), dtype=np.float64)
+    ga = np.ascontiguousarray(g, dtype=np.float64)
+    _lib().orc_ep_combine(T, xa.shape[1], k, S, int(residual_mode), _ptr(xa2), xc, _ptr(ga),
+                          _ptr(ex.dropped), _ptr(ex.recv_row), _ptr(o),
+                          _ptr(ys) if ys is not None else None, tok.shape[0], _ptr(tok), _ptr(y))
+    counts = ex.counts_rank.sum(axis=0).astype(np.int32)
+    return EPResult(la, probs, idx, g, counts, ex, C_rank, ep_aux(ex.counts_rank, probs, k), y)
