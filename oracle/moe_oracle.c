@@ -835,3 +835,45 @@ double orc_ep_aux(int T, int E, int k, int G, const int32_t* counts_rank, const 
     }
     return (double)E * aux;
 }
+
+/* ======================================================================== */
+/* Expert weight quantisation to 4 bits.  [Sparse] §"量化与PagedAttention结合":
+ * the expert weights may be quantised on their own (for example to INT4, with
+ * AWQ) while the router keeps 16-bit precision.  The pages give no scheme.
+ * AWQ stores 4-bit weights in groups of consecutive input elements, each
+ * group with its own scale; its activation-aware choice of the scales needs
+ * calibration data, which this layer does not have, so the reading here is
+ * the plain group-wise rounding that remains:
+ *     scale[r, g] = max over the group's elements |w[r, c]| / 7,
+ *     q[r, c] = round(w[r, c] / scale[r, g]) clamped to [-7, 7]
+ * for groups of `group` consecutive columns c (round half to even; an
+ * all-zero group gets scale 0 and q 0); the dequantised weight is
+ * q * scale.  As for int8, the integer is decided in IEEE fp32 (the
+ * library's precision).  Two values share one byte: column 2i in the low
+ * nibble, 2i + 1 in the high nibble, each as a 4-bit two's complement. */
+void orc_quantize_int4(int rows, int cols, int group, const void* w, int w_code, uint8_t* packed, float* scale)
+{
+    const int n_groups = cols / group;
+    for (long r = 0; r < rows; ++r) {
+        for (int g = 0; g < n_groups; ++g) {
+            float amax = 0.0f;
+            for (int c = g * group; c < (g + 1) * group; ++c) {
+                const float v = (float)rd(w, w_code, (size_t)r * cols + c);
+                const float a = v < 0.0f ? -v : v;
+                if (a > amax) amax = a;
+            }
+            const float s = amax / 7.0f;
+            scale[(size_t)r * n_groups + g] = s;
+            for (int c = g * group; c < (g + 1) * group; ++c) {
+                const float v = (float)rd(w, w_code, (size_t)r * cols + c);
+                float t = s > 0.0f ? rintf(v / s) : 0.0f;
+                if (t > 7.0f) t = 7.0f;
+                if (t < -7.0f) t = -7.0f;
+                const uint8_t nib = (uint8_t)((int)t & 0xF);
+                uint8_t* b = packed + (size_t)r * (cols / 2) + c / 2;
+                if (c % 2 == 0) *b = (uint8_t)((*b & 0xF0u) | nib);
+                else *b = (uint8_t)((*b & 0x0Fu) | (uint8_t)(nib << 4));
+            }
+        }
+    }
+}

@@ -89,6 +89,8 @@ def _lib():
         L.orc_quantize_int8.argtypes = [i32, i32, vp, i32, vp, vp]
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
+        L.orc_quantize_int4.restype = None
+        L.orc_quantize_int4.argtypes = [i32, i32, i32, vp, i32, vp, vp]
         L.orc_ep_exchange.restype = None
         L.orc_ep_exchange.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.orc_expert_apply.restype = None
@@ -342,6 +344,38 @@ def quantize_int8(w):
 def dequantize_int8(q, scale):
     """q * scale per row, exactly, in fp64."""
     return np.asarray(q, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+INT4_GROUP = 128  # columns per scale group of the 4-bit weights
+
+
+def quantize_int4(w, group: int = INT4_GROUP):
+    """Group-wise symmetric 4-bit quantisation of a 2-D array: (packed uint8 [rows, cols/2],
+    scale fp32 [rows, cols/group]); column 2i in the low nibble, 2i+1 in the high one."""
+    wa, wc = _as_array(w)
+    rows, cols = wa.shape
+    if cols % group or group % 2:
+        raise ValueError("cols must be a multiple of an even group size")
+    packed = np.zeros((rows, cols // 2), dtype=np.uint8)
+    sc = np.empty((rows, cols // group), dtype=np.float32)
+    _lib().orc_quantize_int4(rows, cols, group, _ptr(wa), wc, _ptr(packed), _ptr(sc))
+    return packed, sc
+
+
+def unpack_int4(packed) -> np.ndarray:
+    """The signed 4-bit values of a packed array (marshalling: two nibbles per byte)."""
+    p = np.asarray(packed, dtype=np.uint8)
+    lo = (p & 0xF).astype(np.int8)
+    hi = (p >> 4).astype(np.int8)
+    q = np.stack([lo, hi], axis=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
+    return np.where(q > 7, q - 16, q).astype(np.int8)
+
+
+def dequantize_int4(packed, scale, group: int = INT4_GROUP):
+    """q * scale of every element, exactly, in fp64."""
+    q = unpack_int4(packed).astype(np.float64)
+    s = np.repeat(np.asarray(scale, dtype=np.float64), group, axis=-1)
+    return q * s
 
 
 def num_threads() -> int:

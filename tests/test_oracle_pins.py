@@ -564,3 +564,43 @@ def test_quantize_int8_error_bound_and_range():
     assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-5)).all()
     # scale is max|w| / 127 in fp32
     np.testing.assert_array_equal(s, (np.abs(w).max(axis=1) / np.float32(127.0)).astype(np.float32))
+
+
+# ---------------------------------------------------------------- 4-bit expert weights
+
+def test_quantize_int4_closed_form_and_packing():
+    # group 0 (8 columns, group size 8 here) has amax 7: scale 1, q = round-half-even(w);
+    # group 1 is all zero (scale 0, q 0); in row 1, group 0 is tiny and group 1 large, so the
+    # two groups get independent scales (a per-row scale would round group 0 to zero)
+    w = np.array([[7.0, -2.5, 2.5, -3.5, 0.5, 1.5, -0.49, 6.5, 0, 0, 0, 0, 0, 0, 0, 0],
+                  [0.07, -0.035, 0.0, 0.01, 0, 0, 0, 0, 70.0, -35.0, 10.0, 5.0, 0, 0, 0, -70.0]],
+                 dtype=np.float32)
+    packed, s = orc.quantize_int4(w, group=8)
+    assert packed.shape == (2, 8) and s.shape == (2, 2)
+    assert s[0, 0] == 1.0 and s[0, 1] == 0.0
+    assert s[1, 0] == np.float32(np.float32(0.07) / np.float32(7.0)) and s[1, 1] == 10.0
+    q = orc.unpack_int4(packed)
+    assert q[0].tolist() == [7, -2, 2, -4, 0, 2, 0, 6] + [0] * 8
+    assert q[1].tolist() == [7, -4, 0, 1, 0, 0, 0, 0, 7, -4, 1, 0, 0, 0, 0, -7]
+    # nibble order and two's complement by hand: (7, -2) -> 0x7 | 0xE << 4 = 0xE7; (2, -4) -> 0xC2
+    assert packed[0, 0] == 0xE7 and packed[0, 1] == 0xC2 and packed[0, 3] == 0x60
+    np.testing.assert_array_equal(orc.dequantize_int4(packed, s, group=8)[1, 8:],
+                                  [70.0, -40.0, 10.0, 0.0, 0.0, 0.0, 0.0, -70.0])
+
+
+def test_quantize_int4_error_bound_and_range():
+    rng = np.random.default_rng(22)
+    w = (rng.standard_normal((19, 512)) * rng.uniform(0.01, 3.0, size=(19, 1))).astype(np.float32)
+    w[3, 128:256] = 0.0  # one all-zero group
+    packed, s = orc.quantize_int4(w)
+    assert s.shape == (19, 4)
+    q = orc.unpack_int4(packed).astype(int)
+    assert np.abs(q).max() == 7
+    per_group = np.abs(q).reshape(19, 4, 128).max(axis=2)
+    assert per_group[3, 1] == 0 and s[3, 1] == 0.0
+    assert (np.delete(per_group.reshape(-1), 3 * 4 + 1) == 7).all()  # every other group reaches +-7
+    deq = orc.dequantize_int4(packed, s)
+    err = np.abs(w.astype(np.float64) - deq)
+    assert (err <= np.repeat(s, 128, axis=1).astype(np.float64) * (0.5 + 1e-5)).all()
+    np.testing.assert_array_equal(
+        s, (np.abs(w).reshape(19, 4, 128).max(axis=2) / np.float32(7.0)).astype(np.float32))
