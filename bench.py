@@ -61,6 +61,10 @@ def parse_args():
                     help="noisy top-k gating (training-mode router; noise floor 0.01)")
     ap.add_argument("--int8", action="store_true",
                     help="int8 expert weights with per-row scales (quantised by the library)")
+    ap.add_argument("--int4", action="store_true",
+                    help="4-bit expert weights with scales per group of 128 inputs (quantised by the library)")
+    ap.add_argument("--ep", type=int, default=None,
+                    help="run the layer expert-parallel over this many ranks emulated on the GPU")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step instead: moe_forward + moe_backward")
     ap.add_argument("--no-graph", action="store_true",
@@ -72,7 +76,8 @@ def workload_name(cfg) -> str:
     cap = "none" if cfg.cf is None else f"{cfg.cf:g}"
     shared = f"+{cfg.S}shared" if cfg.S else ""
     noisy = f", noisy top-k gating (noise floor {cfg.noise_min_std:g})" if cfg.noisy else ""
-    wq = " with int8 weights (per-row scales)" if cfg.weights == "int8" else ""
+    wq = {"int8": " with int8 weights (per-row scales)",
+          "int4": " with 4-bit weights (scales per group of 128 inputs)"}.get(cfg.weights, "")
     return (f"{cfg.name} MoE FFN layer: T={cfg.T} d_model={cfg.d} E={cfg.E}{shared} k={cfg.k} "
             f"d_ff={cfg.F} {cfg.act} capacity_factor={cap} {cfg.dtype} experts{wq}, fp32 router{noisy}")
 
@@ -84,6 +89,8 @@ def bench_config(args):
         kw.update(noisy=True, noise_min_std=0.01)
     if args.int8:
         kw.update(weights="int8")
+    if args.int4:
+        kw.update(weights="int4")
     if args.tokens is not None:
         kw.update(T=args.tokens)
     if args.d_ff is not None:
@@ -351,6 +358,8 @@ def algorithmic_gemm_work(cfg, out):
     nmat = 3 if cfg.act == "swiglu" else 2
     if cfg.weights == "int8":  # 1-byte weights and one fp32 scale per output row
         w_bytes = touched * (nmat * cfg.d * cfg.F + 4 * ((nmat - 1) * cfg.F + cfg.d))
+    elif cfg.weights == "int4":  # half-byte weights and one fp32 scale per 128 inputs
+        w_bytes = touched * (nmat * cfg.d * cfg.F // 2 + 4 * nmat * cfg.d * cfg.F // 128)
     else:
         w_bytes = touched * nmat * cfg.d * cfg.F * esz
     srows = cfg.S * cfg.T
@@ -406,12 +415,13 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = bench_config(args)
     inp = make_inputs(cfg, seed=rank, device=dev)
-    if cfg.weights == "int8":
+    if cfg.weights in ("int8", "int4"):
         from sparse_mixture_experts_scan_b300 import quantize_expert_weights
-        inp = quantize_expert_weights(inp)
-    layer = MoELayer(cfg, inp, device=dev)
+        inp = quantize_expert_weights(inp, bits=8 if cfg.weights == "int8" else 4)
+    layer = MoELayer(cfg, inp, device=dev, ep_ranks=args.ep)
     stream = torch.cuda.current_stream(dev)
-    stages = ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
+    # an expert-parallel layer runs only the whole forward: its stage pass is that one call
+    stages = ["moe_forward"] if args.ep else ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
     if args.profile_only:
         # the command ncu captures: warm-up + steps forwards, direct launches, nothing else
         for _ in range(max(args.warmup, 0) + args.steps):
@@ -521,7 +531,7 @@ def run_gpu(args):
     gemm = algorithmic_gemm_work(cfg, out)
     sbytes = stage_bytes(cfg, out, gemm)
     pk = peaks()
-    g_ms = stage_ms["moe_grouped_gemm"]
+    g_ms = stage_ms.get("moe_grouped_gemm", ms_step)
     hbm_bound = gemm["bytes"] == 0 or \
         gemm["flops"] / gemm["bytes"] < pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if gemm["bytes"] == 0 or g_ms <= 0:
@@ -543,10 +553,21 @@ def run_gpu(args):
     if args.tokens is not None or args.d_ff is not None:
         wl_key += f"_T{cfg.T}_F{cfg.F}"
     fused = cfg.dtype == "bf16"
-    if cfg.weights == "int8":
-        wl_key += "_int8"
-        tr = traffic_from_profiles("grouped_gemm_q8.cu", wl_key)
-        kname = "moe_grouped_gemm stage: two k_grouped_gemm_q8 launches (int8 weights, tcgen05)"
+    if args.ep:
+        wl_key += f"_ep{args.ep}"
+        tr = None
+        kname = (f"the whole expert-parallel forward over {args.ep} emulated ranks (moe_forward_ep; the "
+                 "owners' expert kernels dominate)")
+    elif cfg.weights in ("int8", "int4"):
+        wl_key += "_" + cfg.weights
+        max_rows = min(cfg.T, int(cfg.T * cfg.cf / cfg.E)) if cfg.cf else cfg.T
+        if cfg.weights == "int4" or max_rows <= 128:
+            tr = traffic_from_profiles("grouped_gemm_wq.cu", wl_key)
+            kname = (f"moe_grouped_gemm stage: two k_grouped_gemm_wq launches ({cfg.weights} weights converted "
+                     "into tensor memory, tcgen05 with A from TMEM)")
+        else:
+            tr = traffic_from_profiles("grouped_gemm_q8.cu", wl_key)
+            kname = "moe_grouped_gemm stage: two k_grouped_gemm_q8 launches (int8 weights, tcgen05)"
     else:
         tr = traffic_from_profiles("ffn_fused_tc.cu" if fused else "grouped_gemm_ffma.cu", wl_key)
         kname = ("moe_grouped_gemm stage: k_ffn_fused_tc (both expert layers, one persistent tcgen05 launch)"
@@ -560,12 +581,15 @@ def run_gpu(args):
                  "tensor_frac": gemm["flops"] / max(g_ms * 1e-3, 1e-12) / 1e12 / pk["bf16_tflops"],
                  "hbm_gbs": gemm["bytes"] / max(g_ms * 1e-3, 1e-12) / 1e9,
                  "hbm_frac": gemm["bytes"] / max(g_ms * 1e-3, 1e-12) / 1e9 / pk["hbm_gbs"]})
-    mem_stages = {}
-    for s in ("moe_router", "moe_dispatch", "moe_combine"):
-        gbs = sbytes[s] / (stage_ms[s] * 1e-3) / 1e9
-        mem_stages[s] = {"ms": stage_ms[s], "bytes": sbytes[s], "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]}
-    rdc_bytes = sum(sbytes.values())
-    rdc_ms = sum(stage_ms[s] for s in ("moe_router", "moe_dispatch", "moe_combine"))
+    mem_stages, rdc = {}, None
+    if not args.ep:
+        for s in ("moe_router", "moe_dispatch", "moe_combine"):
+            gbs = sbytes[s] / (stage_ms[s] * 1e-3) / 1e9
+            mem_stages[s] = {"ms": stage_ms[s], "bytes": sbytes[s], "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]}
+        rdc_bytes = sum(sbytes.values())
+        rdc_ms = sum(stage_ms[s] for s in ("moe_router", "moe_dispatch", "moe_combine"))
+        rdc = {"bytes": rdc_bytes, "ms": rdc_ms, "GB/s": rdc_bytes / (rdc_ms * 1e-3) / 1e9,
+               "frac": rdc_bytes / (rdc_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
 
     # ---- end to end through the public API with host buffers: every step copies its x
     # from pinned host memory to the device, runs the layer, and copies y and aux back.
@@ -574,7 +598,7 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
-        layers = [layer, MoELayer(cfg, dict(inp), device=dev)]
+        layers = [layer, MoELayer(cfg, dict(inp), device=dev, ep_ranks=args.ep)]
         x_dev = [inp["x"].clone() for _ in layers]  # valid data before the first forward
         for L, xd in zip(layers, x_dev):
             L.set_x(xd)
@@ -646,13 +670,17 @@ def run_gpu(args):
     cpu_base = None
     if not args.no_cpu_baseline:
         cpu_inp = {k: (None if v is None else v.cpu()) for k, v in inp.items()}
-        if cfg.weights == "int8":  # the oracle runs on the exactly dequantised weights
+        if cfg.weights in ("int8", "int4"):  # the oracle runs on the exactly dequantised weights
             from oracle import moe_oracle as orc
             for k_ in ("W1", "W3", "W2"):
                 q_ = cpu_inp.get(k_)
-                if q_ is not None:
+                if q_ is None:
+                    continue
+                if cfg.weights == "int8":
                     cpu_inp[k_] = orc.dequantize_int8(q_.numpy().reshape(-1, q_.shape[-1]),
                                                       cpu_inp[k_ + "_scale"].numpy().reshape(-1)).reshape(q_.shape)
+                else:
+                    cpu_inp[k_] = orc.dequantize_int4(q_.numpy(), cpu_inp[k_ + "_scale"].numpy())
         # about 10 G multiply-adds of expert work: ~10-30 s on the host cores
         per_tok = cfg.d * cfg.F * (3 if cfg.act == "swiglu" else 2) * (cfg.k + cfg.S)
         secs, desc, threads = oracle_step(cfg, cpu_inp, int(max(16, min(cfg.T, 1e10 / per_tok))))
@@ -666,7 +694,8 @@ def run_gpu(args):
         "data": "synthetic (seeded; shapes and distributions of the workload; random-init weights)",
         "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": (f"replicas x{world}" if world > 1 else "single GPU")
+                   + (f"; expert parallel over {args.ep} ranks emulated on each GPU" if args.ep else ""),
                    "launch": ("direct C-ABI calls" if args.no_graph else
                               "one CUDA graph of moe_forward per step (kernels chained by programmatic "
                               "dependent launch)"),
@@ -675,9 +704,7 @@ def run_gpu(args):
                                    "times add up to slightly more than ms_per_step)",
                    "stage_ms": stage_ms,
                    "memory_stages": mem_stages,
-                   "router_dispatch_combine": {"bytes": rdc_bytes, "ms": rdc_ms,
-                                               "GB/s": rdc_bytes / (rdc_ms * 1e-3) / 1e9,
-                                               "frac": rdc_bytes / (rdc_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+                   "router_dispatch_combine": rdc,
                    "wall_s_timed_region": t_wall},
         "roofline": roof,
         "cpu_baseline": cpu_base,

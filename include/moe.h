@@ -108,8 +108,22 @@ typedef struct {
  * MOE_ERR_UNSUPPORTED.  The router weights stay fp32. */
 typedef enum {
     MOE_WEIGHTS_DTYPE = 0, /* expert weights in the layer dtype */
-    MOE_WEIGHTS_INT8 = 1   /* int8 expert weights + fp32 per-row scales */
+    MOE_WEIGHTS_INT8 = 1,  /* int8 expert weights + fp32 per-row scales */
+    MOE_WEIGHTS_INT4 = 2   /* 4-bit expert weights + fp32 scales per group of MOE_INT4_GROUP inputs */
 } moe_weight_format_t;
+
+/* MOE_WEIGHTS_INT4 ([Sparse] §"量化与PagedAttention结合": the experts alone
+ * quantised to INT4 with AWQ, whose storage is group-wise): W[e, n, c] =
+ * q[e, n, c] * scale[e, n, c / MOE_INT4_GROUP] with q in [-7, 7]; two values per
+ * byte, column 2i in the low nibble and 2i + 1 in the high nibble (4-bit two's
+ * complement), so W1 and W3 are [E, F, d / 2] bytes and W2 is [E, d, F / 2];
+ * W1_scale and W3_scale are [E, F, d / MOE_INT4_GROUP] fp32, W2_scale
+ * [E, d, F / MOE_INT4_GROUP] (moe_quantize_int4 makes them).  Needs dtype ==
+ * MOE_BF16, n_shared == 0, no MOE_FLAG_TRAINING or MOE_FLAG_FFMA_EXPERTS, and
+ * d_model and d_ff multiples of MOE_INT4_GROUP; otherwise MOE_ERR_UNSUPPORTED.
+ * The tensor core multiplies bf16 activations by the weights dequantised to bf16
+ * (q * scale in fp32, rounded once). */
+#define MOE_INT4_GROUP 128
 
 /* Noisy top-k gating ([Arch] §2.1 noisy_top_k_gating; [Switch] §"代码实战"
  * NoisyTop1Gate).  With noisy_gating = 1 the router also computes
@@ -135,9 +149,10 @@ typedef struct {
     const float* W_noise;   /* [E, d] fp32 noise projection; required iff noisy_gating */
     const float* b_noise;   /* [E] fp32 noise projection bias, or NULL */
     const float* noise_eps; /* [T, E] fp32 standard normal draws; required iff noisy_gating */
-    const float* W1_scale;  /* [E, F] fp32; required iff weight_format == INT8, else NULL */
-    const float* W3_scale;  /* [E, F] fp32; iff INT8 and SwiGLU */
-    const float* W2_scale;  /* [E, d] fp32; iff INT8 */
+    const float* W1_scale;  /* INT8: [E, F]; INT4: [E, F, d / MOE_INT4_GROUP]; fp32; required iff
+                               weight_format != MOE_WEIGHTS_DTYPE, else NULL */
+    const float* W3_scale;  /* the same shape; iff quantised and SwiGLU */
+    const float* W2_scale;  /* INT8: [E, d]; INT4: [E, d, F / MOE_INT4_GROUP]; iff quantised */
 } moe_inputs_t;
 
 typedef struct {
@@ -246,6 +261,45 @@ moe_status_t moe_backward(const moe_params_t* params, const moe_inputs_t* inputs
                           const moe_grads_t* grads, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Expert parallelism over G ranks, emulated on this GPU ([Arch] §3.2
+ * "分布式训练优化": experts placed on different devices, and the mixed data +
+ * expert parallel mode in which the data is sharded over the workers, each
+ * worker holds a part of the experts and tokens cross devices; [Arch] §5
+ * (问题3): the exchange is an AllToAll; [Sparse] §4.2 "专家分片": 64 experts
+ * cut over 4 cards).
+ *
+ * Rank r holds the tokens [floor(r T / G), floor((r+1) T / G)) and the experts
+ * [r E/G, (r+1) E/G) (E must be a multiple of G).  Every rank routes its own
+ * tokens, applies the capacity rule to its shard alone
+ * (C_r = floor(T_r * cf / E), positions in the shard's token order), and sends
+ * every kept slot's token row to the owner of its expert; each owner runs its
+ * experts on the rows it received (its receive buffer holds its experts in
+ * ascending order and, inside one expert, the rows of rank 0, 1, ... in token
+ * order); the outputs travel back and every rank combines its own tokens
+ * (shared experts: each rank on its own tokens).  Each rank has a private
+ * region of the workspace; the only data that crosses ranks is moved by the
+ * library's exchange kernels (a counts exchange, the token all-to-all and its
+ * reverse), all on `stream`.
+ *
+ * The outputs are those of moe_forward, for the whole batch, with these
+ * meanings: counts = every rank's slots per expert before drops (summed over
+ * ranks); dropped = the per-shard capacity drops; aux = the balance statistic
+ * reduced over all ranks (f and P over all T tokens); perm_row = the slot's row
+ * in the concatenation of all ranks' receive buffers (rank 0's first,
+ * unpadded), -1 if dropped.  Without a capacity limit the result is the single
+ * rank layer's, and perm_row equals moe_forward's.
+ *
+ * Supported: the bf16 tensor-core experts (fused kernel) and the FFMA experts
+ * (fp32, or MOE_FLAG_FFMA_EXPERTS); quantised weights, MOE_FLAG_UNFUSED_EXPERTS and
+ * MOE_FLAG_TRAINING return MOE_ERR_UNSUPPORTED.  G outside 1..MOE_EP_MAX_RANKS
+ * or E not a multiple of G returns MOE_ERR_INVALID_ARG.  The workspace
+ * (moe_ep_workspace_size) must be zeroed once before its first use; bounded
+ * device waits of every rank report to its first word (moe_last_device_status). */
+#define MOE_EP_MAX_RANKS 16
+moe_status_t moe_ep_workspace_size(const moe_params_t* params, int32_t G, size_t* bytes);
+moe_status_t moe_forward_ep(const moe_params_t* params, int32_t G, const moe_inputs_t* inputs,
+                            moe_outputs_t* outputs, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, reads and clears the workspace's device error word.
  * Returns MOE_ERR_DEVICE_TIMEOUT if a bounded device wait expired since the last
  * call, MOE_ERR_CUDA if the synchronisation failed, else MOE_OK.  For tests and
@@ -296,6 +350,17 @@ uint64_t moe_kernel_launches(void);
  * scale 0 and q 0.  For a layer's W1, W3 ([E, F, d]) call it with rows = E*F,
  * cols = d; for W2 ([E, d, F]) with rows = E*d, cols = F.  Enqueues one kernel. */
 moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q,
+                               float* scale, void* stream);
+
+/* Quantise `rows` rows of `cols` weights (device, `dtype` MOE_BF16 or MOE_F32,
+ * row-major; cols a multiple of MOE_INT4_GROUP) to 4 bits with one scale per
+ * group of MOE_INT4_GROUP consecutive columns: scale = max |w| / 7 over the group
+ * (IEEE fp32), q = round-half-even(w / scale) clamped to [-7, 7]; an all-zero
+ * group gets scale 0 and q 0.  Writes q packed two per byte ([rows, cols / 2],
+ * column 2i in the low nibble) and scale [rows, cols / MOE_INT4_GROUP].  For a
+ * layer's W1, W3 ([E, F, d]) call it with rows = E*F, cols = d; for W2
+ * ([E, d, F]) with rows = E*d, cols = F.  Enqueues one kernel. */
+moe_status_t moe_quantize_int4(const void* w, int32_t dtype, int64_t rows, int32_t cols, uint8_t* q,
                                float* scale, void* stream);
 
 /* Diagnostic: enqueues one kernel whose bounded wait (on a barrier that nothing

@@ -27,10 +27,12 @@ MOE_FLAG_FFMA_EXPERTS = 1
 MOE_FLAG_FFMA_ROUTER = 2
 MOE_FLAG_UNFUSED_EXPERTS = 4
 MOE_FLAG_TRAINING = 8
-MOE_WEIGHTS_DTYPE, MOE_WEIGHTS_INT8 = 0, 1
+MOE_WEIGHTS_DTYPE, MOE_WEIGHTS_INT8, MOE_WEIGHTS_INT4 = 0, 1, 2
+MOE_INT4_GROUP = 128
 MOE_MAX_EXPERTS = 512
 MOE_MAX_TOPK = 32
 MOE_NOALLOC_MAX_SLOTS = 131072
+MOE_EP_MAX_RANKS = 16
 
 
 class moe_params_t(ctypes.Structure):
@@ -93,10 +95,17 @@ def load(build_if_stale: bool = True):
     L.moe_dispatch_positions_noalloc.argtypes = [_P(moe_params_t), _vp, _vp, _vp, _vp, _vp]
     L.moe_quantize_int8.restype = _i32
     L.moe_quantize_int8.argtypes = [_vp, _i32, ctypes.c_int64, _i32, _vp, _vp, _vp]
+    L.moe_quantize_int4.restype = _i32
+    L.moe_quantize_int4.argtypes = [_vp, _i32, ctypes.c_int64, _i32, _vp, _vp, _vp]
     L.moe_check_bounded_wait.restype = _i32
     L.moe_check_bounded_wait.argtypes = [_vp, ctypes.c_size_t, _u32, _vp]
     L.moe_kernel_launches.restype = ctypes.c_uint64
     L.moe_kernel_launches.argtypes = []
+    L.moe_ep_workspace_size.restype = _i32
+    L.moe_ep_workspace_size.argtypes = [_P(moe_params_t), _i32, _P(ctypes.c_size_t)]
+    L.moe_forward_ep.restype = _i32
+    L.moe_forward_ep.argtypes = [_P(moe_params_t), _i32, _P(moe_inputs_t), _P(moe_outputs_t), _vp,
+                                 ctypes.c_size_t, _vp]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_status_string.argtypes = [_i32]
     _handle = L
@@ -151,6 +160,17 @@ def moe_backward(params, inputs, outputs, dy, d_aux, grads, workspace, workspace
                                ctypes.c_size_t(workspace_bytes), _vp(stream))
 
 
+def moe_ep_workspace_size(params: moe_params_t, G: int):
+    n = ctypes.c_size_t(0)
+    st = load().moe_ep_workspace_size(ctypes.byref(params), _i32(G), ctypes.byref(n))
+    return st, n.value
+
+
+def moe_forward_ep(params, G, inputs, outputs, workspace, workspace_bytes, stream):
+    return load().moe_forward_ep(ctypes.byref(params), _i32(G), ctypes.byref(inputs), ctypes.byref(outputs),
+                                 _vp(workspace), ctypes.c_size_t(workspace_bytes), _vp(stream))
+
+
 def moe_dispatch_positions_noalloc(params, expert_idx, counts, dropped, perm_row, stream):
     return load().moe_dispatch_positions_noalloc(ctypes.byref(params), _vp(expert_idx), _vp(counts),
                                                  _vp(dropped), _vp(perm_row), _vp(stream))
@@ -162,6 +182,11 @@ def moe_last_device_status(workspace, workspace_bytes, stream):
 
 def moe_quantize_int8(w, dtype, rows, cols, q, scale, stream):
     return load().moe_quantize_int8(_vp(w), _i32(dtype), ctypes.c_int64(rows), _i32(cols), _vp(q), _vp(scale),
+                                    _vp(stream))
+
+
+def moe_quantize_int4(w, dtype, rows, cols, q, scale, stream):
+    return load().moe_quantize_int4(_vp(w), _i32(dtype), ctypes.c_int64(rows), _i32(cols), _vp(q), _vp(scale),
                                     _vp(stream))
 
 

@@ -11,8 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "kernels.h"
-#include "moe.h"
+#include "host.h"
 
 namespace moe {
 
@@ -22,40 +21,7 @@ std::atomic<unsigned long long>& launch_counter()
     return n;
 }
 
-namespace {
-
-constexpr size_t kRegionAlign = 1024;
-
-struct Layout {
-    int T, d, F, E, S, k;
-    int C;             // capacity, -1 = none
-    int n_rblk;        // router blocks
-    int nchunks;       // dispatch-scan blocks
-    int rows_cap;      // rows of the permuted buffers (multiple of 128)
-    int t_pad;         // T rounded up to 128 (shared-expert buffers)
-    size_t esz;        // element size of the activation dtype
-    bool tc_router;    // bf16 router logits on the tensor core
-    bool tc_rbwd;      // router gradients on the tensor core (bf16 layers)
-    int r_bn, r_tiles, e_pad;  // router GEMM: MMA N, expert tiles, padded experts
-    int r_ksplits;             // router GEMM K splits
-    bool r_fuse;               // top-k in the router GEMM's epilogue
-    size_t off_wsplit, off_logits;
-    size_t off_nsplit, off_nlogits;  // noisy gating: W_noise splits, noise logits [ks, T, E]
-    size_t off_psum_chunk;
-    size_t off_ffn_sync;  // fused experts: [0] tile counter, [1] finished CTAs, [2..] per-M-tile counts
-    int ffn_sync_n;
-    size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
-        off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys;
-    // backward (MOE_FLAG_TRAINING): gate and router gradients, the router's share of dx,
-    // dYp (reused for dXp), pre-activations (overwritten in place by their gradients;
-    // relu: dZ1 only), shared-expert pre-activations and input gradient
-    size_t off_bw_dgate, off_bw_dl, off_bw_dn, off_bw_dxr, off_bw_dyp, off_bw_z1, off_bw_z3, off_bw_zs1,
-        off_bw_zs3, off_bw_dxs;
-    // router gradients on the tensor core: split gradients, paired weights, dW partials
-    int e8, r_nblk, r_dw_splits;
-    size_t off_bw_dcat, off_bw_wcat, off_bw_p;
-    size_t total;
-};
+namespace host {
 
 long long capacity_of(const moe_params_t& p)
 {
@@ -82,12 +48,18 @@ moe_status_t validate_params(const moe_params_t* p)
         return MOE_ERR_INVALID_ARG;
     if (std::isnan(p->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (p->noisy_gating != 0 && p->noisy_gating != 1) return MOE_ERR_INVALID_ARG;
-    if (p->weight_format != MOE_WEIGHTS_DTYPE && p->weight_format != MOE_WEIGHTS_INT8) return MOE_ERR_INVALID_ARG;
+    if (p->weight_format != MOE_WEIGHTS_DTYPE && p->weight_format != MOE_WEIGHTS_INT8 &&
+        p->weight_format != MOE_WEIGHTS_INT4)
+        return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(p->noise_min_std) || p->noise_min_std < 0.0f) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && p->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     if (p->weight_format == MOE_WEIGHTS_INT8 &&
         (p->dtype != MOE_BF16 || (p->flags & (MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_TRAINING)) || p->n_shared != 0 ||
          p->d_model % 16 != 0 || p->d_ff % 16 != 0))
+        return MOE_ERR_UNSUPPORTED;
+    if (p->weight_format == MOE_WEIGHTS_INT4 &&
+        (p->dtype != MOE_BF16 || (p->flags & (MOE_FLAG_FFMA_EXPERTS | MOE_FLAG_TRAINING)) || p->n_shared != 0 ||
+         p->d_model % MOE_INT4_GROUP != 0 || p->d_ff % MOE_INT4_GROUP != 0))
         return MOE_ERR_UNSUPPORTED;
     // every index and row count below must fit in int32
     const long long slots = (long long)p->T * p->k;
@@ -196,7 +168,7 @@ moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const mo
     if (p.noisy_gating == 1 ? (!in->W_noise || (rows && !in->noise_eps))
                             : (in->W_noise || in->b_noise || in->noise_eps))
         return MOE_ERR_INVALID_ARG;
-    if (p.weight_format == MOE_WEIGHTS_INT8 ? (!in->W1_scale || !in->W2_scale || (swiglu != (in->W3_scale != nullptr)))
+    if (p.weight_format != MOE_WEIGHTS_DTYPE ? (!in->W1_scale || !in->W2_scale || (swiglu != (in->W3_scale != nullptr)))
                                             : (in->W1_scale || in->W3_scale || in->W2_scale))
         return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
@@ -242,6 +214,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 
 // 2-D byte tensor map over a row-major [rows, cols] int8 matrix, box {64, box_rows},
 // no swizzle (64-byte rows in shared memory), zero fill out of bounds.
+// 2-D byte tensor map over a row-major [rows, cols] array, box {box_cols, box_rows},
+// with the given swizzle (the box's rows are box_cols bytes), zero fill out of bounds.
+bool encode_u8_2d_swizzled(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                           uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows)
 {
     auto enc = tensor_map_encoder();
@@ -270,26 +258,6 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct Ctx {
-    moe_params_t p;
-    const moe_inputs_t* in;
-    moe_outputs_t* out;
-    char* ws;
-    Layout L;
-    cudaStream_t st;
-    int sms;
-    bool bf16, use_tc, fused;
-    bool pdl = false;  // false until this call has launched its first kernel
-    int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
-    CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW, mWn;
-    bool q8 = false;              // int8 expert weights
-    CUtensorMap mQ1, mQ3, mQ2;    // their uint8 maps
-    template <typename T>
-    T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
-    uint32_t* err() const { return reinterpret_cast<uint32_t*>(ws); }
-    unsigned* scan_done() const { return reinterpret_cast<unsigned*>(ws) + 1; }
-};
-
 int pick_bn(int N) { return N >= 256 ? 256 : 128; }
 
 // PDL for every launch of a C-ABI call except its first one (whose predecessor in
@@ -302,12 +270,12 @@ bool take_pdl(Ctx& c)
 }
 
 moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_outputs_t* out, void* ws,
-                     size_t ws_bytes, void* stream, Ctx& c)
+                     size_t ws_bytes, void* stream, Ctx& c, bool io_checked)
 {
     moe_status_t s = validate_params(params);
     if (s != MOE_OK) return s;
     c.p = *params;
-    s = validate_io(c.p, in, out);
+    s = io_checked ? MOE_OK : validate_io(c.p, in, out);
     if (s != MOE_OK) return s;
     c.in = in;
     c.out = out;
@@ -331,8 +299,36 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
             !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, 3 * L.r_bn))
             return MOE_ERR_UNSUPPORTED;
     }
+    // quantised expert weights: the transposed tensor-memory kernel (k_grouped_gemm_wq) for
+    // layers whose experts hold at most 128 token rows each (the expert stage streams the
+    // weights) and for every 4-bit layer; the 8-bit shared-memory converter kernel otherwise
     c.q8 = c.p.weight_format == MOE_WEIGHTS_INT8;
-    if (c.q8) {
+    c.wq = c.p.weight_format == MOE_WEIGHTS_INT4;
+    if (c.q8 || c.wq) {
+        const long long bound = c.L.C >= 0 ? std::min(c.L.C, c.L.T) : c.L.T;  // rows one expert can hold
+        if (c.q8 && bound <= 128) c.wq = true;
+    }
+    if (c.wq) {
+        const Layout& L = c.L;
+        const bool gated = c.p.act == MOE_ACT_SWIGLU;
+        const long long bound = L.C >= 0 ? std::min(L.C, L.T) : L.T;
+        c.wq_bits = c.p.weight_format == MOE_WEIGHTS_INT4 ? 4 : 8;
+        c.wq_nt = gemm_wq_tokens_tile((int)std::min<long long>(bound, 1 << 30), gated);
+        const uint32_t kb_bytes = c.wq_bits == 8 ? 64 : 32;  // bytes of one 64-column K block
+        const CUtensorMapSwizzle swz = c.wq_bits == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+        const uint64_t dcols = (uint64_t)L.d * c.wq_bits / 8, fcols = (uint64_t)L.F * c.wq_bits / 8;
+        bool ok = encode_u8_2d_swizzled(&c.mQ1, in->W1, (uint64_t)L.E * L.F, dcols, kb_bytes, 128, swz) &&
+                  encode_u8_2d_swizzled(&c.mQ3, gated ? in->W3 : in->W1, (uint64_t)L.E * L.F, dcols, kb_bytes, 128,
+                                        swz) &&
+                  encode_u8_2d_swizzled(&c.mQ2, in->W2, (uint64_t)L.E * L.d, fcols, kb_bytes, 128, swz);
+        if (L.rows_cap > 0)
+            ok = ok && encode_bf16_2d(&c.mA1, c.at<void>(L.off_xp), L.rows_cap, L.d, c.wq_nt) &&
+                 encode_bf16_2d(&c.mA2, c.at<void>(L.off_h), L.rows_cap, L.F, c.wq_nt);
+        if (!ok) return MOE_ERR_UNSUPPORTED;
+        c.q8 = false;
+        c.use_tc = false;  // the quantised-weight kernels replace the bf16 tensor-core path
+        c.fused = false;
+    } else if (c.q8) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
         const uint32_t r1 = gated ? 128 : 256;
@@ -542,13 +538,47 @@ moe_status_t stage_gemm(Ctx& c)
     s2.out = c.at<void>(L.off_ys);
     s2.a_rows_alloc = L.T;
 
-    const int mt_routed = L.rows_cap / kSegRows;
+    const int mt_routed = c.routed_experts ? L.rows_cap / kSegRows : 0;
     const int mt_shared = L.t_pad / kSegRows;
     auto grid_for = [&](int tiles, int per_sm) { return std::max(1, std::min(tiles, c.sms * per_sm)); };
     cudaError_t e = cudaSuccess;
     // training: the first layer also keeps its pre-activations for the backward pass
     // (relu's derivative comes from H itself)
     const bool save = (c.p.flags & MOE_FLAG_TRAINING) && c.p.act != MOE_ACT_RELU;
+    if (c.wq) {
+        if (mt_routed == 0) return MOE_OK;
+        GroupedGemmWqArgs w1{};
+        w1.row_off = g1.row_off;
+        w1.rows = g1.rows;
+        w1.G = L.E;
+        w1.N = L.F;
+        w1.n_tiles = ceil_div(L.F, 128);
+        w1.K = L.d;
+        w1.b_rows_per_group = L.F;
+        w1.out = g1.out;
+        w1.ldo = L.F;
+        w1.bias = c.in->b1;
+        w1.scale = c.in->W1_scale;
+        w1.scale3 = c.in->W3_scale;
+        w1.err = c.err();
+        GroupedGemmWqArgs w2 = w1;
+        w2.N = L.d;
+        w2.n_tiles = ceil_div(L.d, 128);
+        w2.K = L.F;
+        w2.b_rows_per_group = L.d;
+        w2.out = g2.out;
+        w2.ldo = L.d;
+        w2.bias = c.in->b2;
+        w2.scale = c.in->W2_scale;
+        w2.scale3 = nullptr;
+        const int token_tiles = L.rows_cap / c.wq_nt;  // bound: segments are padded to 128 rows
+        e = launch_gemm_wq(c.mA1, c.mQ1, c.mQ3, w1, c.wq_bits, act1, c.wq_nt,
+                           grid_for(token_tiles * w1.n_tiles, 1), c.st, take_pdl(c));
+        if (e == cudaSuccess)
+            e = launch_gemm_wq(c.mA2, c.mQ2, c.mQ2, w2, c.wq_bits, kActNone, c.wq_nt,
+                               grid_for(token_tiles * w2.n_tiles, 1), c.st, take_pdl(c));
+        return cuda_status(e);
+    }
     if (c.q8) {
         if (mt_routed == 0) return MOE_OK;
         GroupedGemmQ8Args q1{};
@@ -1390,10 +1420,11 @@ moe_status_t run_backward(Ctx& c, const void* dy, float d_aux, const moe_grads_t
     return cuda_status(e);
 }
 
-}  // namespace
+}  // namespace host
 }  // namespace moe
 
 using namespace moe;
+using namespace moe::host;
 
 extern "C" {
 
@@ -1477,6 +1508,19 @@ moe_status_t moe_check_bounded_wait(void* workspace, size_t workspace_bytes, uin
     if (timeout_us < 1 || timeout_us > 1000000) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_wait_expires(static_cast<uint32_t*>(workspace), 1000ull * timeout_us,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quantize_int4(const void* w, int32_t dtype, int64_t rows, int32_t cols, uint8_t* q, float* scale,
+                               void* stream)
+{
+    if (w == nullptr || q == nullptr || scale == nullptr || rows < 0 || cols < 1) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+    if (cols % MOE_INT4_GROUP != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    return cuda_status(launch_quantize_int4(w, dtype == MOE_BF16, rows, cols, q, scale, sms,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_quantize_int8(const void* w, int32_t dtype, int64_t rows, int32_t cols, int8_t* q, float* scale,

@@ -1,0 +1,550 @@
+// grouped_gemm_wq.cu -- stage 3 with quantised expert weights (8-bit per-row or
+// 4-bit group-wise) for layers whose experts see few tokens each, where the
+// expert stage streams the weights from HBM.
+//
+// "MoE架构解析" §"部署实践": expert weights stored as 8-bit integers lose almost
+// no accuracy and shrink the bytes the expert stage streams; "MoE混合专家模型
+// 原理与实战" §"量化与PagedAttention结合": the experts alone may be quantised to
+// INT4 (AWQ: group-wise scales) while the router keeps its precision.
+//
+// The kernel computes the transposed product, with the weights as the MMA's A
+// operand taken from tensor memory:
+//     D[n, m] = sum_k W[n, k] X[m, k]      (n: 128 weight rows, m: NT tokens)
+// The converter warps read each landed weight tile from shared memory once,
+// turn it into bf16 in registers and write it straight into TMEM
+// (tcgen05.st), so the converted operand never makes a round trip through
+// shared memory; the tensor core reads A from TMEM and the token tile (B,
+// K-major, 128-byte swizzle) from shared memory.  The token tile is small
+// (NT = 32 .. 128 rows, as many as the experts hold), so no MMA work is spent
+// on padding rows of 128-row token tiles.
+//   8-bit: q in [-127, 127] is exact in bf16; the per-row scale is applied to
+//          the accumulator in the epilogue: sum_k q[n,k] x[m,k] * scale[n].
+//   4-bit: the converter multiplies q in [-7, 7] by its group's scale (groups
+//          of 128 input columns) in fp32 and rounds once to bf16.
+// One thread of the epilogue holds one weight row (its TMEM lane) for NT
+// tokens: scale, bias and activation are per-thread scalars, and SwiGLU pairs
+// the W1 and W3 accumulators of the same row.
+//
+// Per CTA (one per SM, 384 threads):
+//   warp 0      TMA: token tile [NT x 64] bf16 and the weight tile(s) [128 x 64]
+//               (8-bit: 64-byte rows, 64-byte swizzle; 4-bit: 32-byte rows,
+//               32-byte swizzle) per stage;
+//   warp 1      TMEM allocation and tcgen05.mma (M = 128, N = NT, K = 16, A from TMEM);
+//   warps 4-7   converters (warp w writes TMEM lanes 32 (w % 4) .. + 31);
+//   warps 8-11  epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
+// Every wait is bounded, as in the other tcgen05 kernels.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_tile.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBW = 128;  // weight rows per A tile (MMA M)
+constexpr int kBK = 64;   // reduction per stage
+constexpr int kThreads = 384;
+constexpr int kGroupCols = 128;  // 4-bit scale groups along K
+constexpr size_t kBarBytes = 256;
+constexpr size_t kTableBytes = sizeof(int) * (3 * kMaxExperts + 2);
+
+template <int WBITS, bool GATED, int NT>
+struct Cfg {
+    static constexpr int kStages = GATED ? 4 : 6;
+    static constexpr int kNA = GATED ? 2 : 1;                    // A tiles per stage
+    static constexpr uint32_t kXBytes = NT * kBK * 2;            // token tile
+    static constexpr uint32_t kWRowBytes = kBK * WBITS / 8;      // 64 or 32
+    static constexpr uint32_t kWBytes = kNA * kBW * kWRowBytes;  // weight tile(s)
+    static constexpr uint32_t kStageBytes = (kXBytes + kWBytes + 1023) / 1024 * 1024;
+    static constexpr uint32_t kAccCols = kNA * NT;               // one accumulator set
+    static constexpr uint32_t kACols = kNA * 32;                 // TMEM A columns per stage
+    static constexpr uint32_t kACol0 = 2 * kAccCols;             // A region after the two accumulators
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kACol0 + kStages * kACols <= kTmemCols, "tensor memory budget");
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kTableBytes;
+};
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by a single thread.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Each thread of the warp stores 32 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// int8 x 4 (one 32-bit word) -> bf16 x 4 (two words), exactly: flipping the sign bit
+// makes the byte v + 128, a byte permute places it in the low mantissa of 2^23, and
+// subtracting 2^23 + 128 leaves v in fp32; |v| <= 128 is exact in bf16.
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u)) - 8388736.0f;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u)) - 8388736.0f;
+    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542u)) - 8388736.0f;
+    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543u)) - 8388736.0f;
+    lo = pack_bf16x2(f0, f1);
+    hi = pack_bf16x2(f2, f3);
+}
+
+// int4 x 8 (one 32-bit word, value 2i in nibble 2i) -> bf16 x 8 of q * s (four words):
+// the nibble plus 8 (offset binary) goes into the low mantissa of 2^23, subtracting
+// 2^23 + 8 leaves q exactly; q * s is rounded once to bf16.
+__device__ __forceinline__ void i4x8_to_bf16(uint32_t w, float s, uint32_t (&o)[4])
+{
+    const uint32_t u = w ^ 0x88888888u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float lo = __uint_as_float(0x4B000000u | ((u >> (8 * p)) & 0xFu)) - 8388616.0f;
+        const float hi = __uint_as_float(0x4B000000u | ((u >> (8 * p + 4)) & 0xFu)) - 8388616.0f;
+        o[p] = pack_bf16x2(lo * s, hi * s);
+    }
+}
+
+// Tiles: group g has tt[g] = ceil(rows[g] / NT) token tiles and n_tiles weight-row
+// tiles; inside a group the token tile runs fastest, so the CTAs working at the same
+// time share each weight tile through L2.
+struct WqTiles {
+    int g = 0;
+    __device__ __forceinline__ void locate(int tile, const int* toff, int n_tiles, int& mt, int& n)
+    {
+        while (tile >= toff[g + 1] * n_tiles) ++g;
+        const int local = tile - toff[g] * n_tiles;
+        const int ttg = toff[g + 1] - toff[g];
+        n = local / ttg;
+        mt = local - n * ttg;
+    }
+};
+
+template <int WBITS, int ACT, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_grouped_gemm_wq(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmW3, const GroupedGemmWqArgs args)
+{
+    constexpr bool GATED = (ACT == kActSwiglu);
+    using C = Cfg<WBITS, GATED, NT>;
+    constexpr int S = C::kStages;
+    constexpr uint32_t IDESC = idesc_bf16_f32(kBW, NT);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full_q = reinterpret_cast<uint64_t*>(base + (size_t)S * C::kStageBytes);
+    uint64_t* full_a = full_q + S;
+    uint64_t* empty = full_a + S;
+    uint64_t* tfull = empty + S;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_toff = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_q) + kBarBytes);  // [G + 1]
+    int* s_roff = s_toff + kMaxExperts + 1;
+    int* s_rows = s_roff + kMaxExperts;
+
+    griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = args.G;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_q[s], 1);
+            mbar_init(&full_a[s], 4);  // one arrival per converter warp
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+        if (GATED) tma_prefetch_desc(&tmW3);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    griddep_wait();  // segment tables and the token rows come from earlier kernels
+    for (int i = threadIdx.x; i < G; i += kThreads) {
+        s_roff[i] = args.row_off[i];
+        s_rows[i] = args.rows[i];
+    }
+    __syncthreads();
+    if (warp == 0) {  // token-tile offsets: exclusive prefix of ceil(rows / NT) over the groups
+        const int per = (G + 31) / 32;
+        const int b = lane * per, e = min(G, b + per);
+        int sum = 0;
+        for (int i = b; i < e; ++i) sum += (s_rows[i] + NT - 1) / NT;
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+        for (int i = b; i < e; ++i) {
+            s_toff[i] = run;
+            run += (s_rows[i] + NT - 1) / NT;
+        }
+        if (lane == 31) s_toff[G] = incl;
+    }
+    __syncthreads();
+
+    const int n_tiles = args.n_tiles;
+    const int total = s_toff[G] * n_tiles;
+    const int num_kb = ceil_div(args.K, kBK);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_act = policy_evict_last();
+            const uint64_t pol_w = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, filled = 0, fill_par = 0;
+            bool ok = true;
+            WqTiles tm;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int mt, n;
+                tm.locate(tile, s_toff, n_tiles, mt, n);
+                const int x_row = s_roff[tm.g] + mt * NT;
+                const int w_row = tm.g * args.b_rows_per_group + n * kBW;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = base + (size_t)stage * C::kStageBytes;
+                    mbar_arrive_expect_tx(&full_q[stage], C::kXBytes + C::kWBytes);
+                    tma_load_2d(st, &tmX, &full_q[stage], kb * kBK, x_row, pol_act);
+                    const int wc = kb * (int)C::kWRowBytes;  // byte column of the weight rows
+                    tma_load_2d(st + C::kXBytes, &tmW, &full_q[stage], wc, w_row, pol_w);
+                    if (GATED) tma_load_2d(st + C::kXBytes + kBW * C::kWRowBytes, &tmW3, &full_q[stage], wc, w_row, pol_w);
+                    filled |= 1u << stage;
+                    fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(args.err, kErrTimeoutProducer);
+                *abort_flag = 1;
+                for (int s = 0; s < S; ++s)
+                    if (((filled >> s) & 1u) && !mbar_wait_short(&full_q[s], (fill_par >> s) & 1u))
+                        atomicOr(args.err, kErrTimeoutDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full_a[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t x0 = smem_u32(base + (size_t)stage * C::kStageBytes);
+                    const uint32_t a0 = tmem_base + C::kACol0 + stage * C::kACols;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t bdesc = sdesc_kmajor_sw128(x0 + k * 32);
+                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+                        mma_bf16_ts(d_tmem, a0 + k * 8, bdesc, IDESC, accum);
+                        if (GATED) mma_bf16_ts(d_tmem + NT, a0 + 32 + k * 8, bdesc, IDESC, accum);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(&tfull[acc]);
+            }
+            if (!ok) {
+                atomicOr(args.err, kErrTimeoutMma);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);
+            if (!mbar_wait_short(drain, 0)) atomicOr(args.err, kErrTimeoutDrain);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ converters
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // this thread's weight row in the tile (its TMEM lane)
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        WqTiles tm;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            int mt, n;
+            tm.locate(tile, s_toff, n_tiles, mt, n);
+            const int w_row = tm.g * args.b_rows_per_group + n * kBW + r;  // global weight row
+            const bool w_ok = n * kBW + r < args.N;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                float s1 = 0.0f, s3 = 0.0f;
+                if constexpr (WBITS == 4) {  // the group scales of this K-block (before the wait)
+                    const int ng = args.K / kGroupCols;
+                    const int grp = (kb * kBK) / kGroupCols;
+                    if (w_ok) {
+                        s1 = __ldg(&args.scale[(size_t)w_row * ng + grp]);
+                        if (GATED) s3 = __ldg(&args.scale3[(size_t)w_row * ng + grp]);
+                    }
+                }
+                if (!mbar_wait(&full_q[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* wt = base + (size_t)stage * C::kStageBytes + C::kXBytes;
+#pragma unroll
+                for (int h = 0; h < C::kNA; ++h) {
+                    const uint8_t* row = wt + (size_t)(h * kBW + r) * C::kWRowBytes;
+                    uint32_t v[32];
+                    if constexpr (WBITS == 8) {
+                        // 64-byte rows, 64-byte swizzle: 16-byte chunk c at c ^ ((r >> 1) & 3)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 1) & 3)) << 4));
+                            i8x4_to_bf16(u.x, v[c * 8 + 0], v[c * 8 + 1]);
+                            i8x4_to_bf16(u.y, v[c * 8 + 2], v[c * 8 + 3]);
+                            i8x4_to_bf16(u.z, v[c * 8 + 4], v[c * 8 + 5]);
+                            i8x4_to_bf16(u.w, v[c * 8 + 6], v[c * 8 + 7]);
+                        }
+                    } else {
+                        // 32-byte rows, 32-byte swizzle: 16-byte chunk c at c ^ ((r >> 2) & 1)
+                        const float sc = h == 0 ? s1 : s3;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 2) & 1)) << 4));
+                            uint32_t o[4];
+                            i4x8_to_bf16(u.x, sc, o);
+                            v[c * 16 + 0] = o[0], v[c * 16 + 1] = o[1], v[c * 16 + 2] = o[2], v[c * 16 + 3] = o[3];
+                            i4x8_to_bf16(u.y, sc, o);
+                            v[c * 16 + 4] = o[0], v[c * 16 + 5] = o[1], v[c * 16 + 6] = o[2], v[c * 16 + 7] = o[3];
+                            i4x8_to_bf16(u.z, sc, o);
+                            v[c * 16 + 8] = o[0], v[c * 16 + 9] = o[1], v[c * 16 + 10] = o[2], v[c * 16 + 11] = o[3];
+                            i4x8_to_bf16(u.w, sc, o);
+                            v[c * 16 + 12] = o[0], v[c * 16 + 13] = o[1], v[c * 16 + 14] = o[2], v[c * 16 + 15] = o[3];
+                        }
+                    }
+                    tmem_st_32cols(t_row + C::kACol0 + stage * C::kACols + h * 32, v);
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_a[stage]);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(args.err, kErrTimeoutProducer);
+            *abort_flag = 1;
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+        const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(args.bias);
+        bool ok = true;
+        int it = 0;
+        WqTiles tm;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            int mt, n;
+            tm.locate(tile, s_toff, n_tiles, mt, n);
+            const int acc = it & 1;
+            if (!mbar_wait(&tfull[acc], (it >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const int col = n * kBW + r;  // this thread's output column
+            const bool col_ok = col < args.N;
+            const size_t wr = (size_t)tm.g * args.b_rows_per_group + (col_ok ? col : 0);
+            // per-row factors: the 8-bit scales (the 4-bit ones were applied by the converters)
+            float f1 = 1.0f, f3 = 1.0f, b = 0.0f;
+            if constexpr (WBITS == 8) {
+                f1 = args.scale[wr];
+                if (GATED) f3 = args.scale3[wr];
+            }
+            if (!GATED && bias != nullptr) b = __bfloat162float(bias[wr]);
+            const int m0 = mt * NT;
+            const int valid = min(NT, s_rows[tm.g] - m0);
+            __nv_bfloat16* o = out + (size_t)(s_roff[tm.g] + m0) * args.ldo + col;
+            const uint32_t t_lane = tmem_base + acc * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < NT / 32; ++c) {
+                uint32_t va[32], vb[32];
+                tmem_ld_32cols(t_lane + c * 32, va);
+                if constexpr (GATED) tmem_ld_32cols(t_lane + NT + c * 32, vb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int m = c * 32 + j;
+                    float z = __uint_as_float(va[j]) * f1;
+                    float y;
+                    if constexpr (GATED) {
+                        y = activate_bf16out<kActSwiglu>(z) * (__uint_as_float(vb[j]) * f3);
+                    } else {
+                        y = activate_bf16out<ACT>(z + b);
+                    }
+                    if (col_ok && m < valid) o[(size_t)m * args.ldo] = __float2bfloat16_rn(y);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(args.err, kErrTimeoutEpilogue);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int WBITS, int ACT, int NT>
+cudaError_t launch_t(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3, const GroupedGemmWqArgs& a,
+                     int grid, cudaStream_t st, bool pdl)
+{
+    using C = Cfg<WBITS, ACT == kActSwiglu, NT>;
+    auto kern = k_grouped_gemm_wq<WBITS, ACT, NT>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, pdl, x, w, w3, a);
+}
+
+template <int WBITS, int NT>
+cudaError_t launch_nt(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3, const GroupedGemmWqArgs& a,
+                      int act, int grid, cudaStream_t st, bool pdl)
+{
+    switch (act) {
+    case kActNone: return launch_t<WBITS, kActNone, NT>(x, w, w3, a, grid, st, pdl);
+    case kActRelu: return launch_t<WBITS, kActRelu, NT>(x, w, w3, a, grid, st, pdl);
+    case kActGeluTanh: return launch_t<WBITS, kActGeluTanh, NT>(x, w, w3, a, grid, st, pdl);
+    case kActGeluErf: return launch_t<WBITS, kActGeluErf, NT>(x, w, w3, a, grid, st, pdl);
+    default:
+        if constexpr (NT <= 64) return launch_t<WBITS, kActSwiglu, NT>(x, w, w3, a, grid, st, pdl);
+        return cudaErrorInvalidValue;  // the gated layer's tensor-memory budget caps NT at 64
+    }
+}
+
+// One warp per (row, group of 128 columns): scale = max|w| / 7, q = rint(w / scale)
+// (IEEE fp32 division) clamped to [-7, 7], two values per byte (low nibble first).
+template <typename T>
+__global__ void __launch_bounds__(256) k_quantize_int4(const T* __restrict__ w, long long rows, int cols,
+                                                       uint8_t* __restrict__ q, float* __restrict__ scale)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ng = cols / kGroupCols;
+    const long long items = rows * ng;
+    for (long long it = (long long)blockIdx.x * 8 + warp; it < items; it += (long long)gridDim.x * 8) {
+        const long long row = it / ng;
+        const int g = (int)(it - row * ng);
+        const T* src = w + row * cols + g * kGroupCols + lane * 4;
+        float v[4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = to_f32(src[i]);
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = amax / 7.0f;
+        if (lane == 0) scale[it] = s;
+        uint32_t nib[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float t = s > 0.0f ? rintf(v[i] / s) : 0.0f;
+            t = fminf(fmaxf(t, -7.0f), 7.0f);
+            nib[i] = static_cast<uint32_t>(static_cast<int>(t)) & 0xFu;
+        }
+        const uint16_t packed = static_cast<uint16_t>(nib[0] | (nib[1] << 4) | (nib[2] << 8) | (nib[3] << 12));
+        *reinterpret_cast<uint16_t*>(q + row * (cols / 2) + g * (kGroupCols / 2) + lane * 2) = packed;
+    }
+}
+
+}  // namespace
+
+int gemm_wq_tokens_tile(int max_rows_per_expert, bool gated)
+{
+    if (max_rows_per_expert <= 32) return 32;
+    if (max_rows_per_expert <= 64 || gated) return 64;
+    return 128;
+}
+
+cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3,
+                           const GroupedGemmWqArgs& a, int wbits, int act, int nt, int grid, cudaStream_t st, bool pdl)
+{
+    if (wbits == 8) {
+        if (nt == 32) return launch_nt<8, 32>(x, w, w3, a, act, grid, st, pdl);
+        if (nt == 64) return launch_nt<8, 64>(x, w, w3, a, act, grid, st, pdl);
+        return launch_nt<8, 128>(x, w, w3, a, act, grid, st, pdl);
+    }
+    if (nt == 32) return launch_nt<4, 32>(x, w, w3, a, act, grid, st, pdl);
+    if (nt == 64) return launch_nt<4, 64>(x, w, w3, a, act, grid, st, pdl);
+    return launch_nt<4, 128>(x, w, w3, a, act, grid, st, pdl);
+}
+
+cudaError_t launch_quantize_int4(const void* w, bool bf16, long long rows, int cols, uint8_t* q, float* scale,
+                                 int sms, cudaStream_t st)
+{
+    const long long items = rows * (cols / kGroupCols);
+    long long grid = (items + 7) / 8;
+    if (grid > (long long)sms * 32) grid = (long long)sms * 32;
+    if (grid < 1) grid = 1;
+    if (bf16)
+        return launch_kernel(k_quantize_int4<__nv_bfloat16>, dim3((int)grid), dim3(256), 0, st, false,
+                             static_cast<const __nv_bfloat16*>(w), rows, cols, q, scale);
+    return launch_kernel(k_quantize_int4<float>, dim3((int)grid), dim3(256), 0, st, false,
+                         static_cast<const float*>(w), rows, cols, q, scale);
+}
+
+}  // namespace moe

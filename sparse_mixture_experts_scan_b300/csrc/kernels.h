@@ -168,6 +168,36 @@ size_t gemm_q8_smem();
 cudaError_t launch_quantize_int8(const void* w, bool bf16, long long rows, int cols, int8_t* q, float* scale,
                                  int sms, cudaStream_t st);
 
+// Quantised expert weights for layers whose experts hold few tokens (the expert
+// stage streams the weights): the transposed product D[n, m] = W[n, :] . X[m, :]
+// with the weight tile converted to bf16 into tensor memory (the MMA's A operand)
+// and the token tile (NT rows) as B.  8-bit: per-row scales applied in the
+// epilogue; 4-bit: group scales (128 input columns) applied by the converters.
+// maps: X (bf16 [rows, K], box {64, NT}), W and W3 (uint8 [groups * rows, K bytes],
+// box {64 or 32 bytes, 128}, 64- or 32-byte swizzle).
+struct GroupedGemmWqArgs {
+    const int* row_off;    // [G] padded segment starts of the token rows
+    const int* rows;       // [G] token rows per group
+    int G;
+    int N, n_tiles, K;     // output columns (weight rows per group), tiles of 128, reduction
+    int b_rows_per_group;
+    void* out;             // [rows, ldo] bf16
+    int ldo;
+    const void* bias;      // [G, b_rows_per_group] bf16 or nullptr
+    const float* scale;    // 8-bit: [G, b_rows_per_group]; 4-bit: [G, b_rows_per_group, K / 128]
+    const float* scale3;   // SwiGLU: the W3 rows' scales
+    uint32_t* err;
+};
+// Token rows per tile for a layer whose experts hold at most max_rows_per_expert rows.
+int gemm_wq_tokens_tile(int max_rows_per_expert, bool gated);
+cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3,
+                           const GroupedGemmWqArgs& a, int wbits, int act, int nt, int grid, cudaStream_t st,
+                           bool pdl);
+// Group-wise symmetric 4-bit quantisation (groups of 128 columns, scale = max|w| / 7,
+// q = rint(w / scale) in [-7, 7], two values per byte, low nibble first).
+cudaError_t launch_quantize_int4(const void* w, bool bf16, long long rows, int cols, uint8_t* q, float* scale,
+                                 int sms, cudaStream_t st);
+
 // FFMA kernel over fp32 or bf16 operands (A [a_rows_alloc, lda], B [*, ldb]).
 cudaError_t launch_gemm_ffma(const void* A, int lda, const void* B, const void* B3, int ldb,
                              const GroupedGemmArgs& args, int act, bool bf16, int grid,

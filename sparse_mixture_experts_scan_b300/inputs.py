@@ -20,9 +20,9 @@ Configurations (shapes and distributions of the workloads the pages discuss):
   decode    the first 64 tokens of skewed with the same weights (capacity 1.0 -> C = 0)
   decode_nocap  the same without a capacity limit
 
-Int8 expert weights (weights="int8"): the tensors above are drawn as usual; the
-layer quantises W1, W3, W2 itself (moe_quantize_int8), so the inputs carry no
-quantisation arithmetic.
+Int8 / int4 expert weights (weights="int8" / "int4"): the tensors above are drawn
+as usual; the library quantises W1, W3, W2 itself (moe_quantize_int8 /
+moe_quantize_int4), so the inputs carry no quantisation arithmetic.
 
 Noisy top-k gating (any config with noisy=True): after the tensors above, W_noise
 and b_noise ~ U(-1/sqrt(d), 1/sqrt(d)) (nn.Linear's default initialisation of the
@@ -58,7 +58,7 @@ class LayerConfig:
     parent: str | None = None    # take the first T tokens of this config's inputs
     noisy: bool = False          # noisy top-k gating (training mode)
     noise_min_std: float = 0.0   # floor added to the softplus noise scale
-    weights: str = "dtype"       # dtype | int8 (expert weights quantised per output row)
+    weights: str = "dtype"       # dtype | int8 (per output row) | int4 (per group of 128 inputs)
 
     @property
     def torch_dtype(self):

@@ -34,7 +34,8 @@ def make_params(cfg: LayerConfig, *, flags: int = 0, residual_mode: int | None =
         residual_mode=cfg.residual_mode if residual_mode is None else residual_mode,
         act=ACT_CODES[cfg.act], dtype=_lib.MOE_BF16 if cfg.dtype == "bf16" else _lib.MOE_F32,
         flags=flags, noisy_gating=int(cfg.noisy), noise_min_std=float(cfg.noise_min_std),
-        weight_format=_lib.MOE_WEIGHTS_INT8 if cfg.weights == "int8" else _lib.MOE_WEIGHTS_DTYPE)
+        weight_format={"int8": _lib.MOE_WEIGHTS_INT8, "int4": _lib.MOE_WEIGHTS_INT4}.get(cfg.weights,
+                                                                                         _lib.MOE_WEIGHTS_DTYPE))
 
 
 def _ptr(t):
@@ -55,12 +56,19 @@ class MoELayer:
 
     def __init__(self, cfg: LayerConfig, weights: dict, device="cuda", *, flags: int = 0,
                  residual_mode: int | None = None, want_logits: bool = False,
-                 want_probs: bool = False, want_perm: bool = True):
+                 want_probs: bool = False, want_perm: bool = True, ep_ranks: int | None = None):
         self.cfg = cfg
         self.device = torch.device(device)
         self.params = make_params(cfg, flags=flags, residual_mode=residual_mode)
-        st, nbytes = _lib.moe_workspace_size(self.params)
-        check(st, "moe_workspace_size")
+        # ep_ranks = G: the layer runs expert-parallel over G ranks emulated on this GPU
+        # (moe_forward_ep); only the whole forward is available then
+        self.ep_ranks = ep_ranks
+        if ep_ranks is None:
+            st, nbytes = _lib.moe_workspace_size(self.params)
+            check(st, "moe_workspace_size")
+        else:
+            st, nbytes = _lib.moe_ep_workspace_size(self.params, ep_ranks)
+            check(st, "moe_ep_workspace_size")
         self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         self.workspace_bytes = nbytes
         self.weights = {k: (None if v is None else v.contiguous()) for k, v in weights.items()}
@@ -97,6 +105,13 @@ class MoELayer:
         self.inputs.x = x.data_ptr()
 
     def run(self, stage: str = "moe_forward", stream=None) -> dict:
+        if self.ep_ranks is not None:
+            if stage != "moe_forward":
+                raise ValueError("an expert-parallel layer runs the whole forward only")
+            check(_lib.moe_forward_ep(self.params, self.ep_ranks, self.inputs, self.outputs,
+                                      self.workspace.data_ptr(), self.workspace_bytes,
+                                      _stream_handle(stream)), "moe_forward_ep")
+            return self.out
         fn = getattr(_lib, stage)
         check(fn(self.params, self.inputs, self.outputs, self.workspace.data_ptr(),
                  self.workspace_bytes, _stream_handle(stream)), stage)
@@ -155,12 +170,28 @@ def quantize_int8(w: torch.Tensor, stream=None):
     return q, scale
 
 
-def quantize_expert_weights(weights: dict, stream=None) -> dict:
-    """The layer's inputs with W1, W3, W2 replaced by int8 + per-row scales."""
+def quantize_int4(w: torch.Tensor, stream=None):
+    """Group-wise 4-bit quantisation of a [..., cols] device tensor (moe_quantize_int4):
+    returns (q uint8 [..., cols / 2], two values per byte; scale fp32 [..., cols / 128])."""
+    w = w.contiguous()
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    q = torch.empty((*w.shape[:-1], cols // 2), dtype=torch.uint8, device=w.device)
+    scale = torch.empty((*w.shape[:-1], cols // _lib.MOE_INT4_GROUP), dtype=torch.float32, device=w.device)
+    dt = _lib.MOE_BF16 if w.dtype == torch.bfloat16 else _lib.MOE_F32
+    check(_lib.moe_quantize_int4(w.data_ptr(), dt, rows, cols, q.data_ptr(), scale.data_ptr(),
+                                 _stream_handle(stream)), "moe_quantize_int4")
+    return q, scale
+
+
+def quantize_expert_weights(weights: dict, stream=None, bits: int = 8) -> dict:
+    """The layer's inputs with W1, W3, W2 replaced by int8 + per-row scales (bits = 8)
+    or packed 4-bit values + group scales (bits = 4)."""
+    quant = {8: quantize_int8, 4: quantize_int4}[bits]
     out = dict(weights)
     for k in ("W1", "W3", "W2"):
         if weights.get(k) is not None:
-            out[k], out[k + "_scale"] = quantize_int8(weights[k], stream)
+            out[k], out[k + "_scale"] = quant(weights[k], stream)
     return out
 
 

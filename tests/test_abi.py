@@ -13,7 +13,8 @@ def test_library_exports_every_header_function():
                           "moe_grouped_gemm", "moe_combine", "moe_last_device_status",
                           "moe_status_string", "moe_dispatch_positions_noalloc",
                           "moe_kernel_launches", "moe_backward", "moe_quantize_int8",
-                          "moe_check_bounded_wait"}
+                          "moe_check_bounded_wait", "moe_ep_workspace_size", "moe_forward_ep",
+                          "moe_quantize_int4"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -232,7 +233,8 @@ def test_backward_validation_happens_before_any_launch():
     ("switch", {"flags": 1}, _lib.MOE_ERR_UNSUPPORTED),          # FFMA experts
     ("switch", {"flags": 8}, _lib.MOE_ERR_UNSUPPORTED),          # training
     ("switch", {"d_model": 776}, _lib.MOE_ERR_UNSUPPORTED),      # d not a multiple of 16
-    ("switch", {"weight_format": 2}, _lib.MOE_ERR_INVALID_ARG),
+    ("switch", {"weight_format": 2}, _lib.MOE_OK),               # the 4-bit format (d, F multiples of 128)
+    ("switch", {"weight_format": 3}, _lib.MOE_ERR_INVALID_ARG),
 ])
 def test_int8_weight_combinations(base, over, expect):
     p = make_params(config(base, weights="int8"))
@@ -276,4 +278,76 @@ def test_bounded_wait_check_validates_before_launch():
     assert _lib.moe_check_bounded_wait((1 << 40) + 16, 1024, 1000, None) == _lib.MOE_ERR_WORKSPACE
     assert _lib.moe_check_bounded_wait(1 << 40, 1024, 0, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_check_bounded_wait(1 << 40, 1024, 2000000, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0
+
+
+# ---- expert parallelism over G emulated ranks ---------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "deepseek", "skewed"])
+def test_ep_workspace_size(name):
+    cfg = config(name)
+    p = make_params(cfg)
+    one = _lib.moe_workspace_size(p)[1]
+    for G in (1, 2, 4, 8):
+        if cfg.E % G:
+            continue
+        st, n = _lib.moe_ep_workspace_size(p, G)
+        assert st == _lib.MOE_OK
+        assert n > one  # every rank's private region plus the owners' receive buffers
+
+
+@pytest.mark.parametrize("G,expect", [(0, _lib.MOE_ERR_INVALID_ARG), (-1, _lib.MOE_ERR_INVALID_ARG),
+                                      (17, _lib.MOE_ERR_INVALID_ARG), (3, _lib.MOE_ERR_INVALID_ARG),
+                                      (16, _lib.MOE_ERR_INVALID_ARG), (8, _lib.MOE_OK)])
+def test_ep_rank_count_validated(G, expect):
+    # mixtral: E = 8, so G must divide 8 (16 > E fails the divisibility)
+    st, _ = _lib.moe_ep_workspace_size(make_params(config("mixtral")), G)
+    assert st == expect
+
+
+@pytest.mark.parametrize("over,flags", [({"weights": "int8"}, 0), ({}, _lib.MOE_FLAG_TRAINING),
+                                        ({}, _lib.MOE_FLAG_UNFUSED_EXPERTS)])
+def test_ep_unsupported_combinations(over, flags):
+    p = make_params(config("switch", **over), flags=flags)
+    assert _lib.moe_ep_workspace_size(p, 2)[0] == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_ep_forward_validates_before_any_launch():
+    cfg = config("tiny")
+    p = make_params(cfg)
+    n0 = _lib.moe_kernel_launches()
+    inputs, outputs = _lib.moe_inputs_t(), _lib.moe_outputs_t()
+    # null pointers everywhere: rejected on the host, nothing launched
+    assert _lib.moe_forward_ep(p, 2, inputs, outputs, None, 0, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_forward_ep(p, 3, inputs, outputs, None, 0, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0
+
+
+# ---- 4-bit expert weights -------------------------------------------------------
+
+@pytest.mark.parametrize("over,expect", [
+    ({}, _lib.MOE_OK),
+    ({"d": 192}, _lib.MOE_ERR_UNSUPPORTED),                  # d_model not a multiple of the group
+    ({"F": 320}, _lib.MOE_ERR_UNSUPPORTED),                  # d_ff not a multiple of the group
+    ({"dtype": "f32"}, _lib.MOE_ERR_UNSUPPORTED),
+    ({"S": 2}, _lib.MOE_ERR_UNSUPPORTED),                    # shared experts
+])
+def test_int4_weight_combinations(over, expect):
+    kw = dict(T=64, d=256, E=8, k=2, F=512, weights="int4")
+    kw.update(over)
+    cfg = config("mixtral", **kw)
+    assert _lib.moe_workspace_size(make_params(cfg))[0] == expect
+
+
+def test_int4_training_unsupported():
+    cfg = config("mixtral", T=64, d=256, E=8, k=2, F=512, weights="int4")
+    assert _lib.moe_workspace_size(make_params(cfg, flags=_lib.MOE_FLAG_TRAINING))[0] == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_quantize_int4_rejects_bad_arguments():
+    n0 = _lib.moe_kernel_launches()
+    assert _lib.moe_quantize_int4(16, _lib.MOE_BF16, 4, 100, 16, 16, None) == _lib.MOE_ERR_INVALID_ARG  # cols % 128
+    assert _lib.moe_quantize_int4(None, _lib.MOE_BF16, 4, 128, 16, 16, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_quantize_int4(16, 7, 4, 128, 16, 16, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_quantize_int4(16, _lib.MOE_BF16, 0, 128, 16, 16, None) == _lib.MOE_OK  # nothing to do
     assert _lib.moe_kernel_launches() == n0

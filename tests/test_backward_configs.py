@@ -81,3 +81,68 @@ def test_full_size_backward(name):
         for k in ("dW1", "dW2", "dW3"):
             if ref[k] is not None:
                 assert rel_frobenius(grads[k][e].double().cpu().numpy(), ref[k][e]) <= 2e-2, k
+
+
+# Weight gradients at the full layer widths against the oracle.  The device backward
+# runs on a token subset of the full-size inputs (the full weights), so that every
+# expert holds few enough tokens for the oracle to compute its whole gradient in fp64.
+# An expert's weight gradients depend only on the tokens routed to it: they equal
+# those of a one-expert layer whose only expert is e, fed those tokens with
+# dL/d(expert output) = gate * dy (a layer whose router gives gate 1).
+SUB_T = {"mixtral": 128, "deepseek": 256}
+
+
+def _expert_grads_oracle(cfg, cpu, e, tokens, gates, dy):
+    t = torch.as_tensor(tokens, dtype=torch.long)
+    n = len(tokens)
+    one = lambda k: None if cpu.get(k) is None else cpu[k][e:e + 1]  # noqa: E731
+    dyg = (torch.as_tensor(gates, dtype=torch.float64)[:, None] * dy[t].double()).numpy()
+    ref = orc.backward(cpu["x"][t], torch.zeros(1, cfg.d), None, one("W1"), one("W3"), one("W2"), None, None,
+                       idx=np.zeros((n, 1), np.int32), dropped=np.zeros((n, 1), np.uint8), dy=dyg, d_aux=0.0,
+                       E=1, S=0, act_name=cfg.act, renormalize=False, residual_mode=0)
+    return {k: (None if ref[k] is None else ref[k][0]) for k in ("dW1", "dW3", "dW2")}
+
+
+@pytest.mark.parametrize("name", ["mixtral", "deepseek"])
+def test_full_width_expert_gradients_on_a_token_subset(name):
+    full = config(name)
+    cfg = config(name, T=SUB_T[name])
+    inp = make_inputs(full, 0, device="cuda")
+    rng = np.random.default_rng(13)
+    tokens = np.sort(rng.choice(full.T, size=cfg.T, replace=False))
+    sub = dict(inp)
+    sub["x"] = inp["x"][torch.as_tensor(tokens, device="cuda")].contiguous()
+    g = torch.Generator(device="cuda").manual_seed(6)
+    dy = torch.randn(cfg.T, cfg.d, generator=g, device="cuda").to(cfg.torch_dtype)
+    layer = MoELayer(cfg, sub, flags=TRAIN)
+    layer.run()
+    grads = {k: (None if v is None else v.cpu()) for k, v in layer.backward(dy, 0.37).items()}
+    torch.cuda.synchronize()
+    assert layer.device_status() == _lib.MOE_OK
+    out = to_cpu(layer.out)
+    cpu = to_cpu(sub)
+    del inp, sub
+    dy_cpu = dy.cpu()
+    idx, drop = out["expert_idx"].numpy(), out["dropped"].numpy().astype(bool)
+    gates = out["gates"].numpy()
+    counts = np.bincount(idx[~drop], minlength=cfg.E)
+    touched = np.nonzero(counts)[0]
+    # routed experts: the least and the most loaded (all of them for the fine-grained layer)
+    check = touched if cfg.E > 8 else [touched[np.argmin(counts[touched])], touched[np.argmax(counts[touched])]]
+    for e in check:
+        hit = (idx == e) & ~drop
+        tok_e = np.nonzero(hit.any(axis=1))[0]
+        ref = _expert_grads_oracle(cfg, cpu, int(e), tok_e, gates[hit], dy_cpu)
+        for k in ("dW1", "dW3", "dW2"):
+            if ref[k] is not None:
+                err = rel_frobenius(grads[k][e].double().numpy(), ref[k])
+                assert err <= 2e-2, (int(e), k, err)
+    # untouched experts get exactly zero
+    for e in np.nonzero(counts == 0)[0]:
+        assert not grads["dW2"][e].any() and not grads["dW1"][e].any()
+    # shared experts: every token, gate 1
+    for s in range(cfg.S):
+        ref = _expert_grads_oracle(cfg, cpu, cfg.E + s, np.arange(cfg.T), np.ones(cfg.T), dy_cpu)
+        for k in ("dW1", "dW3", "dW2"):
+            err = rel_frobenius(grads[k][cfg.E + s].double().numpy(), ref[k])
+            assert err <= 2e-2, ("shared", s, k, err)
