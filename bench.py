@@ -67,6 +67,8 @@ def parse_args():
                     help="run the layer expert-parallel over this many ranks emulated on the GPU")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step instead: moe_forward + moe_backward")
+    ap.add_argument("--split-router-per-call", action="store_true",
+                    help="split the router weights on every call instead of once per weight update")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each stage directly instead of replaying a captured CUDA graph")
     return ap.parse_args()
@@ -340,12 +342,13 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- GPU arm
 
-def algorithmic_gemm_work(cfg, out):
+def algorithmic_gemm_work(cfg, out, direct=False):
     """Bytes and flops the grouped-GEMM stage must move/do for this batch.
 
     Bytes: weights of every expert that received >= 1 kept row (W1, W3, W2), the
     permuted activations read once, the hidden activations written and read once,
-    the expert outputs written once (shared experts: all T rows).  Flops: 2 per
+    the expert outputs written once (shared experts: all T rows; with the combine
+    finished in the stage, the kept rows of y plus their token and gate).  Flops: 2 per
     multiply-add on kept rows only."""
     import torch
     kept = (out["dropped"] == 0)
@@ -364,14 +367,24 @@ def algorithmic_gemm_work(cfg, out):
         w_bytes = touched * nmat * cfg.d * cfg.F * esz
     srows = cfg.S * cfg.T
     act_bytes = (rows * (cfg.d + 2 * cfg.F + cfg.d) + cfg.T * cfg.d * (1 if cfg.S else 0)
-                 + srows * (2 * cfg.F + cfg.d)) * esz
+                 + srows * (2 * cfg.F + cfg.d)) * esz + (rows * 8 if direct else 0)
     flops = cfg.expert_flops(rows)
     return {"bytes": w_bytes + act_bytes, "weight_bytes": w_bytes, "flops": flops,
             "kept_rows": rows, "touched_experts": touched}
 
 
-def stage_bytes(cfg, out, gemm):
-    """Minimum HBM bytes of the memory-bound stages (router, dispatch, combine)."""
+def direct_combine(cfg, args) -> bool:
+    """True when the library finishes the combine inside the expert stage: a top-1 bf16
+    layer on the fused tensor-core kernel without shared experts or the residual on every
+    token (the GEMM2 epilogue writes y, the dispatch copies the dropped tokens)."""
+    return (cfg.k == 1 and cfg.S == 0 and cfg.residual_mode == 0 and cfg.dtype == "bf16"
+            and cfg.weights == "dtype" and not getattr(args, "ep", None) and not getattr(args, "backward", False))
+
+
+def stage_bytes(cfg, out, gemm, direct=False):
+    """Minimum HBM bytes of the memory-bound stages (router, dispatch, combine).  With the
+    combine finished in the expert stage, the combine moves nothing and the dispatch also
+    copies the dropped tokens' rows into y."""
     esz = 2 if cfg.dtype == "bf16" else 4
     T, d, k, E = cfg.T, cfg.d, cfg.k, cfg.E
     rows = gemm["kept_rows"]
@@ -380,6 +393,9 @@ def stage_bytes(cfg, out, gemm):
         router += E * d * 4 + T * E * 4  # W_noise and the normal draws
     dispatch = T * k * 4 + rows * d * esz * 2 + T * k * (1 + 4 + 4)
     pass_tok = int((out["dropped"].bool().all(dim=1)).sum()) if cfg.residual_mode == 0 else T
+    if direct:
+        dispatch += 2 * pass_tok * d * esz + rows * 8
+        return {"moe_router": router, "moe_dispatch": dispatch, "moe_combine": 0}
     combine = rows * d * esz + T * d * esz + pass_tok * d * esz + T * k * 8 + \
         (T * d * esz if cfg.S else 0)
     return {"moe_router": router, "moe_dispatch": dispatch, "moe_combine": combine}
@@ -418,7 +434,9 @@ def run_gpu(args):
     if cfg.weights in ("int8", "int4"):
         from sparse_mixture_experts_scan_b300 import quantize_expert_weights
         inp = quantize_expert_weights(inp, bits=8 if cfg.weights == "int8" else 4)
-    layer = MoELayer(cfg, inp, device=dev, ep_ranks=args.ep)
+    # bf16 layers: the router weights' three-term split is made once, as after a weight update
+    prepared = cfg.dtype == "bf16" and not args.split_router_per_call
+    layer = MoELayer(cfg, inp, device=dev, ep_ranks=args.ep, prepared_router=prepared)
     stream = torch.cuda.current_stream(dev)
     # an expert-parallel layer runs only the whole forward: its stage pass is that one call
     stages = ["moe_forward"] if args.ep else ["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"]
@@ -528,8 +546,9 @@ def run_gpu(args):
     value = replica_throughput(world, cfg.T, ms_step)
 
     out = layer.out
-    gemm = algorithmic_gemm_work(cfg, out)
-    sbytes = stage_bytes(cfg, out, gemm)
+    direct = direct_combine(cfg, args)
+    gemm = algorithmic_gemm_work(cfg, out, direct)
+    sbytes = stage_bytes(cfg, out, gemm, direct)
     pk = peaks()
     g_ms = stage_ms.get("moe_grouped_gemm", ms_step)
     hbm_bound = gemm["bytes"] == 0 or \
@@ -598,7 +617,7 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
-        layers = [layer, MoELayer(cfg, dict(inp), device=dev, ep_ranks=args.ep)]
+        layers = [layer, MoELayer(cfg, dict(inp), device=dev, ep_ranks=args.ep, prepared_router=prepared)]
         x_dev = [inp["x"].clone() for _ in layers]  # valid data before the first forward
         for L, xd in zip(layers, x_dev):
             L.set_x(xd)
@@ -694,6 +713,8 @@ def run_gpu(args):
         "data": "synthetic (seeded; shapes and distributions of the workload; random-init weights)",
         "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)",
+                   "router_weights": ("split into three bf16 terms once (moe_prepare_router_weights), as "
+                                      "after a weight update" if prepared else "split on every call"),
                    "parallelism": (f"replicas x{world}" if world > 1 else "single GPU")
                    + (f"; expert parallel over {args.ep} ranks emulated on each GPU" if args.ep else ""),
                    "launch": ("direct C-ABI calls" if args.no_graph else

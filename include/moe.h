@@ -153,6 +153,11 @@ typedef struct {
                                weight_format != MOE_WEIGHTS_DTYPE, else NULL */
     const float* W3_scale;  /* the same shape; iff quantised and SwiGLU */
     const float* W2_scale;  /* INT8: [E, d]; INT4: [E, d, F / MOE_INT4_GROUP]; iff quantised */
+    const void* router_weights; /* the router weights as moe_prepare_router_weights made them from
+                                   W_gate (and W_noise) for these params, or NULL: the router then
+                                   makes them in the workspace on every call.  Only for layers
+                                   whose router runs on the tensor core (bf16, no
+                                   MOE_FLAG_FFMA_ROUTER); otherwise it must be NULL */
 } moe_inputs_t;
 
 typedef struct {
@@ -169,6 +174,21 @@ typedef struct {
     int32_t* perm_row;   /* [T, k] row of the slot in the expert-contiguous, token-ascending,
                             unpadded order of kept slots; -1 if dropped; or NULL */
 } moe_outputs_t;
+
+/* Router weights prepared once per weight update.  The tensor-core router of bf16
+ * layers multiplies x by W_gate split exactly into three bf16 terms
+ * (W = hi + mid + lo; [Switch] §"选择性精度" asks for an fp32 router); by default
+ * every call makes that split in its workspace (one small kernel).  A caller whose
+ * router weights change only at weight updates can make it once:
+ * moe_router_weights_size gives the bytes (it depends on E, d_model and
+ * noisy_gating only), moe_prepare_router_weights writes the split of W_gate (and,
+ * with noisy gating, of W_noise) into a caller-owned, 16-byte aligned device
+ * buffer on `stream`, and moe_inputs_t.router_weights points the layer at it.  The
+ * buffer is valid for any T.  Layers whose router runs on CUDA cores (fp32, or
+ * MOE_FLAG_FFMA_ROUTER) return MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_router_weights_size(const moe_params_t* params, size_t* bytes);
+moe_status_t moe_prepare_router_weights(const moe_params_t* params, const float* W_gate, const float* W_noise,
+                                        void* prepared, size_t prepared_bytes, void* stream);
 
 /* Bytes of device workspace moe_forward needs for these params.  Depends only
  * on the params.  The workspace must be 256-byte aligned and must be zeroed

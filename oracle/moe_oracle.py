@@ -494,6 +494,25 @@ def expert_apply(x, W1, W3, W2, b1, b2, tokens, experts, *, act_name: str) -> np
     return out
 
 
+def combine_rows(x, gates, dropped, row_of, o, *, S: int = 0, ys=None, residual_mode: int = 0,
+                 tokens=None) -> np.ndarray:
+    """The combine for the listed tokens: sum over kept slots (slot order) of
+    gates[t,j] * o[row_of[t,j]] + the shared outputs ys [S, T, d] + pass(t) x[t]."""
+    xa, xc = _as_array(x)
+    T, d = xa.shape
+    ga = np.ascontiguousarray(np.asarray(gates, dtype=np.float64))
+    k = ga.shape[1]
+    da = np.ascontiguousarray(np.asarray(dropped, dtype=np.uint8))
+    ra = _i32(row_of)
+    oa = np.ascontiguousarray(np.asarray(o, dtype=np.float64))
+    tok = np.arange(T, dtype=np.int32) if tokens is None else _i32(tokens)
+    ysa = None if ys is None else np.ascontiguousarray(np.asarray(ys, dtype=np.float64))
+    y = np.empty((tok.shape[0], d), dtype=np.float64)
+    _lib().orc_ep_combine(T, d, k, S, int(residual_mode), _ptr(xa), xc, _ptr(ga), _ptr(da), _ptr(ra), _ptr(oa),
+                          _ptr(ysa) if ysa is not None else None, tok.shape[0], _ptr(tok), _ptr(y))
+    return y
+
+
 def ep_aux(counts_rank, probs, k: int) -> float:
     ca = _i32(counts_rank)
     pa = np.ascontiguousarray(np.asarray(probs, dtype=np.float64))

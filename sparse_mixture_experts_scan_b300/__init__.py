@@ -10,7 +10,8 @@ CUDA library
 """
 from ._lib import (moe_backward, moe_combine, moe_dispatch, moe_ep_workspace_size, moe_forward, moe_forward_ep,
                    moe_grouped_gemm, moe_kernel_launches, moe_last_device_status, moe_quantize_int4,
-                   moe_quantize_int8, moe_router, moe_status_string, moe_workspace_size)
+                   moe_quantize_int8, moe_prepare_router_weights, moe_router, moe_router_weights_size,
+                   moe_status_string, moe_workspace_size)
 from .inputs import CONFIGS, LayerConfig, config, make_inputs
 from .layer import (MoEError, MoELayer, check, forward, make_params, quantize_expert_weights, quantize_int4,
                     quantize_int8)
@@ -19,6 +20,7 @@ __all__ = [
     "moe_forward", "moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine",
     "moe_workspace_size", "moe_last_device_status", "moe_status_string", "moe_backward",
     "moe_quantize_int8", "moe_quantize_int4", "moe_kernel_launches", "moe_forward_ep", "moe_ep_workspace_size",
+    "moe_router_weights_size", "moe_prepare_router_weights",
     "quantize_int8", "quantize_int4", "quantize_expert_weights",
     "CONFIGS", "LayerConfig", "config", "make_inputs", "MoEError", "MoELayer", "check",
     "forward", "make_params",

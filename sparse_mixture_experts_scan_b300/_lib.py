@@ -45,7 +45,8 @@ class moe_params_t(ctypes.Structure):
 class moe_inputs_t(ctypes.Structure):
     _fields_ = [("x", _vp), ("W_gate", _vp), ("b_gate", _vp), ("W1", _vp), ("W3", _vp),
                 ("W2", _vp), ("b1", _vp), ("b2", _vp), ("W_noise", _vp), ("b_noise", _vp),
-                ("noise_eps", _vp), ("W1_scale", _vp), ("W3_scale", _vp), ("W2_scale", _vp)]
+                ("noise_eps", _vp), ("W1_scale", _vp), ("W3_scale", _vp), ("W2_scale", _vp),
+                ("router_weights", _vp)]
 
 
 class moe_outputs_t(ctypes.Structure):
@@ -101,6 +102,10 @@ def load(build_if_stale: bool = True):
     L.moe_check_bounded_wait.argtypes = [_vp, ctypes.c_size_t, _u32, _vp]
     L.moe_kernel_launches.restype = ctypes.c_uint64
     L.moe_kernel_launches.argtypes = []
+    L.moe_router_weights_size.restype = _i32
+    L.moe_router_weights_size.argtypes = [_P(moe_params_t), _P(ctypes.c_size_t)]
+    L.moe_prepare_router_weights.restype = _i32
+    L.moe_prepare_router_weights.argtypes = [_P(moe_params_t), _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.moe_ep_workspace_size.restype = _i32
     L.moe_ep_workspace_size.argtypes = [_P(moe_params_t), _i32, _P(ctypes.c_size_t)]
     L.moe_forward_ep.restype = _i32
@@ -158,6 +163,17 @@ def moe_backward(params, inputs, outputs, dy, d_aux, grads, workspace, workspace
     return load().moe_backward(ctypes.byref(params), ctypes.byref(inputs), ctypes.byref(outputs), _vp(dy),
                                _f32(d_aux), ctypes.byref(grads), _vp(workspace),
                                ctypes.c_size_t(workspace_bytes), _vp(stream))
+
+
+def moe_router_weights_size(params: moe_params_t):
+    n = ctypes.c_size_t(0)
+    st = load().moe_router_weights_size(ctypes.byref(params), ctypes.byref(n))
+    return st, n.value
+
+
+def moe_prepare_router_weights(params, W_gate, W_noise, prepared, prepared_bytes, stream):
+    return load().moe_prepare_router_weights(ctypes.byref(params), _vp(W_gate), _vp(W_noise), _vp(prepared),
+                                             ctypes.c_size_t(prepared_bytes), _vp(stream))
 
 
 def moe_ep_workspace_size(params: moe_params_t, G: int):

@@ -106,12 +106,15 @@ Layout make_layout(const moe_params_t& p)
         o = align_up(o + bytes, kRegionAlign);
         return at;
     };
-    L.off_wsplit = take(L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
+    const size_t split_bytes = 3 * sizeof(uint16_t) * (size_t)router_split_rows(L.E) * L.d;
+    L.off_wsplit = take(L.tc_router ? split_bytes : 0);
     L.off_logits = take(sizeof(float) * (size_t)L.T * L.E * (L.r_ksplits > 1 ? L.r_ksplits + 1 : 1));
     const bool noisy = p.noisy_gating == 1;
-    L.off_nsplit = take(noisy && L.tc_router ? 3 * sizeof(uint16_t) * (size_t)L.e_pad * L.d : 0);
+    L.off_nsplit = take(noisy && L.tc_router ? split_bytes : 0);
     L.off_nlogits = take(noisy ? sizeof(float) * (size_t)L.T * L.E * L.r_ksplits : 0);
-    L.ffn_sync_n = 2 + L.rows_cap / kSegRows;
+    // fused experts' scheduler words: tile counter, finished CTAs, one counter per routed
+    // M-tile and, with shared experts, one per shared M-tile
+    L.ffn_sync_n = 2 + L.rows_cap / kSegRows + (L.S > 0 ? L.t_pad / kSegRows : 0);
     L.off_ffn_sync = take(sizeof(unsigned) * L.ffn_sync_n);
     L.off_psum = take(sizeof(float) * L.n_rblk * L.E);
     L.off_psum_chunk = take(sizeof(float) * (size_t)L.nchunks * L.E);
@@ -126,6 +129,8 @@ Layout make_layout(const moe_params_t& p)
     L.off_xp = take(L.esz * (size_t)L.rows_cap * L.d);
     L.off_h = take(L.esz * (size_t)L.rows_cap * L.F);
     L.off_yp = take(L.esz * (size_t)L.rows_cap * L.d);
+    L.off_row_token = take(sizeof(int32_t) * (size_t)L.rows_cap);
+    L.off_row_gate = take(sizeof(float) * (size_t)L.rows_cap);
     L.off_hs = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.S * L.F : 0);
     L.off_ys = take(L.S > 0 ? L.esz * (size_t)L.t_pad * L.d : 0);
     const bool train = (p.flags & MOE_FLAG_TRAINING) != 0u;
@@ -171,7 +176,9 @@ moe_status_t validate_io(const moe_params_t& p, const moe_inputs_t* in, const mo
     if (p.weight_format != MOE_WEIGHTS_DTYPE ? (!in->W1_scale || !in->W2_scale || (swiglu != (in->W3_scale != nullptr)))
                                             : (in->W1_scale || in->W3_scale || in->W2_scale))
         return MOE_ERR_INVALID_ARG;
-    const void* ptrs[] = {in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
+    const bool tc_router = p.dtype == MOE_BF16 && !(p.flags & MOE_FLAG_FFMA_ROUTER);
+    if (in->router_weights && !tc_router) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {in->router_weights, in->x, in->W_gate, in->b_gate, in->W1, in->W3, in->W2, in->b1, in->b2,
                           out->y, out->expert_idx, out->gates, out->counts, out->dropped, out->aux,
                           out->logits, out->probs, out->perm_row, in->W_noise, in->b_noise, in->noise_eps,
                           in->W1_scale, in->W3_scale, in->W2_scale};
@@ -292,11 +299,15 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     c.fused = c.use_tc && !(c.p.flags & MOE_FLAG_UNFUSED_EXPERTS);
     if (c.L.tc_router) {
         const Layout& L = c.L;
-        if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) ||
-            !encode_bf16_2d(&c.mW, c.at<void>(L.off_wsplit), 3ull * L.e_pad, L.d, 3 * L.r_bn))
+        // the split router weights: the caller's prepared buffer (gate, then noise) or the workspace
+        const uint64_t srows = 3ull * router_split_rows(L.E);
+        const size_t sbytes = 2 * srows * (size_t)L.d;
+        const void* wsplit = in->router_weights ? in->router_weights : c.at<void>(L.off_wsplit);
+        const void* nsplit = in->router_weights ? static_cast<const char*>(in->router_weights) + sbytes
+                                                : c.at<void>(L.off_nsplit);
+        if (!encode_bf16_2d(&c.mX, in->x, L.T, L.d, 128) || !encode_bf16_2d(&c.mW, wsplit, srows, L.d, 3 * L.r_bn))
             return MOE_ERR_UNSUPPORTED;
-        if (c.p.noisy_gating == 1 &&
-            !encode_bf16_2d(&c.mWn, c.at<void>(L.off_nsplit), 3ull * L.e_pad, L.d, 3 * L.r_bn))
+        if (c.p.noisy_gating == 1 && !encode_bf16_2d(&c.mWn, nsplit, srows, L.d, 3 * L.r_bn))
             return MOE_ERR_UNSUPPORTED;
     }
     // quantised expert weights: the transposed tensor-memory kernel (k_grouped_gemm_wq) for
@@ -311,11 +322,14 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.wq) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
-        const long long bound = L.C >= 0 ? std::min(L.C, L.T) : L.T;
+        // token rows per tile: what an expert holds on average (capped by the capacity)
+        const long long avg = ((long long)L.T * L.k + L.E - 1) / L.E;
+        const long long est = L.C >= 0 ? std::min<long long>(L.C, avg) : avg;
         c.wq_bits = c.p.weight_format == MOE_WEIGHTS_INT4 ? 4 : 8;
-        c.wq_nt = gemm_wq_tokens_tile((int)std::min<long long>(bound, 1 << 30), gated);
-        const uint32_t kb_bytes = c.wq_bits == 8 ? 64 : 32;  // bytes of one 64-column K block
-        const CUtensorMapSwizzle swz = c.wq_bits == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+        c.wq_nt = gemm_wq_tokens_tile((int)std::min<long long>(est, 1 << 30), gated);
+        // one stage reads 128 bytes of each weight row (128 int8 or 256 int4 values)
+        const uint32_t kb_bytes = 128;
+        const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
         const uint64_t dcols = (uint64_t)L.d * c.wq_bits / 8, fcols = (uint64_t)L.F * c.wq_bits / 8;
         bool ok = encode_u8_2d_swizzled(&c.mQ1, in->W1, (uint64_t)L.E * L.F, dcols, kb_bytes, 128, swz) &&
                   encode_u8_2d_swizzled(&c.mQ3, gated ? in->W3 : in->W1, (uint64_t)L.E * L.F, dcols, kb_bytes, 128,
@@ -344,6 +358,12 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     } else if (c.use_tc) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
+        // a top-1 layer without shared experts or the residual on every token: each kept
+        // row is one token's whole routed output, so the fused kernel's GEMM2 epilogue
+        // scales it by the gate and writes y (the arithmetic k_combine would apply), and
+        // the dispatch copies the dropped tokens' x; training keeps Yp for the backward
+        c.direct_y = c.fused && c.p.k == 1 && L.S == 0 && c.p.residual_mode == 0 &&
+                     !(c.p.flags & MOE_FLAG_TRAINING);
         c.bn1 = c.fused || gated ? 256 : pick_bn(L.F);
         c.bn2 = c.fused ? 256 : pick_bn(L.d);
         const int b1_rows = gated ? c.bn1 / 2 : c.bn1;
@@ -430,17 +450,20 @@ moe_status_t stage_router(Ctx& c)
         g.psum_part = a.psum_part;
         g.scan_done = a.scan_done;
     }
-    cudaError_t e = launch_split_wgate(c.in->W_gate, c.L.E, c.L.e_pad, c.L.r_bn, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
-                                       take_pdl(c));
-    if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st);
+    const bool prepared = c.in->router_weights != nullptr;  // split once by the caller
+    cudaError_t e = prepared ? cudaSuccess
+                             : launch_split_wgate(c.in->W_gate, c.L.E, c.L.d, c.at<void>(c.L.off_wsplit), c.sms, c.st,
+                                                  take_pdl(c));
+    if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mW, g, c.L.r_bn, c.sms, c.st, take_pdl(c));
     if (noisy) {  // the same GEMM on W_noise, without bias, into the noise-logit partials
         RouterGemmArgs gn = g;
         gn.bg = nullptr;
         gn.logits = c.at<float>(c.L.off_nlogits);
         if (e == cudaSuccess)
-            e = launch_split_wgate(c.in->W_noise, c.L.E, c.L.e_pad, c.L.r_bn, c.L.d, c.at<void>(c.L.off_nsplit), c.sms, c.st,
-                                   take_pdl(c));
-        if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mWn, gn, c.L.r_bn, c.sms, c.st);
+            e = prepared ? cudaSuccess
+                         : launch_split_wgate(c.in->W_noise, c.L.E, c.L.d, c.at<void>(c.L.off_nsplit), c.sms, c.st,
+                                              take_pdl(c));
+        if (e == cudaSuccess) e = launch_router_logits_tc(c.mX, c.mWn, gn, c.L.r_bn, c.sms, c.st, take_pdl(c));
     }
     if (e == cudaSuccess && !g.fuse) e = launch_router_topk(a, c.st);
     return cuda_status(e);
@@ -482,6 +505,11 @@ moe_status_t stage_dispatch(Ctx& c)
     a.slot_row = c.at<int32_t>(c.L.off_slot_row);
     a.ffn_sync = c.at<unsigned>(c.L.off_ffn_sync);
     a.ffn_sync_n = c.L.ffn_sync_n;
+    if (c.direct_y) {
+        a.row_token = c.at<int32_t>(c.L.off_row_token);
+        a.row_gate = c.at<float>(c.L.off_row_gate);
+        a.y_pass = c.out->y;
+    }
     return cuda_status(launch_dispatch(a, c.sms, c.st, take_pdl(c)));
 }
 
@@ -624,6 +652,9 @@ moe_status_t stage_gemm(Ctx& c)
         const int out1 = gated ? c.bn1 / 2 : c.bn1;
         g1.n_tiles = ceil_div(L.F, out1);
         g2.n_tiles = ceil_div(L.d, c.bn2);
+        // the shared experts join the fused kernel's tile list when their GEMM2 K blocks
+        // never straddle two experts (d_ff a multiple of 64)
+        const bool fold_shared = c.fused && L.S > 0 && mt_routed > 0 && gated && L.F % 64 == 0;
         if (mt_routed > 0 && c.fused) {
             FusedFfnArgs f{};
             f.mtile_off = g1.mtile_off;
@@ -652,9 +683,30 @@ moe_status_t stage_gemm(Ctx& c)
             f.mt_done = sync + 2;
             f.mt_max = L.ffn_sync_n - 2;
             f.err = c.err();
-            const CUtensorMap maps[5] = {c.mA1, c.mB1, c.mB3, c.mA2, c.mB2};
-            e = launch_ffn_fused_tc(maps, f, act1, grid_for(mt_routed * (g1.n_tiles + g2.n_tiles), 1), c.st,
-                                    take_pdl(c));
+            if (c.direct_y) {
+                f.y = c.out->y;
+                f.row_token = c.at<int32_t>(L.off_row_token);
+                f.row_gate = c.at<float>(L.off_row_gate);
+            }
+            int tiles = mt_routed * (g1.n_tiles + g2.n_tiles);
+            if (fold_shared) {
+                f.S = L.S;
+                f.shared_rows = L.T;
+                f.mt_s = mt_shared;
+                f.n_tiles_s1 = ceil_div(L.S * L.F, out1);
+                f.b1_row0 = L.E * L.F;
+                f.b2_group0 = L.E;
+                f.seg_k2 = L.F;
+                f.hs = s1.out;
+                f.ldhs = L.S * L.F;
+                f.ys = s2.out;
+                f.zs1 = s1.z1;
+                f.zs3 = s1.z3;
+                f.mt_s0 = L.rows_cap / kSegRows;
+                tiles += mt_shared * (f.n_tiles_s1 + g2.n_tiles);
+            }
+            const CUtensorMap maps[7] = {c.mA1, c.mB1, c.mB3, c.mA2, c.mB2, c.mAs1, c.mAs2};
+            e = launch_ffn_fused_tc(maps, f, act1, grid_for(tiles, 1), c.st, take_pdl(c));
         } else if (mt_routed > 0) {
             e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st,
                                take_pdl(c));
@@ -662,7 +714,7 @@ moe_status_t stage_gemm(Ctx& c)
                 e = launch_gemm_tc(c.mA2, c.mB2, c.mB2, g2, kActNone, c.bn2, grid_for(mt_routed * g2.n_tiles, 1),
                                    c.st, take_pdl(c));
         }
-        if (e == cudaSuccess && L.S > 0) {
+        if (e == cudaSuccess && L.S > 0 && !fold_shared) {
             s1.n_tiles = ceil_div(s1.N, out1);
             s2.n_tiles = ceil_div(L.d, c.bn2);
             e = launch_gemm_tc(c.mAs1, c.mB1, c.mB3, s1, act1, c.bn1, grid_for(mt_shared * s1.n_tiles, 1), c.st,
@@ -697,6 +749,7 @@ moe_status_t stage_gemm(Ctx& c)
 moe_status_t stage_combine(Ctx& c)
 {
     if (c.L.T == 0) return MOE_OK;
+    if (c.direct_y) return MOE_OK;  // the expert stage and the dispatch wrote y
     CombineArgs a{};
     a.yp = c.at<void>(c.L.off_yp);
     a.ys = c.L.S > 0 ? c.at<void>(c.L.off_ys) : nullptr;
@@ -1435,6 +1488,37 @@ moe_status_t moe_workspace_size(const moe_params_t* params, size_t* bytes)
     if (s != MOE_OK) return s;
     *bytes = make_layout(*params).total;
     return MOE_OK;
+}
+
+moe_status_t moe_router_weights_size(const moe_params_t* params, size_t* bytes)
+{
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = validate_params(params);
+    if (s != MOE_OK) return s;
+    if (params->dtype != MOE_BF16 || (params->flags & MOE_FLAG_FFMA_ROUTER)) return MOE_ERR_UNSUPPORTED;
+    *bytes = 3 * sizeof(uint16_t) * (size_t)router_split_rows(params->E) * params->d_model *
+             (params->noisy_gating == 1 ? 2 : 1);
+    return MOE_OK;
+}
+
+moe_status_t moe_prepare_router_weights(const moe_params_t* params, const float* W_gate, const float* W_noise,
+                                        void* prepared, size_t prepared_bytes, void* stream)
+{
+    size_t need = 0;
+    moe_status_t s = moe_router_weights_size(params, &need);
+    if (s != MOE_OK) return s;
+    if (W_gate == nullptr || prepared == nullptr || !aligned16(prepared) || !aligned16(W_gate) ||
+        (params->noisy_gating == 1) != (W_noise != nullptr) || (W_noise && !aligned16(W_noise)))
+        return MOE_ERR_INVALID_ARG;
+    if (prepared_bytes < need) return MOE_ERR_WORKSPACE;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_split_wgate(W_gate, params->E, params->d_model, prepared, sms, st, false);
+    if (e == cudaSuccess && W_noise != nullptr)
+        e = launch_split_wgate(W_noise, params->E, params->d_model, static_cast<char*>(prepared) + need / 2, sms, st,
+                               false);
+    return cuda_status(e);
 }
 
 moe_status_t moe_forward(const moe_params_t* params, const moe_inputs_t* inputs, moe_outputs_t* outputs,

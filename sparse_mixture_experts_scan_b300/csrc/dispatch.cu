@@ -118,6 +118,15 @@ __global__ void __launch_bounds__(1024) k_dispatch_scan(DispatchArgs a)
             const int ee = tid % E, p = tid / E;
             float acc = 0.0f;
             int r = r0 + p;
+            // up to 16 loads in flight per thread (one or two memory round trips for the
+            // few hundred rows a block sums), added in order
+            for (; r + 15 * P < r1; r += 16 * P) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = __ldcg(&a.psum_part[(size_t)(r + u * P) * E + ee]);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) acc += v[u];
+            }
             for (; r + 3 * P < r1; r += 4 * P) {
                 float v[4];
 #pragma unroll
@@ -247,11 +256,17 @@ __global__ void __launch_bounds__(256) k_permute(DispatchArgs a)
             a.dropped[s] = keep ? 0 : 1;
             if (a.perm_row) a.perm_row[s] = keep ? a.kept_off[e] + pos : -1;
             a.slot_row[s] = row;
+            if (keep && a.row_token) {
+                a.row_token[row] = t;
+                a.row_gate[row] = a.gates[s];
+            }
         }
-        if (!keep) continue;
+        // top-1 direct combine: a dropped token's output is its input (0 + x = x)
+        if (!keep && a.y_pass == nullptr) continue;
         const uint4* src =
             reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)t * a.row_bytes);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)row * a.row_bytes);
+        uint4* dst = keep ? reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)row * a.row_bytes)
+                          : reinterpret_cast<uint4*>(static_cast<char*>(a.y_pass) + (size_t)t * a.row_bytes);
         // up to four 16-byte vectors per lane in flight before any store
         for (int v = lane; v < nvec; v += 128) {
             uint4 r[4];

@@ -110,23 +110,56 @@ __global__ void __launch_bounds__(1024) k_ep_plan(EpArgs a)
     __shared__ int wsum[32][3];
     __shared__ int s_pad[kMaxExperts], s_mt[kMaxExperts];
     __shared__ double dsum[32];
+    __shared__ float s_part[1024];
     griddep_launch_dependents();
     griddep_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, E = a.E;
+    // probability sums: thread (e, p) adds the rows p, p + Pn, ... of every rank's
+    // partials of expert e (loads issued four at a time); the Pn slices are then added
+    // in a fixed order
+    const int Pn = 1024 / E;
+    if (tid < Pn * E) {
+        const int e = tid % E, p = tid / E;
+        float acc = 0.0f;
+        for (int r = 0; r < a.G; ++r) {
+            if (a.t0[r + 1] <= a.t0[r]) continue;  // an empty shard ran no dispatch
+            const float* src = a.psum_chunk[r];
+            const int nc = a.nchunks[r];
+            int c = p;
+            for (; c + 3 * Pn < nc; c += 4 * Pn) {
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldcg(&src[(size_t)(c + u * Pn) * E + e]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc += v[u];
+            }
+            for (; c < nc; c += Pn) acc += __ldcg(&src[(size_t)c * E + e]);
+        }
+        s_part[tid] = acc;
+    }
+    // kept and pre-drop counts of every rank (independent loads first)
+    int kk[kEpMaxRanks], cc[kEpMaxRanks];
     int tot = 0, cnt = 0;
     float P = 0.0f;
     if (tid < E) {
-        for (int r = 0; r < a.G; ++r) {
-            const bool has = a.t0[r + 1] > a.t0[r];  // an empty shard ran no dispatch
-            a.base[r * E + tid] = tot;
-            if (!has) continue;
-            tot += __ldcg(&a.kept[r][tid]);
-            cnt += __ldcg(&a.counts_rank[r * E + tid]);
-            for (int c = 0; c < a.nchunks[r]; ++c) P += __ldcg(&a.psum_chunk[r][(size_t)c * E + tid]);
+#pragma unroll
+        for (int r = 0; r < kEpMaxRanks; ++r) {
+            const bool has = r < a.G && a.t0[r + 1] > a.t0[r];
+            kk[r] = has ? __ldcg(&a.kept[r][tid]) : 0;
+            cc[r] = has ? __ldcg(&a.counts_rank[r * E + tid]) : 0;
+        }
+#pragma unroll
+        for (int r = 0; r < kEpMaxRanks; ++r) {
+            if (r < a.G) a.base[r * E + tid] = tot;
+            tot += kk[r];
+            cnt += cc[r];
         }
         a.tot[tid] = tot;
         a.counts[tid] = cnt;
     }
+    __syncthreads();
+    if (tid < E)
+        for (int p = 0; p < Pn; ++p) P += s_part[p * E + tid];
     const int tiles = ceil_div(tot, kSegRows);
     const int v3[3] = {tiles * kSegRows, tot, tiles};
     int ex[3];
@@ -382,6 +415,8 @@ extern "C" moe_status_t moe_forward_ep(const moe_params_t* params, int32_t G, co
         if (s != MOE_OK) return s;
         // every rank's bounded waits report to the first word of the caller's workspace
         ctx[r].err_word = at<uint32_t>(workspace, 0);
+        // the owners run the experts here, so every rank combines with k_combine
+        ctx[r].direct_y = false;
     }
     // the owners' expert kernels: tensor maps over the receive buffers and the
     // owner's slice of the expert weights

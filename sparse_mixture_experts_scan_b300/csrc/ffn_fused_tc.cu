@@ -23,6 +23,15 @@
 // Tile ids travel from the producer (which claims them) to the MMA issuer and the
 // epilogue through a 4-entry shared-memory ring guarded by mbarriers.  The last
 // CTA to finish resets the scheduler counters for the next launch.
+//
+// Shared experts ("MoE 混合专家模型串讲" §"共享专家隔离": always on, gate 1) join the
+// same tile list when present: one group of all T token rows read straight from
+// x, hidden S * d_ff (the S experts' W1 / W3 rows are consecutive, so their
+// concatenation is one wider SwiGLU), and a GEMM2 whose K = S * d_ff runs over the
+// S experts' W2 matrices in turn.  The list is
+//     [shared GEMM1][routed GEMM1][routed GEMM2][shared GEMM2],
+// so the shared rows keep the SMs busy while nothing else is ready and their GEMM2
+// tiles, last, never wait.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_tile.cuh"
@@ -78,11 +87,38 @@ __device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target,
     }
 }
 
+// GEMM2 epilogue of a top-1 layer that finishes the combine in place: the row's
+// expert output o = bf16(acc + b2) is what Yp would hold, and the token's output is
+// y = bf16(gate * o) -- exactly the arithmetic of the combine kernel for one kept
+// slot (an fp32 multiply-add from zero, one rounding).  Every thread of the warp
+// must call it (tcgen05.ld is warp-collective).
+template <int BN>
+__device__ __forceinline__ void epilogue_direct(uint32_t t_lane, __nv_bfloat16* yrow, bool row_ok, int n0, int N,
+                                                const __nv_bfloat16* bias, size_t bias_base, float gate)
+{
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t va[32];
+        tmem_ld_32cols(t_lane + c * 32, va);
+        tmem_ld_wait();
+        const int col0 = n0 + c * 32;
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float z = __uint_as_float(va[i]);
+            if (bias != nullptr && col0 + i < N) z += __bfloat162float(bias[bias_base + col0 + i]);
+            o[i] = fmaf(gate, __bfloat162float(__float2bfloat16_rn(z)), 0.0f);
+        }
+        if (row_ok) store_row32(yrow, col0, N, o);
+    }
+}
+
 template <int BN, int ACT1, bool SAVE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ffn_fused_tc(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
-                   const __grid_constant__ CUtensorMap tmB2, const FusedFfnArgs args)
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmAs1,
+                   const __grid_constant__ CUtensorMap tmAs2, const FusedFfnArgs args)
 {
     using C = FCfg<BN>;
     constexpr bool GATED = (ACT1 == kActSwiglu);
@@ -133,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATED) tma_prefetch_desc(&tmB3);
         tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB2);
+        if (args.S > 0) {
+            tma_prefetch_desc(&tmAs1);
+            tma_prefetch_desc(&tmAs2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -151,10 +191,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    const int total1 = s_mt[G] * args.n_tiles1;
-    const int total = total1 + s_mt[G] * args.n_tiles2;
+    // tile list: [shared GEMM1 | routed GEMM1 | routed GEMM2 | shared GEMM2]
+    const int ts1 = args.S > 0 ? args.mt_s * args.n_tiles_s1 : 0;
+    const int ts2 = args.S > 0 ? args.mt_s * args.n_tiles2 : 0;
+    const int o1 = ts1;                                   // first routed GEMM1 tile
+    const int total1 = o1 + s_mt[G] * args.n_tiles1;     // first routed GEMM2 tile
+    const int o2s = total1 + s_mt[G] * args.n_tiles2;     // first shared GEMM2 tile
+    const int total = o2s + ts2;
     const int nkb1 = ceil_div(args.K1, kBK);
     const int nkb2 = ceil_div(args.K2, kBK);
+    const int nkbs2 = args.S > 0 ? ceil_div(args.S * args.seg_k2, kBK) : 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -176,26 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ring[slot] = t;
                 mbar_arrive(&ring_full[slot]);
                 if (t < 0) break;
-                int m, n;
-                const bool second = t >= total1;
-                int g;
-                if (second) {
+                int m, n, g = 0;
+                // kind: 0 shared GEMM1, 1 routed GEMM1, 2 routed GEMM2, 3 shared GEMM2
+                const int kind = t < o1 ? 0 : t < total1 ? 1 : t < o2s ? 2 : 3;
+                if (kind == 0 || kind == 3) {
+                    const int ls = kind == 0 ? t : t - o2s;
+                    m = ls % args.mt_s;
+                    n = ls / args.mt_s;
+                } else if (kind == 2) {
                     tm2.locate(t - total1, s_mt, args.n_tiles2, m, n);
                     g = tm2.g;
-                    // H rows of this M-tile must be complete (all n_tiles1 GEMM1 tiles)
-                    if (!wait_counter(&args.mt_done[s_mt[g] + m], 4u * (unsigned)args.n_tiles1, abort_flag)) {
+                } else {
+                    tm1.locate(t - o1, s_mt, args.n_tiles1, m, n);
+                    g = tm1.g;
+                }
+                if (kind >= 2) {
+                    // H rows of this M-tile must be complete (all GEMM1 tiles of the M-tile)
+                    const unsigned* ctr = kind == 2 ? &args.mt_done[s_mt[g] + m] : &args.mt_done[args.mt_s0 + m];
+                    const unsigned need = 4u * (unsigned)(kind == 2 ? args.n_tiles1 : args.n_tiles_s1);
+                    if (!wait_counter(ctr, need, abort_flag)) {
                         ok = false;
                         break;
                     }
                     fence_proxy_async_global();
-                } else {
-                    tm1.locate(t, s_mt, args.n_tiles1, m, n);
-                    g = tm1.g;
                 }
-                const int a_row = s_roff[g] + m * kBM;
-                const int b_row = second ? g * args.b2_rows_per_group + n * BN
-                                         : g * args.b1_rows_per_group + n * OUT1;
-                const int nkb = second ? nkb2 : nkb1;
+                const int a_row = (kind == 1 || kind == 2) ? s_roff[g] + m * kBM : m * kBM;
+                const int b_row = kind == 2 ? g * args.b2_rows_per_group + n * BN
+                                  : kind == 1 ? g * args.b1_rows_per_group + n * OUT1
+                                  : kind == 0 ? args.b1_row0 + n * OUT1
+                                              : 0;  // shared GEMM2: per K segment below
+                const int nkb = kind == 2 ? nkb2 : kind == 3 ? nkbs2 : nkb1;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -205,16 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* dA = sA + stage * C::A_BYTES;
                     uint8_t* dB = sB + stage * C::B_BYTES;
                     // each TMA names its kernel-parameter tensor map directly
-                    if (second) {
+                    if (kind == 2) {
                         tma_load_2d(dA, &tmA2, &full[stage], kb * kBK, a_row, pol_act);
                         tma_load_2d(dB, &tmB2, &full[stage], kb * kBK, b_row, pol_w);
-                    } else if (GATED) {
-                        tma_load_2d(dA, &tmA1, &full[stage], kb * kBK, a_row, pol_act);
-                        tma_load_2d(dB, &tmB1, &full[stage], kb * kBK, b_row, pol_w);
-                        tma_load_2d(dB + C::B_BYTES / 2, &tmB3, &full[stage], kb * kBK, b_row, pol_w);
+                    } else if (kind == 3) {
+                        // K column kb * 64 of the concatenated hidden layer: expert seg, column kc
+                        const int seg = (kb * kBK) / args.seg_k2, kc = kb * kBK - seg * args.seg_k2;
+                        tma_load_2d(dA, &tmAs2, &full[stage], kb * kBK, a_row, pol_act);
+                        tma_load_2d(dB, &tmB2, &full[stage], kc, (args.b2_group0 + seg) * args.b2_rows_per_group + n * BN,
+                                    pol_w);
                     } else {
-                        tma_load_2d(dA, &tmA1, &full[stage], kb * kBK, a_row, pol_act);
+                        const CUtensorMap* mA = kind == 0 ? &tmAs1 : &tmA1;
+                        tma_load_2d(dA, mA, &full[stage], kb * kBK, a_row, pol_act);
                         tma_load_2d(dB, &tmB1, &full[stage], kb * kBK, b_row, pol_w);
+                        if (GATED) tma_load_2d(dB + C::B_BYTES / 2, &tmB3, &full[stage], kb * kBK, b_row, pol_w);
                     }
                     filled |= 1u << stage;
                     fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
@@ -246,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int t = ring[slot];
                 if (t < 0) break;
-                const int nkb = t >= total1 ? nkb2 : nkb1;
+                const int nkb = t < total1 ? nkb1 : t < o2s ? nkb2 : nkbs2;
                 const int acc = it & 1;
                 if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, abort_flag)) {
                     ok = false;
@@ -301,13 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int t = ring[slot];
             if (t < 0) break;
-            const bool second = t >= total1;
-            int m, n, g;
-            if (second) {
+            const int kind = t < o1 ? 0 : t < total1 ? 1 : t < o2s ? 2 : 3;
+            int m, n, g = 0;
+            if (kind == 0 || kind == 3) {
+                const int ls = kind == 0 ? t : t - o2s;
+                m = ls % args.mt_s;
+                n = ls / args.mt_s;
+            } else if (kind == 2) {
                 tm2.locate(t - total1, s_mt, args.n_tiles2, m, n);
                 g = tm2.g;
             } else {
-                tm1.locate(t, s_mt, args.n_tiles1, m, n);
+                tm1.locate(t - o1, s_mt, args.n_tiles1, m, n);
                 g = tm1.g;
             }
             const int acc = it & 1;
@@ -317,30 +381,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const int row = m * kBM + r_in_tile;
-            const bool row_ok = row < s_rows[g];
+            const bool shared = kind == 0 || kind == 3;
+            const bool row_ok = row < (shared ? args.shared_rows : s_rows[g]);
             const uint32_t t_lane = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            if (second) {
+            if (kind == 2 && args.y != nullptr) {
+                // top-1 direct combine: the row's token and gate from the dispatch
+                const int prow = s_roff[g] + (row_ok ? row : 0);
+                const int tok = args.row_token[prow];
+                const float gate = args.row_gate[prow];
+                __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(args.y) + (size_t)(row_ok ? tok : 0) * args.ldy;
+                epilogue_direct<BN>(t_lane, yrow, row_ok, n * BN, args.N2, bias2,
+                                    (size_t)g * args.b2_rows_per_group, gate);
+            } else if (kind == 2) {
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.yp) + (size_t)(s_roff[g] + row) * args.ldy;
                 epilogue_tile<BN, kActNone>(t_lane, orow, row_ok, n * BN, args.N2, bias2,
                                             (size_t)g * args.b2_rows_per_group, 1, args.b2_rows_per_group);
-            } else {
+            } else if (kind == 3) {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.ys) + (size_t)row * args.ldy;
+                epilogue_tile<BN, kActNone>(t_lane, orow, row_ok, n * BN, args.N2, nullptr, 0, 1, 0);
+            } else if (kind == 1) {
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.h) + (size_t)(s_roff[g] + row) * args.ldh;
                 const size_t zo = (size_t)(s_roff[g] + row) * args.ldh;
                 epilogue_tile<BN, ACT1, SAVE>(t_lane, orow, row_ok, n * OUT1, args.N1, bias1,
                                               (size_t)g * args.b1_rows_per_group, 1, args.b1_rows_per_group,
                                               SAVE ? static_cast<__nv_bfloat16*>(args.z1) + zo : nullptr,
                                               SAVE && GATED ? static_cast<__nv_bfloat16*>(args.z3) + zo : nullptr);
+            } else {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.hs) + (size_t)row * args.ldhs;
+                const size_t zo = (size_t)row * args.ldhs;
+                epilogue_tile<BN, ACT1, SAVE>(t_lane, orow, row_ok, n * OUT1, args.S * args.seg_k2, nullptr, 0, 1, 0,
+                                              SAVE ? static_cast<__nv_bfloat16*>(args.zs1) + zo : nullptr,
+                                              SAVE && GATED ? static_cast<__nv_bfloat16*>(args.zs3) + zo : nullptr);
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
-            if (!second) {
+            if (kind <= 1) {
                 // publish this warp's 32 H rows to the GEMM2 tiles that read them: each
                 // of the 4 epilogue warps adds 1, so an M-tile is complete at 4 * n_tiles1
                 fence_proxy_async_global();
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) red_release_gpu_add(&args.mt_done[s_mt[g] + m], 1u);
+                unsigned* ctr = kind == 1 ? &args.mt_done[s_mt[g] + m] : &args.mt_done[args.mt_s0 + m];
+                if (lane == 0) red_release_gpu_add(ctr, 1u);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ring_empty[slot]);
@@ -376,8 +459,11 @@ cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, c
     const size_t smem = FCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
+    // without shared experts the two shared-expert maps are never read: pass the first map
+    const CUtensorMap& s1 = a.S > 0 ? maps[5] : maps[0];
+    const CUtensorMap& s2 = a.S > 0 ? maps[6] : maps[0];
     return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, pdl, maps[0], maps[1], maps[2], maps[3],
-                         maps[4], a);
+                         maps[4], s1, s2, a);
 }
 
 }  // namespace

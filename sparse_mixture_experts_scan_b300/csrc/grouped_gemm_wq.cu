@@ -25,13 +25,21 @@
 // tokens: scale, bias and activation are per-thread scalars, and SwiGLU pairs
 // the W1 and W3 accumulators of the same row.
 //
-// Per CTA (one per SM, 384 threads):
-//   warp 0      TMA: token tile [NT x 64] bf16 and the weight tile(s) [128 x 64]
-//               (8-bit: 64-byte rows, 64-byte swizzle; 4-bit: 32-byte rows,
-//               32-byte swizzle) per stage;
+// Per CTA (one per SM, 512 threads):
+//   warp 0      TMA, per shared-memory stage of KS = 128 (8-bit) or 256 (4-bit) K
+//               values: the weight tile(s) [128 rows x 128 bytes] (128-byte swizzle:
+//               every row segment a copy fetches is 128 contiguous bytes of HBM) and
+//               the token tile as KS / 64 boxes [NT x 64] bf16;
 //   warp 1      TMEM allocation and tcgen05.mma (M = 128, N = NT, K = 16, A from TMEM);
-//   warps 4-7   converters (warp w writes TMEM lanes 32 (w % 4) .. + 31);
-//   warps 8-11  epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
+//   warps 4-11  converters, two per TMEM lane quarter (warp w writes lanes
+//               32 (w % 4) .. + 31): with SwiGLU one converts the W1 tile and the
+//               other the W3 tile, otherwise each converts one half of the K block;
+//   warps 12-15 epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
+// The shared-memory stages (S, as many as fit: they keep the weight stream's bytes
+// in flight) and the TMEM operand slots (NA of 64 K values each, as many as the
+// accumulators leave) are separate rings: a stage feeds KS / 64 slots; it is refilled
+// once the MMAs that read its token tile are done, a slot is rewritten once the MMAs
+// that read it are done.
 // Every wait is bounded, as in the other tcgen05 kernels.
 #include "common.cuh"
 #include "kernels.h"
@@ -42,25 +50,35 @@ namespace moe {
 namespace {
 
 constexpr int kBW = 128;  // weight rows per A tile (MMA M)
-constexpr int kBK = 64;   // reduction per stage
-constexpr int kThreads = 384;
+constexpr int kBK = 64;   // reduction per TMEM operand slot
+constexpr int kThreads = 512;
+constexpr int kConvWarps = 8;
 constexpr int kGroupCols = 128;  // 4-bit scale groups along K
-constexpr size_t kBarBytes = 256;
+constexpr size_t kBarBytes = 512;
 constexpr size_t kTableBytes = sizeof(int) * (3 * kMaxExperts + 2);
+constexpr size_t kSmemBudget = 200 * 1024;  // shared-memory stages
 
 template <int WBITS, bool GATED, int NT>
 struct Cfg {
-    static constexpr int kStages = GATED ? 4 : 6;
-    static constexpr int kNA = GATED ? 2 : 1;                    // A tiles per stage
-    static constexpr uint32_t kXBytes = NT * kBK * 2;            // token tile
-    static constexpr uint32_t kWRowBytes = kBK * WBITS / 8;      // 64 or 32
+    static_assert(NT % 32 == 0, "token tile");
+    static constexpr int kNA = GATED ? 2 : 1;                    // A tiles per K block
+    static constexpr int kKS = WBITS == 8 ? 128 : 256;           // K values per shared-memory stage
+    static constexpr int kSub = kKS / kBK;                       // TMEM slots per stage
+    static constexpr uint32_t kXBoxBytes = NT * kBK * 2;         // one [NT x 64] token box
+    static constexpr uint32_t kXBytes = kSub * kXBoxBytes;       // the stage's token tile
+    static constexpr uint32_t kWRowBytes = kKS * WBITS / 8;      // 128 bytes
     static constexpr uint32_t kWBytes = kNA * kBW * kWRowBytes;  // weight tile(s)
     static constexpr uint32_t kStageBytes = (kXBytes + kWBytes + 1023) / 1024 * 1024;
+    static constexpr int kStagesFit = (int)(kSmemBudget / kStageBytes);
+    static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;  // shared-memory stages
     static constexpr uint32_t kAccCols = kNA * NT;               // one accumulator set
-    static constexpr uint32_t kACols = kNA * 32;                 // TMEM A columns per stage
-    static constexpr uint32_t kACol0 = 2 * kAccCols;             // A region after the two accumulators
+    static constexpr uint32_t kACols = kNA * 32;                 // TMEM A columns per slot
+    static constexpr uint32_t kACol0 = 2 * kAccCols;             // A slots after the two accumulators
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kACol0 + kStages * kACols <= kTmemCols, "tensor memory budget");
+    static constexpr int kSlotsFit = (int)((kTmemCols - kACol0) / kACols);
+    static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;  // TMEM operand slots
+    static_assert(kSlots >= 2 && kStages >= 2, "pipeline depth");
+    static_assert(2 * (kStages + kSlots) + 5 <= (int)(kBarBytes / 8) - 2, "barrier space");
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kTableBytes;
 };
 
@@ -87,6 +105,17 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Each thread of the warp stores 16 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -143,14 +172,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool GATED = (ACT == kActSwiglu);
     using C = Cfg<WBITS, GATED, NT>;
     constexpr int S = C::kStages;
+    constexpr int NA = C::kSlots;
     constexpr uint32_t IDESC = idesc_bf16_f32(kBW, NT);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full_q = reinterpret_cast<uint64_t*>(base + (size_t)S * C::kStageBytes);
-    uint64_t* full_a = full_q + S;
-    uint64_t* empty = full_a + S;
-    uint64_t* tfull = empty + S;
+    uint64_t* full_q = reinterpret_cast<uint64_t*>(base + (size_t)S * C::kStageBytes);  // [S] stage landed
+    uint64_t* empty = full_q + S;                                                      // [S] stage consumed
+    uint64_t* full_a = empty + S;                                                      // [NA] slot written
+    uint64_t* a_empty = full_a + NA;                                                   // [NA] slot consumed
+    uint64_t* tfull = a_empty + NA;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -165,8 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_q[s], 1);
-            mbar_init(&full_a[s], 4);  // one arrival per converter warp
             mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < NA; ++a) {
+            mbar_init(&full_a[a], kConvWarps);  // one arrival per converter warp
+            mbar_init(&a_empty[a], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -218,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int n_tiles = args.n_tiles;
     const int total = s_toff[G] * n_tiles;
-    const int num_kb = ceil_div(args.K, kBK);
+    const int num_kb = ceil_div(args.K, C::kKS);  // shared-memory stages per tile
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -241,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* st = base + (size_t)stage * C::kStageBytes;
                     mbar_arrive_expect_tx(&full_q[stage], C::kXBytes + C::kWBytes);
-                    tma_load_2d(st, &tmX, &full_q[stage], kb * kBK, x_row, pol_act);
+#pragma unroll
+                    for (int u = 0; u < C::kSub; ++u)
+                        tma_load_2d(st + u * C::kXBoxBytes, &tmX, &full_q[stage], kb * C::kKS + u * kBK, x_row,
+                                    pol_act);
                     const int wc = kb * (int)C::kWRowBytes;  // byte column of the weight rows
                     tma_load_2d(st + C::kXBytes, &tmW, &full_q[stage], wc, w_row, pol_w);
                     if (GATED) tma_load_2d(st + C::kXBytes + kBW * C::kWRowBytes, &tmW3, &full_q[stage], wc, w_row, pol_w);
@@ -268,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int it = 0;
+            int slot = 0;
+            uint32_t sphase = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
                 const int acc = it & 1;
                 if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, abort_flag)) {
@@ -276,21 +315,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full_a[stage], phase, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t x0 = smem_u32(base + (size_t)stage * C::kStageBytes);
-                    const uint32_t a0 = tmem_base + C::kACol0 + stage * C::kACols;
+                for (int kb = 0; kb < num_kb && ok; ++kb) {
+                    const uint32_t xs = smem_u32(base + (size_t)stage * C::kStageBytes);
+                    for (int u = 0; u < C::kSub; ++u) {
+                        // the converters wrote this slot after the stage's TMA landed, so the
+                        // token tile of the stage is in shared memory too
+                        if (!mbar_wait(&full_a[slot], sphase, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t x0 = xs + u * C::kXBoxBytes;
+                        const uint32_t a0 = tmem_base + C::kACol0 + slot * C::kACols;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        const uint64_t bdesc = sdesc_kmajor_sw128(x0 + k * 32);
-                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-                        mma_bf16_ts(d_tmem, a0 + k * 8, bdesc, IDESC, accum);
-                        if (GATED) mma_bf16_ts(d_tmem + NT, a0 + 32 + k * 8, bdesc, IDESC, accum);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            const uint64_t bdesc = sdesc_kmajor_sw128(x0 + k * 32);
+                            const uint32_t accum = (kb | u | k) != 0 ? 1u : 0u;
+                            mma_bf16_ts(d_tmem, a0 + k * 8, bdesc, IDESC, accum);
+                            if (GATED) mma_bf16_ts(d_tmem + NT, a0 + 32 + k * 8, bdesc, IDESC, accum);
+                        }
+                        mma_commit(&a_empty[slot]);
+                        if (++slot == NA) {
+                            slot = 0;
+                            sphase ^= 1u;
+                        }
                     }
+                    if (!ok) break;
                     mma_commit(&empty[stage]);
                     if (++stage == S) {
                         stage = 0;
@@ -306,72 +356,88 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(drain);
             if (!mbar_wait_short(drain, 0)) atomicOr(args.err, kErrTimeoutDrain);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 4 + kConvWarps) {
         // ------------------------------------------------------------ converters
         const int q = warp & 3;
-        const int r = q * 32 + lane;  // this thread's weight row in the tile (its TMEM lane)
+        const int part = (warp - 4) >> 2;  // SwiGLU: the W1 / W3 tile; otherwise the K half
+        const int r = q * 32 + lane;       // this thread's weight row in the tile (its TMEM lane)
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        int stage = 0;
-        uint32_t phase = 0;
+        const int h = GATED ? part : 0;    // which weight tile of the stage
+        const int kh = GATED ? -1 : part;  // which K half (-1: both)
+        int stage = 0, slot = 0;
+        uint32_t phase = 0, sphase = 0;
         bool ok = true;
         WqTiles tm;
+        const float* __restrict__ scales = (GATED && part == 1) ? args.scale3 : args.scale;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             int mt, n;
             tm.locate(tile, s_toff, n_tiles, mt, n);
             const int w_row = tm.g * args.b_rows_per_group + n * kBW + r;  // global weight row
             const bool w_ok = n * kBW + r < args.N;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                float s1 = 0.0f, s3 = 0.0f;
-                if constexpr (WBITS == 4) {  // the group scales of this K-block (before the wait)
+            for (int kb = 0; kb < num_kb && ok; ++kb) {
+                // 4-bit: the group scales of the stage's two 128-column groups (before the waits)
+                float sc0 = 0.0f, sc1 = 0.0f;
+                if constexpr (WBITS == 4) {
                     const int ng = args.K / kGroupCols;
-                    const int grp = (kb * kBK) / kGroupCols;
+                    const int g0 = (kb * C::kKS) / kGroupCols;
                     if (w_ok) {
-                        s1 = __ldg(&args.scale[(size_t)w_row * ng + grp]);
-                        if (GATED) s3 = __ldg(&args.scale3[(size_t)w_row * ng + grp]);
+                        sc0 = __ldg(&scales[(size_t)w_row * ng + g0]);
+                        if (g0 + 1 < ng) sc1 = __ldg(&scales[(size_t)w_row * ng + g0 + 1]);
                     }
                 }
                 if (!mbar_wait(&full_q[stage], phase, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* wt = base + (size_t)stage * C::kStageBytes + C::kXBytes;
-#pragma unroll
-                for (int h = 0; h < C::kNA; ++h) {
-                    const uint8_t* row = wt + (size_t)(h * kBW + r) * C::kWRowBytes;
+                // this thread's 128-byte weight row; 16-byte chunk c sits at c ^ (r % 8)
+                const uint8_t* row = base + (size_t)stage * C::kStageBytes + C::kXBytes +
+                                     (size_t)(h * kBW + r) * C::kWRowBytes;
+                for (int u = 0; u < C::kSub; ++u) {
+                    if (!mbar_wait(&a_empty[slot], sphase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     uint32_t v[32];
-                    if constexpr (WBITS == 8) {
-                        // 64-byte rows, 64-byte swizzle: 16-byte chunk c at c ^ ((r >> 1) & 3)
+                    // 16-byte chunks of sub-block u (64 K values) that this thread converts
+                    constexpr int kChunks = WBITS == 8 ? 4 : 2;
+                    const int cbase = u * kChunks + (kh < 0 ? 0 : kh * (kChunks / 2));
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 1) & 3)) << 4));
-                            i8x4_to_bf16(u.x, v[c * 8 + 0], v[c * 8 + 1]);
-                            i8x4_to_bf16(u.y, v[c * 8 + 2], v[c * 8 + 3]);
-                            i8x4_to_bf16(u.z, v[c * 8 + 4], v[c * 8 + 5]);
-                            i8x4_to_bf16(u.w, v[c * 8 + 6], v[c * 8 + 7]);
-                        }
-                    } else {
-                        // 32-byte rows, 32-byte swizzle: 16-byte chunk c at c ^ ((r >> 2) & 1)
-                        const float sc = h == 0 ? s1 : s3;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 2) & 1)) << 4));
+                    for (int ci = 0; ci < (GATED ? kChunks : kChunks / 2); ++ci) {
+                        const int c = cbase + ci;
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+                        if constexpr (WBITS == 8) {
+                            i8x4_to_bf16(w.x, v[ci * 8 + 0], v[ci * 8 + 1]);
+                            i8x4_to_bf16(w.y, v[ci * 8 + 2], v[ci * 8 + 3]);
+                            i8x4_to_bf16(w.z, v[ci * 8 + 4], v[ci * 8 + 5]);
+                            i8x4_to_bf16(w.w, v[ci * 8 + 6], v[ci * 8 + 7]);
+                        } else {
+                            const float scu = (u * kBK) / kGroupCols == 0 ? sc0 : sc1;
                             uint32_t o[4];
-                            i4x8_to_bf16(u.x, sc, o);
-                            v[c * 16 + 0] = o[0], v[c * 16 + 1] = o[1], v[c * 16 + 2] = o[2], v[c * 16 + 3] = o[3];
-                            i4x8_to_bf16(u.y, sc, o);
-                            v[c * 16 + 4] = o[0], v[c * 16 + 5] = o[1], v[c * 16 + 6] = o[2], v[c * 16 + 7] = o[3];
-                            i4x8_to_bf16(u.z, sc, o);
-                            v[c * 16 + 8] = o[0], v[c * 16 + 9] = o[1], v[c * 16 + 10] = o[2], v[c * 16 + 11] = o[3];
-                            i4x8_to_bf16(u.w, sc, o);
-                            v[c * 16 + 12] = o[0], v[c * 16 + 13] = o[1], v[c * 16 + 14] = o[2], v[c * 16 + 15] = o[3];
+                            i4x8_to_bf16(w.x, scu, o);
+                            v[ci * 16 + 0] = o[0], v[ci * 16 + 1] = o[1], v[ci * 16 + 2] = o[2], v[ci * 16 + 3] = o[3];
+                            i4x8_to_bf16(w.y, scu, o);
+                            v[ci * 16 + 4] = o[0], v[ci * 16 + 5] = o[1], v[ci * 16 + 6] = o[2], v[ci * 16 + 7] = o[3];
+                            i4x8_to_bf16(w.z, scu, o);
+                            v[ci * 16 + 8] = o[0], v[ci * 16 + 9] = o[1], v[ci * 16 + 10] = o[2], v[ci * 16 + 11] = o[3];
+                            i4x8_to_bf16(w.w, scu, o);
+                            v[ci * 16 + 12] = o[0], v[ci * 16 + 13] = o[1], v[ci * 16 + 14] = o[2], v[ci * 16 + 15] = o[3];
                         }
                     }
-                    tmem_st_32cols(t_row + C::kACol0 + stage * C::kACols + h * 32, v);
+                    const uint32_t dst = t_row + C::kACol0 + slot * C::kACols + h * 32;
+                    if constexpr (GATED) {
+                        tmem_st_32cols(dst, v);  // the whole sub-block of one tile's row
+                    } else {
+                        tmem_st_16cols(dst + kh * 16, v);  // one K half of the sub-block
+                    }
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_a[slot]);
+                    if (++slot == NA) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
                 }
-                tmem_st_wait();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_a[stage]);
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
@@ -382,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicOr(args.err, kErrTimeoutProducer);
             *abort_flag = 1;
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 4 + kConvWarps) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int r = q * 32 + lane;
@@ -414,15 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int valid = min(NT, s_rows[tm.g] - m0);
             __nv_bfloat16* o = out + (size_t)(s_roff[tm.g] + m0) * args.ldo + col;
             const uint32_t t_lane = tmem_base + acc * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+            constexpr int CH = NT < 32 ? NT : 32;  // accumulator columns per load
 #pragma unroll 1
-            for (int c = 0; c < NT / 32; ++c) {
-                uint32_t va[32], vb[32];
-                tmem_ld_32cols(t_lane + c * 32, va);
-                if constexpr (GATED) tmem_ld_32cols(t_lane + NT + c * 32, vb);
+            for (int c = 0; c < NT / CH; ++c) {
+                uint32_t va[CH], vb[CH];
+                if constexpr (CH == 32) {
+                    tmem_ld_32cols(t_lane + c * CH, va);
+                    if constexpr (GATED) tmem_ld_32cols(t_lane + NT + c * CH, vb);
+                } else {
+                    tmem_ld_16cols(t_lane + c * CH, va);
+                    if constexpr (GATED) tmem_ld_16cols(t_lane + NT + c * CH, vb);
+                }
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int m = c * 32 + j;
+                for (int j = 0; j < CH; ++j) {
+                    const int m = c * CH + j;
                     float z = __uint_as_float(va[j]) * f1;
                     float y;
                     if constexpr (GATED) {
@@ -513,10 +585,10 @@ __global__ void __launch_bounds__(256) k_quantize_int4(const T* __restrict__ w, 
 
 }  // namespace
 
-int gemm_wq_tokens_tile(int max_rows_per_expert, bool gated)
+int gemm_wq_tokens_tile(int rows_per_expert, bool gated)
 {
-    if (max_rows_per_expert <= 32) return 32;
-    if (max_rows_per_expert <= 64 || gated) return 64;
+    if (rows_per_expert <= 32) return 32;
+    if (rows_per_expert <= 64 || gated) return 64;
     return 128;
 }
 

@@ -33,6 +33,7 @@ struct Layout {
     int ffn_sync_n;
     size_t off_psum, off_hist, off_base, off_rank, off_slot_row, off_kept, off_row_off,
         off_kept_off, off_mtile, off_xp, off_h, off_yp, off_hs, off_ys;
+    size_t off_row_token, off_row_gate;  // token and gate of each permuted row (top-1 direct combine)
     // backward (MOE_FLAG_TRAINING): gate and router gradients, the router's share of dx,
     // dYp (reused for dXp), pre-activations (overwritten in place by their gradients;
     // relu: dZ1 only), shared-expert pre-activations and input gradient
@@ -59,6 +60,8 @@ struct Ctx {
     bool q8 = false;              // int8 expert weights
     CUtensorMap mQ1, mQ3, mQ2;    // their uint8 maps
     bool routed_experts = true;   // stage_gemm runs the routed experts (false: shared experts only)
+    bool direct_y = false;        // top-1 layer: the fused kernel's GEMM2 epilogue writes y itself
+                                  // (and the dispatch copies dropped tokens), no combine launch
     bool wq = false;              // quantised weights on the tensor-memory kernel (k_grouped_gemm_wq)
     int wq_bits = 8, wq_nt = 128; // its weight bits and token rows per tile
     template <typename T>

@@ -67,10 +67,12 @@ struct RouterGemmArgs {
 };
 int router_tc_bn(int T, int E);  // experts per router GEMM tile (16..64; MMA N = 3x), ~128 CTAs
 int router_tc_ksplits(int T, int E, int d);  // K splits so that small batches still fill ~128 CTAs
-cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d, void* out, int sms,
-                               cudaStream_t st, bool pdl);
+// The three-term split of an [E, d] fp32 router weight, [router_split_rows(E) / 16][3][16][d]
+// bf16 (E rounded up to 64; rows >= E zero): independent of the batch size.
+int router_split_rows(int E);
+cudaError_t launch_split_wgate(const float* Wg, int E, int d, void* out, int sms, cudaStream_t st, bool pdl);
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
-                                    int bn, int sms, cudaStream_t st);
+                                    int bn, int sms, cudaStream_t st, bool pdl);
 
 // ---- stage 2: dispatch -----------------------------------------------------
 struct DispatchArgs {
@@ -101,6 +103,11 @@ struct DispatchArgs {
     int32_t* slot_row;    // [T, k] padded row of the slot or -1
     unsigned* ffn_sync;   // fused-FFN scheduler words cleared by the scan, or nullptr
     int ffn_sync_n;
+    // top-1 direct combine (or nullptr): the token and gate of each kept row, and y, into
+    // which the permute copies the x row of every dropped token
+    int32_t* row_token;
+    float* row_gate;
+    void* y_pass;
 };
 size_t dispatch_scan_smem(int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st, bool pdl);
@@ -138,8 +145,32 @@ struct FusedFfnArgs {
     unsigned* mt_done;     // [mt_max] epilogue-warp arrivals per M-tile (0 at launch)
     int mt_max;
     uint32_t* err;
+    // Shared experts in the same tile list (S > 0; SwiGLU, no bias): one group of
+    // shared_rows token rows read straight from x, hidden S * d_ff (the S experts'
+    // W1 / W3 rows are consecutive), GEMM2 over K = S * d_ff in segments of seg_k2
+    // columns, segment s reading W2 group b2_group0 + s.  Their GEMM1 tiles come first
+    // in the list, their GEMM2 tiles last.
+    int S;
+    int shared_rows;       // T
+    int mt_s;              // M-tiles of the shared group
+    int n_tiles_s1;        // GEMM1 column tiles of the shared hidden layer
+    int b1_row0;           // first W1 / W3 row of the shared experts (E * d_ff)
+    int b2_group0;         // first W2 group of the shared experts (E)
+    int seg_k2;            // d_ff, a multiple of 64
+    void* hs;              // [T_pad, S * d_ff]
+    int ldhs;
+    void* ys;              // [T_pad, d_model]
+    void* zs1;             // training: the shared pre-activations [T, S * d_ff], or nullptr
+    void* zs3;
+    int mt_s0;             // first mt_done counter of the shared M-tiles
+    // top-1 direct combine (y != nullptr): the GEMM2 epilogue writes
+    // y[row_token[r]] = gate * bf16(Yp row r) instead of Yp (ld = ldy)
+    void* y;
+    const int32_t* row_token;
+    const float* row_gate;
 };
-// maps: A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2); MMA N = 256.
+// maps: A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2), As1 (x), As2 (Hs) (the last
+// two are read only when S > 0; the array may then hold 5 maps); MMA N = 256.
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
                                 cudaStream_t st, bool pdl);
 
@@ -174,7 +205,7 @@ cudaError_t launch_quantize_int8(const void* w, bool bf16, long long rows, int c
 // and the token tile (NT rows) as B.  8-bit: per-row scales applied in the
 // epilogue; 4-bit: group scales (128 input columns) applied by the converters.
 // maps: X (bf16 [rows, K], box {64, NT}), W and W3 (uint8 [groups * rows, K bytes],
-// box {64 or 32 bytes, 128}, 64- or 32-byte swizzle).
+// box {128 bytes, 128 rows}, 128-byte swizzle).
 struct GroupedGemmWqArgs {
     const int* row_off;    // [G] padded segment starts of the token rows
     const int* rows;       // [G] token rows per group
@@ -188,8 +219,9 @@ struct GroupedGemmWqArgs {
     const float* scale3;   // SwiGLU: the W3 rows' scales
     uint32_t* err;
 };
-// Token rows per tile for a layer whose experts hold at most max_rows_per_expert rows.
-int gemm_wq_tokens_tile(int max_rows_per_expert, bool gated);
+// Token rows per tile (32, 64 or 128) for a layer whose experts hold about
+// rows_per_expert rows.
+int gemm_wq_tokens_tile(int rows_per_expert, bool gated);
 cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3,
                            const GroupedGemmWqArgs& a, int wbits, int act, int nt, int grid, cudaStream_t st,
                            bool pdl);

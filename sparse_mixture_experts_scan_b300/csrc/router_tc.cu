@@ -18,14 +18,18 @@
 // registers with round-to-nearest additions.  The error is then bounded by the
 // chunk length, independent of d, and comparable to an fp32 FFMA dot product.
 //
-// k_split_wgate writes the three terms tile by tile, [E_pad / BN][3][BN][d] bf16
-// (rows >= E zero), into the workspace.  k_router_logits_tc: persistent, one CTA
-// per SM, warp-specialised like the grouped GEMM: warp 0 TMA (x tile 128 x 64 and
-// one box of the tile's 3 BN term rows per stage), warp 1 tcgen05.mma (M = 128,
-// N = 3 BN: the hi, mid and lo products of a K-step in one instruction, each in
-// its own column group of the accumulator), warps 2-5 epilogue (chunk promotion
-// (lo + mid) + hi into fp32 registers, bias add, fp32 logits to global).  Softmax,
-// top-k and gates follow in k_router_topk (router.cu).
+// k_split_wgate writes the three terms in blocks of 16 experts,
+// [E_pad / 16][3][16][d] bf16 (rows >= E zero, E_pad a multiple of 64): a tile of
+// BN experts (16, 32 or 64) is BN / 16 consecutive blocks, so one TMA box of 3 BN
+// rows holds its three terms whatever BN is, and the split depends on W_gate
+// alone -- it can be made once per weight update (moe_prepare_router_weights) or
+// by every call into the workspace.  k_router_logits_tc: persistent, one CTA per
+// SM, warp-specialised like the grouped GEMM: warp 0 TMA (x tile 128 x 64 and one
+// box of the tile's 3 BN term rows per stage), warp 1 tcgen05.mma (M = 128, N = 3 BN:
+// the hi, mid and lo products of a K-step in one instruction; accumulator column
+// 48 b + 16 q + j holds term q of expert 16 b + j of the tile), warps 2-5 epilogue
+// (chunk promotion (lo + mid) + hi into fp32 registers, bias add, fp32 logits to
+// global).  Softmax, top-k and gates follow in k_router_topk (router.cu).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -66,11 +70,12 @@ __device__ __forceinline__ void split3(float w, __nv_bfloat16& hi, __nv_bfloat16
     lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
 }
 
-// out is [E_pad / BN][3][BN][d]: for each tile of BN experts, its hi, mid and lo rows
-// (rows >= E zero), so one TMA box of 3 BN rows holds a tile's three terms.  With d a
-// multiple of 8 and W_gate 16-byte aligned every thread splits 8 consecutive weights
-// of a row (two 16-byte loads, three 16-byte stores); otherwise one weight.
-__global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int BN, int d,
+// out is [E_pad / 16][3][16][d]: for each block of 16 experts, its hi, mid and lo rows
+// (rows >= E zero).  With d a multiple of 8 and W_gate 16-byte aligned every thread
+// splits 8 consecutive weights of a row (two 16-byte loads, three 16-byte stores);
+// otherwise one weight.
+constexpr int kSplitBlock = 16;
+__global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ Wg, int E, int E_pad, int d,
                                                      __nv_bfloat16* __restrict__ out)
 {
     griddep_launch_dependents();
@@ -93,11 +98,11 @@ __global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ W
             __align__(16) __nv_bfloat16 h[8], m[8], lo[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) split3(w[q], h[q], m[q], lo[q]);
-            const int tile = e / BN, el = e - tile * BN;
-            const size_t r0 = (size_t)tile * 3 * BN + el;  // hi row; mid and lo rows BN and 2 BN further
+            const int blk = e / kSplitBlock, el = e - blk * kSplitBlock;
+            const size_t r0 = (size_t)blk * 3 * kSplitBlock + el;  // hi row; mid and lo rows 16 and 32 further
             *reinterpret_cast<uint4*>(out + r0 * d + col) = *reinterpret_cast<const uint4*>(h);
-            *reinterpret_cast<uint4*>(out + (r0 + BN) * d + col) = *reinterpret_cast<const uint4*>(m);
-            *reinterpret_cast<uint4*>(out + (r0 + 2 * BN) * d + col) = *reinterpret_cast<const uint4*>(lo);
+            *reinterpret_cast<uint4*>(out + (r0 + kSplitBlock) * d + col) = *reinterpret_cast<const uint4*>(m);
+            *reinterpret_cast<uint4*>(out + (r0 + 2 * kSplitBlock) * d + col) = *reinterpret_cast<const uint4*>(lo);
         }
         return;
     }
@@ -107,11 +112,11 @@ __global__ void __launch_bounds__(256) k_split_wgate(const float* __restrict__ W
         const float w = e < E ? Wg[i] : 0.0f;  // Wg is [E, d]: the same flat index for e < E
         __nv_bfloat16 h, m, lo;
         split3(w, h, m, lo);
-        const int tile = e / BN, el = e - tile * BN;
-        const size_t r0 = (size_t)tile * 3 * BN + el;
+        const int blk = e / kSplitBlock, el = e - blk * kSplitBlock;
+        const size_t r0 = (size_t)blk * 3 * kSplitBlock + el;
         out[r0 * d + col] = h;
-        out[(r0 + BN) * d + col] = m;
-        out[(r0 + 2 * BN) * d + col] = lo;
+        out[(r0 + kSplitBlock) * d + col] = m;
+        out[(r0 + 2 * kSplitBlock) * d + col] = lo;
     }
 }
 
@@ -123,17 +128,6 @@ __device__ __forceinline__ bool wait_short(uint64_t* bar, uint32_t parity)
     return true;
 }
 
-// Each thread of the warp loads 16 consecutive fp32 columns of its TMEM lane.
-__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 
 // The rest of the router for one token per thread when a tile holds every expert:
 // logits (+ bias) written out, softmax, the k largest logits (ties to the lower expert
@@ -213,7 +207,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
 {
     using C = RCfg<BN>;
     constexpr uint32_t IDESC = idesc_bf16_f32(kRBM, C::N);
-    constexpr int CHUNK = BN < 32 ? BN : 32;  // TMEM columns per epilogue load
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -254,7 +247,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    griddep_wait();  // the W_gate splits come from the previous kernel
+    griddep_wait();  // x and the W_gate splits may come from earlier kernels
     if (FUSE && blockIdx.x == 0 && threadIdx.x == 0) *a.scan_done = 0u;  // re-arm the dispatch scan
 
     const int m_tiles = ceil_div(a.T, kRBM);
@@ -368,30 +361,18 @@ __global__ void __launch_bounds__(kRThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t t_lane = tmem_base + acc * C::N + (static_cast<uint32_t>(q * 32) << 16);
-                // promote the chunk: (lo + mid) + hi per expert, added to the fp32 running sums
+                // promote the chunk: (lo + mid) + hi per expert, added to the fp32 running
+                // sums; block b of 16 experts has its hi, mid, lo columns at 48 b + {0, 16, 32}
 #pragma unroll
-                for (int c = 0; c < BN / CHUNK; ++c) {
-                    if constexpr (CHUNK == 32) {
-                        uint32_t rh[32], rm[32], rl[32];
-                        tmem_ld_32cols(t_lane + c * 32, rh);
-                        tmem_ld_32cols(t_lane + BN + c * 32, rm);
-                        tmem_ld_32cols(t_lane + 2 * BN + c * 32, rl);
-                        tmem_ld_wait();
+                for (int c = 0; c < BN / kSplitBlock; ++c) {
+                    uint32_t rh[16], rm[16], rl[16];
+                    tmem_ld_16cols(t_lane + c * 3 * kSplitBlock, rh);
+                    tmem_ld_16cols(t_lane + c * 3 * kSplitBlock + kSplitBlock, rm);
+                    tmem_ld_16cols(t_lane + c * 3 * kSplitBlock + 2 * kSplitBlock, rl);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            sum[c * 32 + i] +=
-                                (__uint_as_float(rl[i]) + __uint_as_float(rm[i])) + __uint_as_float(rh[i]);
-                    } else {
-                        uint32_t rh[16], rm[16], rl[16];
-                        tmem_ld_16cols(t_lane + c * 16, rh);
-                        tmem_ld_16cols(t_lane + BN + c * 16, rm);
-                        tmem_ld_16cols(t_lane + 2 * BN + c * 16, rl);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            sum[c * 16 + i] +=
-                                (__uint_as_float(rl[i]) + __uint_as_float(rm[i])) + __uint_as_float(rh[i]);
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        sum[c * 16 + i] += (__uint_as_float(rl[i]) + __uint_as_float(rm[i])) + __uint_as_float(rh[i]);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -438,14 +419,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
 template <int BN, bool FUSE>
 cudaError_t launch_bn(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a, int sms,
-                      cudaStream_t st)
+                      cudaStream_t st, bool pdl)
 {
     auto kern = k_router_logits_tc<BN, FUSE>;
     const size_t smem = RCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int tiles = ceil_div(a.T, kRBM) * a.n_tiles * a.k_splits;
-    return launch_kernel(kern, dim3(tiles < sms ? tiles : sms), dim3(kRThreads), smem, st, true, x, w, a);
+    return launch_kernel(kern, dim3(tiles < sms ? tiles : sms), dim3(kRThreads), smem, st, pdl, x, w, a);
 }
 
 }  // namespace
@@ -471,25 +452,27 @@ int router_tc_ksplits(int T, int E, int d)
     return ks;
 }
 
-cudaError_t launch_split_wgate(const float* Wg, int E, int E_pad, int bn, int d, void* out, int sms, cudaStream_t st,
-                               bool pdl)
+int router_split_rows(int E) { return (E + 63) / 64 * 64; }
+
+cudaError_t launch_split_wgate(const float* Wg, int E, int d, void* out, int sms, cudaStream_t st, bool pdl)
 {
+    const int E_pad = router_split_rows(E);
     const size_t n = (d % 8 == 0) ? (size_t)E_pad * d / 8 : (size_t)E_pad * d;
     size_t grid = (n + 255) / 256;
     if (grid > (size_t)sms * 8) grid = (size_t)sms * 8;
-    return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, bn, d,
+    return launch_kernel(k_split_wgate, dim3((int)grid), dim3(256), 0, st, pdl, Wg, E, E_pad, d,
                          static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_router_logits_tc(const CUtensorMap& x, const CUtensorMap& w, const RouterGemmArgs& a,
-                                    int bn, int sms, cudaStream_t st)
+                                    int bn, int sms, cudaStream_t st, bool pdl)
 {
     // a.fuse is set only for tiles of at most 32 experts (one tile, no K split): there the
     // epilogue's per-token softmax and top-k are short; wider tiles keep the top-k kernel
     switch (bn) {
-    case 16: return a.fuse ? launch_bn<16, true>(x, w, a, sms, st) : launch_bn<16, false>(x, w, a, sms, st);
-    case 32: return a.fuse ? launch_bn<32, true>(x, w, a, sms, st) : launch_bn<32, false>(x, w, a, sms, st);
-    default: return launch_bn<64, false>(x, w, a, sms, st);
+    case 16: return a.fuse ? launch_bn<16, true>(x, w, a, sms, st, pdl) : launch_bn<16, false>(x, w, a, sms, st, pdl);
+    case 32: return a.fuse ? launch_bn<32, true>(x, w, a, sms, st, pdl) : launch_bn<32, false>(x, w, a, sms, st, pdl);
+    default: return launch_bn<64, false>(x, w, a, sms, st, pdl);
     }
 }
 

@@ -56,7 +56,8 @@ class MoELayer:
 
     def __init__(self, cfg: LayerConfig, weights: dict, device="cuda", *, flags: int = 0,
                  residual_mode: int | None = None, want_logits: bool = False,
-                 want_probs: bool = False, want_perm: bool = True, ep_ranks: int | None = None):
+                 want_probs: bool = False, want_perm: bool = True, ep_ranks: int | None = None,
+                 prepared_router: bool = False):
         self.cfg = cfg
         self.device = torch.device(device)
         self.params = make_params(cfg, flags=flags, residual_mode=residual_mode)
@@ -92,11 +93,28 @@ class MoELayer:
             W_noise=_ptr(w.get("W_noise")), b_noise=_ptr(w.get("b_noise")),
             noise_eps=_ptr(w.get("noise_eps")), W1_scale=_ptr(w.get("W1_scale")),
             W3_scale=_ptr(w.get("W3_scale")), W2_scale=_ptr(w.get("W2_scale")))
+        # prepared_router: split the router weights once (moe_prepare_router_weights) instead
+        # of on every call; the buffer stays valid until the router weights change
+        self.router_weights = None
+        if prepared_router:
+            self.prepare_router()
         o = self.out
         self.outputs = _lib.moe_outputs_t(
             y=_ptr(o["y"]), expert_idx=_ptr(o["expert_idx"]), gates=_ptr(o["gates"]),
             counts=_ptr(o["counts"]), dropped=_ptr(o["dropped"]), aux=_ptr(o["aux"]),
             logits=_ptr(o["logits"]), probs=_ptr(o["probs"]), perm_row=_ptr(o["perm_row"]))
+
+    def prepare_router(self, stream=None) -> None:
+        """(Re)make the split router weights from the current W_gate (and W_noise)."""
+        st, nbytes = _lib.moe_router_weights_size(self.params)
+        check(st, "moe_router_weights_size")
+        if self.router_weights is None or self.router_weights.numel() < nbytes:
+            self.router_weights = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.device)
+        w = self.weights
+        check(_lib.moe_prepare_router_weights(self.params, w["W_gate"].data_ptr(), _ptr(w.get("W_noise")),
+                                              self.router_weights.data_ptr(), nbytes, _stream_handle(stream)),
+              "moe_prepare_router_weights")
+        self.inputs.router_weights = self.router_weights.data_ptr()
 
     def set_x(self, x: torch.Tensor) -> None:
         """Point the layer at a new [T, d] input (kept alive by the layer)."""

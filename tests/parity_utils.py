@@ -133,3 +133,27 @@ def sample_tokens(cfg, out: dict, n: int, seed: int = 1234) -> np.ndarray:
         hit = np.nonzero((out["expert_idx"].numpy() == e).any(axis=1))[0][:64]
         picks |= set(hit.tolist())
     return np.array(sorted(picks))
+
+
+def quantized_oracle_rows(cfg, inp: dict, qinp: dict, r, tokens, dequantize):
+    """Oracle rows of the listed tokens for a layer with quantised expert weights, on the
+    exactly dequantised weights, one expert at a time (a full-size layer's dequantised
+    weights would not fit the host's memory in fp64): the experts' outputs for the
+    tokens' kept slots (orc.expert_apply), then the oracle's combine."""
+    tok = np.asarray(tokens, dtype=np.int64)
+    slots = [(int(t), j) for t in tok for j in range(cfg.k) if not r.dropped[t, j]]
+    row_of = np.full((cfg.T, cfg.k), -1, dtype=np.int32)
+    for n, (t, j) in enumerate(slots):
+        row_of[t, j] = n
+    o = np.zeros((max(len(slots), 1), cfg.d))
+    for e in sorted({int(r.idx[t, j]) for t, j in slots}):
+        sel = [n for n, (t, j) in enumerate(slots) if r.idx[t, j] == e]
+        one = {}
+        for name in ("W1", "W3", "W2"):
+            q = qinp.get(name)
+            one[name] = None if q is None else dequantize(q[e:e + 1].numpy(), qinp[name + "_scale"][e:e + 1].numpy())
+        b1 = None if inp.get("b1") is None else inp["b1"][e:e + 1]
+        b2 = None if inp.get("b2") is None else inp["b2"][e:e + 1]
+        o[sel] = orc.expert_apply(inp["x"], one["W1"], one["W3"], one["W2"], b1, b2,
+                                  [slots[n][0] for n in sel], np.zeros(len(sel), dtype=np.int32), act_name=cfg.act)
+    return orc.combine_rows(inp["x"], r.gates, r.dropped, row_of, o, residual_mode=cfg.residual_mode, tokens=tok)

@@ -14,7 +14,7 @@ def test_library_exports_every_header_function():
                           "moe_status_string", "moe_dispatch_positions_noalloc",
                           "moe_kernel_launches", "moe_backward", "moe_quantize_int8",
                           "moe_check_bounded_wait", "moe_ep_workspace_size", "moe_forward_ep",
-                          "moe_quantize_int4"}
+                          "moe_quantize_int4", "moe_router_weights_size", "moe_prepare_router_weights"}
     L = _lib.load()
     for n in names:
         assert hasattr(L, n), n
@@ -29,7 +29,7 @@ def test_status_strings():
 def test_struct_layouts_match_header():
     # moe_params_t: 11 int32/float fields, uint32 flags, noisy_gating, noise_min_std, weight_format
     assert ctypes.sizeof(_lib.moe_params_t) == 15 * 4
-    assert ctypes.sizeof(_lib.moe_inputs_t) == 14 * 8
+    assert ctypes.sizeof(_lib.moe_inputs_t) == 15 * 8
     assert ctypes.sizeof(_lib.moe_outputs_t) == 9 * 8
 
 
@@ -350,4 +350,41 @@ def test_quantize_int4_rejects_bad_arguments():
     assert _lib.moe_quantize_int4(None, _lib.MOE_BF16, 4, 128, 16, 16, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_quantize_int4(16, 7, 4, 128, 16, 16, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_quantize_int4(16, _lib.MOE_BF16, 0, 128, 16, 16, None) == _lib.MOE_OK  # nothing to do
+    assert _lib.moe_kernel_launches() == n0
+
+
+# ---- router weights prepared once per weight update ------------------------------
+
+@pytest.mark.parametrize("name,noisy", [("switch", False), ("deepseek", False), ("skewed", True), ("mixtral", True)])
+def test_router_weights_size(name, noisy):
+    cfg = config(name, noisy=noisy)
+    st, n = _lib.moe_router_weights_size(make_params(cfg))
+    e_pad = (cfg.E + 63) // 64 * 64
+    assert st == _lib.MOE_OK and n == 3 * 2 * e_pad * cfg.d * (2 if noisy else 1)
+    # independent of the batch size
+    assert _lib.moe_router_weights_size(make_params(cfg, T=7))[1] == n
+
+
+def test_router_weights_need_the_tensor_core_router():
+    assert _lib.moe_router_weights_size(make_params(config("tiny")))[0] == _lib.MOE_ERR_UNSUPPORTED
+    p = make_params(config("switch"), flags=_lib.MOE_FLAG_FFMA_ROUTER)
+    assert _lib.moe_router_weights_size(p)[0] == _lib.MOE_ERR_UNSUPPORTED
+    n0 = _lib.moe_kernel_launches()
+    p = make_params(config("switch"))
+    _, n = _lib.moe_router_weights_size(p)
+    assert _lib.moe_prepare_router_weights(p, None, None, 1 << 40, n, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_prepare_router_weights(p, 1 << 40, None, 1 << 41, n - 1, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.moe_prepare_router_weights(p, 1 << 40, 1 << 42, 1 << 41, n, None) == _lib.MOE_ERR_INVALID_ARG  # no noise
+    assert _lib.moe_prepare_router_weights(p, (1 << 40) + 4, None, 1 << 41, n, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.moe_kernel_launches() == n0
+
+
+def test_prepared_router_weights_rejected_for_cuda_core_routers():
+    cfg = config("tiny")
+    p = make_params(cfg)
+    _, need = _lib.moe_workspace_size(p)
+    ins, outs = _fake_io(cfg)
+    ins.router_weights = 1 << 41
+    n0 = _lib.moe_kernel_launches()
+    assert _lib.moe_forward(p, ins, outs, 1 << 44, need, None) == _lib.MOE_ERR_INVALID_ARG
     assert _lib.moe_kernel_launches() == n0

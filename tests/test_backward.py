@@ -27,6 +27,7 @@ CASES = {
     "relu_capacity_k1": config("switch", T=1000, d=192, E=16, k=1, F=384, cf=1.0),
     "swiglu_renorm": config("mixtral", T=300, d=256, E=8, k=2, F=512),
     "swiglu_shared": config("deepseek", T=200, d=128, E=16, k=4, F=200),
+    "swiglu_shared_fused": config("deepseek", T=260, d=128, E=16, k=3, F=192),  # shared experts in the fused kernel
     "fp32_swiglu_shared": config("deepseek", T=100, d=64, E=8, k=2, F=48, dtype="f32"),
     "ragged_dims": config("mixtral", T=77, d=200, E=5, k=2, F=328),
     "noisy_switch_capacity": config("switch", T=1000, d=256, E=32, k=1, F=384, cf=1.25, noisy=True,

@@ -13,7 +13,7 @@ import torch
 
 from oracle import moe_oracle as orc
 from parity_utils import (check_dropped_tokens_pass_x, check_router_vs_fp64, check_routing_bitexact,
-                          rel_frobenius, sample_tokens, to_cpu)
+                          quantized_oracle_rows, rel_frobenius, sample_tokens, to_cpu)
 from sparse_mixture_experts_scan_b300 import MoELayer, _lib, config, make_inputs, quantize_expert_weights, quantize_int4
 
 pytestmark = pytest.mark.gpu
@@ -60,18 +60,15 @@ def _run(cfg, seed=0):
     return to_cpu(inp), to_cpu(qinp), to_cpu(layer.out)
 
 
-def _dequantized(qinp, name):
-    q = qinp.get(name)
-    return None if q is None else orc.dequantize_int4(q.numpy(), qinp[name + "_scale"].numpy())
+def _dequantize(q, scale):
+    return orc.dequantize_int4(q, scale)
 
 
 def _check(cfg, inp, qinp, out, tokens=None):
     r = check_routing_bitexact(cfg, out)
     check_router_vs_fp64(cfg, inp, out)
     tok = np.arange(cfg.T) if tokens is None else tokens
-    y_ref = orc.output_rows(inp["x"], _dequantized(qinp, "W1"), _dequantized(qinp, "W3"), _dequantized(qinp, "W2"),
-                            inp["b1"], inp["b2"], r.idx, r.gates, r.dropped, E=cfg.E, S=cfg.S, act_name=cfg.act,
-                            residual_mode=cfg.residual_mode, tokens=tok)
+    y_ref = quantized_oracle_rows(cfg, inp, qinp, r, tok, _dequantize)
     err = rel_frobenius(out["y"][torch.as_tensor(tok)].double().numpy(), y_ref)
     assert err <= 2e-2, err
     check_dropped_tokens_pass_x(cfg, inp, out)

@@ -30,6 +30,9 @@ SMALL = {
     "gelu_tanh_bias": _case("tiny", T=257, d=128, E=4, k=2, F=256, dtype="bf16"),
     "gelu_erf_k_eq_E": _case("tiny", T=130, d=64, E=3, k=3, F=64, act="gelu_erf", dtype="bf16"),
     "shared_experts": _case("deepseek", T=200, d=128, E=16, k=4, F=200),
+    # d_ff a multiple of 64: the shared experts run inside the fused expert kernel
+    "shared_experts_fused": _case("deepseek", T=333, d=256, E=16, k=3, F=192, S=3),
+    "shared_experts_capacity": _case("deepseek", T=400, d=128, E=16, k=2, F=128, cf=0.5),
     "single_expert": _case("mixtral", T=1000, d=128, E=1, k=1, F=256),
     "ragged_dims": _case("mixtral", T=77, d=200, E=5, k=2, F=328),
     "many_experts_drops": _case("skewed", T=512, d=128, E=256, k=8, F=128),
@@ -186,8 +189,8 @@ def test_ffma_router_matches_oracle_and_tensor_core_router(name):
 
 
 @pytest.mark.parametrize("name", ["swiglu_renorm", "relu_capacity", "switch_like_k1", "gelu_tanh_bias",
-                                  "shared_experts", "ragged_dims", "many_experts_drops", "max_experts",
-                                  "single_expert"])
+                                  "shared_experts", "shared_experts_fused", "shared_experts_capacity",
+                                  "ragged_dims", "many_experts_drops", "max_experts", "single_expert"])
 def test_fused_and_two_launch_experts_agree_bitwise(name):
     # The fused persistent kernel (dynamic tiles, GEMM2 tiles waiting on GEMM1 tiles)
     # and the two grouped-GEMM launches accumulate every output element in the same
@@ -376,3 +379,57 @@ def test_expired_device_wait_is_reported_and_the_context_stays_usable():
     out = to_cpu(layer.out)
     r = check_routing_bitexact(cfg, out)
     check_output(cfg, to_cpu(inp), out, r)
+
+
+@pytest.mark.parametrize("name", ["switch_like_k1", "swiglu_renorm", "max_experts", "router_split_k",
+                                  "many_experts_drops"])
+def test_prepared_router_weights_give_identical_outputs(name):
+    # The router weights split once (moe_prepare_router_weights) are the same bits the
+    # per-call split writes into the workspace, so every output is identical.
+    cfg = SMALL[name]
+    inp = _inputs(cfg, random_bias=True)
+    a = MoELayer(cfg, inp, want_logits=True, want_probs=True)
+    b = MoELayer(cfg, inp, want_logits=True, want_probs=True, prepared_router=True)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert b.device_status() == _lib.MOE_OK
+    for k in ("y", "logits", "probs", "expert_idx", "gates", "counts", "dropped", "aux", "perm_row"):
+        assert torch.equal(a.out[k], b.out[k]), k
+    # the prepared buffer does not depend on the batch size: reuse it for a smaller, ragged batch
+    t2 = min(77, cfg.T - 5)
+    small = replace(cfg, T=t2)
+    sinp = dict(inp)
+    sinp["x"] = inp["x"][:t2].contiguous()
+    c = MoELayer(small, sinp, want_logits=True)
+    d = MoELayer(small, sinp, want_logits=True)
+    d.inputs.router_weights = b.router_weights.data_ptr()
+    c.run()
+    d.run()
+    torch.cuda.synchronize()
+    for k in ("y", "logits", "expert_idx", "gates", "aux"):
+        assert torch.equal(c.out[k], d.out[k]), k
+
+
+def test_prepared_router_weights_with_noisy_gating():
+    cfg = _case("mixtral", T=300, d=128, E=24, k=3, F=128, noisy=True, noise_min_std=0.01)
+    inp = _inputs(cfg)
+    a = MoELayer(cfg, inp, want_logits=True)
+    b = MoELayer(cfg, inp, want_logits=True, prepared_router=True)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    for k in ("y", "logits", "expert_idx", "gates", "aux"):
+        assert torch.equal(a.out[k], b.out[k]), k
+
+
+def test_top1_stage_entry_points_equal_forward():
+    # top-1 layers finish the combine inside the expert stage (its GEMM2 epilogue writes y,
+    # the dispatch copies dropped tokens): the stage calls still compose to the forward
+    cfg = SMALL["switch_like_k1"]
+    inp = _inputs(cfg)
+    a = run_device(cfg, inp)
+    b = run_device(cfg, inp, stages=["moe_router", "moe_dispatch", "moe_grouped_gemm", "moe_combine"])
+    for k in ("y", "expert_idx", "gates", "counts", "dropped", "aux", "perm_row", "logits"):
+        assert torch.equal(a[k], b[k]), k
+    assert int(a["dropped"].sum()) > 0  # the case has dropped tokens (y = x for them)
