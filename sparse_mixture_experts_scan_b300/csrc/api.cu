@@ -322,9 +322,12 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
     if (c.wq) {
         const Layout& L = c.L;
         const bool gated = c.p.act == MOE_ACT_SWIGLU;
-        // token rows per tile: what an expert holds on average (capped by the capacity)
+        // token rows per tile: enough for the rows an expert can hold (the capacity, or the
+        // batch), but not far beyond what it holds on average, so that the token tile is not
+        // mostly padding
         const long long avg = ((long long)L.T * L.k + L.E - 1) / L.E;
-        const long long est = L.C >= 0 ? std::min<long long>(L.C, avg) : avg;
+        const long long bound = L.C >= 0 ? std::min<long long>(L.C, L.T) : L.T;
+        const long long est = std::min<long long>(bound, 2 * avg + 16);
         c.wq_bits = c.p.weight_format == MOE_WEIGHTS_INT4 ? 4 : 8;
         c.wq_nt = gemm_wq_tokens_tile((int)std::min<long long>(est, 1 << 30), gated);
         // one stage reads 128 bytes of each weight row (128 int8 or 256 int4 values)

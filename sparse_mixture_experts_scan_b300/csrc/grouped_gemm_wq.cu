@@ -20,7 +20,7 @@
 //   8-bit: q in [-127, 127] is exact in bf16; the per-row scale is applied to
 //          the accumulator in the epilogue: sum_k q[n,k] x[m,k] * scale[n].
 //   4-bit: the converter multiplies q in [-7, 7] by its group's scale (groups
-//          of 128 input columns) in fp32 and rounds once to bf16.
+//          of 128 input columns) in packed bf16 arithmetic: bf16(q * bf16(scale)).
 // One thread of the epilogue holds one weight row (its TMEM lane) for NT
 // tokens: scale, bias and activation are per-thread scalars, and SwiGLU pairs
 // the W1 and W3 accumulators of the same row.
@@ -135,17 +135,30 @@ __device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t&
     hi = pack_bf16x2(f2, f3);
 }
 
-// int4 x 8 (one 32-bit word, value 2i in nibble 2i) -> bf16 x 8 of q * s (four words):
-// the nibble plus 8 (offset binary) goes into the low mantissa of 2^23, subtracting
-// 2^23 + 8 leaves q exactly; q * s is rounded once to bf16.
-__device__ __forceinline__ void i4x8_to_bf16(uint32_t w, float s, uint32_t (&o)[4])
+// int4 x 8 (one 32-bit word, value 2i in nibble 2i) -> bf16 x 8 of q * s (four words),
+// in packed bf16x2 arithmetic: the nibble plus 8 (offset binary) becomes the low
+// mantissa of bf16 128 (0x4300: 128 + n is exact for n < 128), one byte permute
+// builds a pair (the permute's sign-replicate selector 8 yields the zero bytes), a
+// packed subtraction of 136 leaves q exactly, and a packed multiply by the scale
+// (rounded to bf16, s2 = {s, s}) gives bf16(q * bf16(s)).
+__device__ __forceinline__ void i4x8_to_bf16(uint32_t w, uint32_t s2, uint32_t (&o)[4])
 {
     const uint32_t u = w ^ 0x88888888u;
+    const uint32_t lo = u & 0x0F0F0F0Fu;         // elements 0, 2, 4, 6 (one per byte)
+    const uint32_t hi = (u >> 4) & 0x0F0F0F0Fu;  // elements 1, 3, 5, 7
+    const uint32_t k136 = 0x43084308u;           // bf16 {136, 136}
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const float lo = __uint_as_float(0x4B000000u | ((u >> (8 * p)) & 0xFu)) - 8388616.0f;
-        const float hi = __uint_as_float(0x4B000000u | ((u >> (8 * p + 4)) & 0xFu)) - 8388616.0f;
-        o[p] = pack_bf16x2(lo * s, hi * s);
+        // bytes [lo.p, 0, hi.p, 0] | 0x43004300 = bf16 {128 + n_2p, 128 + n_2p+1}; prmt.b32 (not
+        // the __byte_perm intrinsic, which masks the selector to its byte index) honours the
+        // sign-replicate bit of selector 8: lo's byte 0 is below 16, so it yields 0x00
+        const uint32_t sel = 0x8080u | (uint32_t)p | ((uint32_t)(4 + p) << 8);
+        uint32_t v;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(lo), "r"(hi), "r"(sel));
+        v |= 0x43004300u;
+        uint32_t q;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v), "r"(k136));
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[p]) : "r"(q), "r"(s2));
     }
 }
 
@@ -374,15 +387,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tm.locate(tile, s_toff, n_tiles, mt, n);
             const int w_row = tm.g * args.b_rows_per_group + n * kBW + r;  // global weight row
             const bool w_ok = n * kBW + r < args.N;
+            // 4-bit: the group scales of a stage's two 128-column groups, loaded one stage
+            // ahead (each thread's scales are a separate sector, so the load is slow)
+            const int ng = WBITS == 4 ? args.K / kGroupCols : 0;
+            const float* srow = scales + (size_t)(w_ok ? w_row : 0) * ng;
+            float nx0 = 0.0f, nx1 = 0.0f;
+            if (WBITS == 4 && w_ok) {
+                nx0 = __ldg(&srow[0]);
+                if (1 < ng) nx1 = __ldg(&srow[1]);
+            }
             for (int kb = 0; kb < num_kb && ok; ++kb) {
-                // 4-bit: the group scales of the stage's two 128-column groups (before the waits)
-                float sc0 = 0.0f, sc1 = 0.0f;
+                const float sc0 = nx0, sc1 = nx1;
                 if constexpr (WBITS == 4) {
-                    const int ng = args.K / kGroupCols;
-                    const int g0 = (kb * C::kKS) / kGroupCols;
-                    if (w_ok) {
-                        sc0 = __ldg(&scales[(size_t)w_row * ng + g0]);
-                        if (g0 + 1 < ng) sc1 = __ldg(&scales[(size_t)w_row * ng + g0 + 1]);
+                    const int g1 = ((kb + 1) * C::kKS) / kGroupCols;  // the next stage's first group
+                    if (w_ok && g1 < ng) {
+                        nx0 = __ldg(&srow[g1]);
+                        if (g1 + 1 < ng) nx1 = __ldg(&srow[g1 + 1]);
                     }
                 }
                 if (!mbar_wait(&full_q[stage], phase, abort_flag)) {
@@ -411,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             i8x4_to_bf16(w.z, v[ci * 8 + 4], v[ci * 8 + 5]);
                             i8x4_to_bf16(w.w, v[ci * 8 + 6], v[ci * 8 + 7]);
                         } else {
-                            const float scu = (u * kBK) / kGroupCols == 0 ? sc0 : sc1;
+                            const float scf = (u * kBK) / kGroupCols == 0 ? sc0 : sc1;
+                            const uint32_t scu = pack_bf16x2(scf, scf);
                             uint32_t o[4];
                             i4x8_to_bf16(w.x, scu, o);
                             v[ci * 16 + 0] = o[0], v[ci * 16 + 1] = o[1], v[ci * 16 + 2] = o[2], v[ci * 16 + 3] = o[3];
@@ -589,6 +610,7 @@ int gemm_wq_tokens_tile(int rows_per_expert, bool gated)
 {
     if (rows_per_expert <= 32) return 32;
     if (rows_per_expert <= 64 || gated) return 64;
+    if (rows_per_expert <= 96) return 96;
     return 128;
 }
 
@@ -598,10 +620,12 @@ cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUt
     if (wbits == 8) {
         if (nt == 32) return launch_nt<8, 32>(x, w, w3, a, act, grid, st, pdl);
         if (nt == 64) return launch_nt<8, 64>(x, w, w3, a, act, grid, st, pdl);
+        if (nt == 96) return launch_nt<8, 96>(x, w, w3, a, act, grid, st, pdl);
         return launch_nt<8, 128>(x, w, w3, a, act, grid, st, pdl);
     }
     if (nt == 32) return launch_nt<4, 32>(x, w, w3, a, act, grid, st, pdl);
     if (nt == 64) return launch_nt<4, 64>(x, w, w3, a, act, grid, st, pdl);
+    if (nt == 96) return launch_nt<4, 96>(x, w, w3, a, act, grid, st, pdl);
     return launch_nt<4, 128>(x, w, w3, a, act, grid, st, pdl);
 }
 

@@ -203,7 +203,8 @@ cudaError_t launch_quantize_int8(const void* w, bool bf16, long long rows, int c
 // stage streams the weights): the transposed product D[n, m] = W[n, :] . X[m, :]
 // with the weight tile converted to bf16 into tensor memory (the MMA's A operand)
 // and the token tile (NT rows) as B.  8-bit: per-row scales applied in the
-// epilogue; 4-bit: group scales (128 input columns) applied by the converters.
+// epilogue; 4-bit: group scales (128 input columns) applied by the converters (in
+// bf16: bf16(q * bf16(scale))).
 // maps: X (bf16 [rows, K], box {64, NT}), W and W3 (uint8 [groups * rows, K bytes],
 // box {128 bytes, 128 rows}, 128-byte swizzle).
 struct GroupedGemmWqArgs {
@@ -219,8 +220,8 @@ struct GroupedGemmWqArgs {
     const float* scale3;   // SwiGLU: the W3 rows' scales
     uint32_t* err;
 };
-// Token rows per tile (32, 64 or 128) for a layer whose experts hold about
-// rows_per_expert rows.
+// Token rows per tile (32, 64, 96 or 128; at most 64 for SwiGLU) for a layer whose
+// experts hold about rows_per_expert rows.
 int gemm_wq_tokens_tile(int rows_per_expert, bool gated);
 cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3,
                            const GroupedGemmWqArgs& a, int wbits, int act, int nt, int grid, cudaStream_t st,
