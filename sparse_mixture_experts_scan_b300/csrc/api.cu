@@ -583,7 +583,7 @@ moe_status_t stage_gemm(Ctx& c)
         w1.rows = g1.rows;
         w1.G = L.E;
         w1.N = L.F;
-        w1.n_tiles = ceil_div(L.F, 128);
+        w1.n_tiles = gemm_wq_weight_tiles(L.F, act1, c.wq_nt);
         w1.K = L.d;
         w1.b_rows_per_group = L.F;
         w1.out = g1.out;
@@ -594,7 +594,7 @@ moe_status_t stage_gemm(Ctx& c)
         w1.err = c.err();
         GroupedGemmWqArgs w2 = w1;
         w2.N = L.d;
-        w2.n_tiles = ceil_div(L.d, 128);
+        w2.n_tiles = gemm_wq_weight_tiles(L.d, kActNone, c.wq_nt);
         w2.K = L.F;
         w2.b_rows_per_group = L.d;
         w2.out = g2.out;

@@ -58,10 +58,10 @@ constexpr size_t kBarBytes = 512;
 constexpr size_t kTableBytes = sizeof(int) * (3 * kMaxExperts + 2);
 constexpr size_t kSmemBudget = 200 * 1024;  // shared-memory stages
 
-template <int WBITS, bool GATED, int NT>
+template <int WBITS, bool TWO, int NT>
 struct Cfg {
     static_assert(NT % 32 == 0, "token tile");
-    static constexpr int kNA = GATED ? 2 : 1;                    // A tiles per K block
+    static constexpr int kNA = TWO ? 2 : 1;                      // A tiles per K block
     static constexpr int kKS = WBITS == 8 ? 128 : 256;           // K values per shared-memory stage
     static constexpr int kSub = kKS / kBK;                       // TMEM slots per stage
     static constexpr uint32_t kXBoxBytes = NT * kBK * 2;         // one [NT x 64] token box
@@ -121,43 +121,45 @@ __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t* r
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// int8 x 4 (one 32-bit word) -> bf16 x 4 (two words), exactly: flipping the sign bit
-// makes the byte v + 128, a byte permute places it in the low mantissa of 2^23, and
-// subtracting 2^23 + 128 leaves v in fp32; |v| <= 128 is exact in bf16.
+// int8 x 4 (one 32-bit word) -> bf16 x 4 (two words), exactly, in packed bf16x2
+// arithmetic: a two's-complement byte is v = m - 128 s (m its low seven bits, s its
+// top bit).  With the high byte 0x43, m in the low byte is the bf16 128 + m (seven
+// mantissa bits) and s moved to bit 7 is the bf16 128 or 256 (the exponent's lowest
+// bit), so one packed subtraction leaves v, an integer of magnitude <= 128 (exact).
 __device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    const uint32_t u = w ^ 0x80808080u;
-    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u)) - 8388736.0f;
-    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u)) - 8388736.0f;
-    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542u)) - 8388736.0f;
-    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543u)) - 8388736.0f;
-    lo = pack_bf16x2(f0, f1);
-    hi = pack_bf16x2(f2, f3);
+    const uint32_t wm = w & 0x7F7F7F7Fu;  // m of each byte
+    const uint32_t ws = w & 0x80808080u;  // s of each byte, at bit 7
+    // byte pairs (0, 1) and (2, 3), each byte below the constant 0x43
+    const uint32_t a01 = __byte_perm(wm, 0x43u, 0x4140u), a23 = __byte_perm(wm, 0x43u, 0x4342u);
+    const uint32_t b01 = __byte_perm(ws, 0x43u, 0x4140u), b23 = __byte_perm(ws, 0x43u, 0x4342u);
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a01), "r"(b01));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(a23), "r"(b23));
 }
 
-// int4 x 8 (one 32-bit word, value 2i in nibble 2i) -> bf16 x 8 of q * s (four words),
-// in packed bf16x2 arithmetic: the nibble plus 8 (offset binary) becomes the low
-// mantissa of bf16 128 (0x4300: 128 + n is exact for n < 128), one byte permute
-// builds a pair (the permute's sign-replicate selector 8 yields the zero bytes), a
-// packed subtraction of 136 leaves q exactly, and a packed multiply by the scale
-// (rounded to bf16, s2 = {s, s}) gives bf16(q * bf16(s)).
+// int4 x 8 (one 32-bit word; byte j holds value 2j in its low nibble, 2j + 1 in its
+// high nibble) -> bf16 x 8 of q * s (four words), in packed bf16x2 arithmetic.  Offset
+// binary n = q + 8 (flip each nibble's top bit).  Per byte j one byte permute puts byte j
+// of u in the low half and byte j of u >> 1 in the high half, each below the constant
+// 0x43 byte, and one mask keeps the low nibble (bits 0-3: bf16 128 + n_2j) and the
+// shifted high nibble (bits 3-6: bf16 128 + 8 n_2j+1).  A packed subtraction of
+// {136, 192} leaves {q_2j, 8 q_2j+1} exactly, and a packed multiply by
+// s2 = {bf16(s), bf16(s) / 8} gives bf16(q * bf16(s)) in both halves (the division by 8
+// is exact, so 8 q * (s / 8) = q * s before the one rounding).
 __device__ __forceinline__ void i4x8_to_bf16(uint32_t w, uint32_t s2, uint32_t (&o)[4])
 {
     const uint32_t u = w ^ 0x88888888u;
-    const uint32_t lo = u & 0x0F0F0F0Fu;         // elements 0, 2, 4, 6 (one per byte)
-    const uint32_t hi = (u >> 4) & 0x0F0F0F0Fu;  // elements 1, 3, 5, 7
-    const uint32_t k136 = 0x43084308u;           // bf16 {136, 136}
+    const uint32_t u1 = u >> 1;
+    const uint32_t k_off = 0x43404308u;  // bf16 {low: 136, high: 192}
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        // bytes [lo.p, 0, hi.p, 0] | 0x43004300 = bf16 {128 + n_2p, 128 + n_2p+1}; prmt.b32 (not
-        // the __byte_perm intrinsic, which masks the selector to its byte index) honours the
-        // sign-replicate bit of selector 8: lo's byte 0 is below 16, so it yields 0x00
-        const uint32_t sel = 0x8080u | (uint32_t)p | ((uint32_t)(4 + p) << 8);
-        uint32_t v;
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(lo), "r"(hi), "r"(sel));
-        v |= 0x43004300u;
+        // byte 0 = u.p, byte 2 = u1.p (bytes 1 and 3 are cleared by the mask, which
+        // also sets them to 0x43)
+        const uint32_t v = __byte_perm(u, u1, (uint32_t)p | ((uint32_t)(4 + p) << 8));
+        uint32_t m;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(m) : "r"(v), "r"(0x0078000Fu), "r"(0x43004300u));
         uint32_t q;
-        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v), "r"(k136));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(m), "r"(k_off));
         asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[p]) : "r"(q), "r"(s2));
     }
 }
@@ -177,13 +179,20 @@ struct WqTiles {
     }
 };
 
-template <int WBITS, int ACT, int NT>
+// PAIR (layers without SwiGLU): a tile is 256 weight rows, two A tiles of 128 rows
+// against one token tile, so each token tile is loaded half as often and every
+// converter warp turns a whole 64-value sub-block of one A tile into bf16 (as with
+// SwiGLU's W1 / W3 pair).
+template <int WBITS, int ACT, int NT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm_wq(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmW3, const GroupedGemmWqArgs args)
 {
     constexpr bool GATED = (ACT == kActSwiglu);
-    using C = Cfg<WBITS, GATED, NT>;
+    static_assert(!(GATED && PAIR), "SwiGLU already pairs W1 and W3");
+    constexpr bool TWO = GATED || PAIR;               // two A tiles per K block
+    constexpr int kTileRows = PAIR ? 2 * kBW : kBW;   // weight rows per tile
+    using C = Cfg<WBITS, TWO, NT>;
     constexpr int S = C::kStages;
     constexpr int NA = C::kSlots;
     constexpr uint32_t IDESC = idesc_bf16_f32(kBW, NT);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mt, n;
                 tm.locate(tile, s_toff, n_tiles, mt, n);
                 const int x_row = s_roff[tm.g] + mt * NT;
-                const int w_row = tm.g * args.b_rows_per_group + n * kBW;
+                const int w_row = tm.g * args.b_rows_per_group + n * kTileRows;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -295,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int wc = kb * (int)C::kWRowBytes;  // byte column of the weight rows
                     tma_load_2d(st + C::kXBytes, &tmW, &full_q[stage], wc, w_row, pol_w);
                     if (GATED) tma_load_2d(st + C::kXBytes + kBW * C::kWRowBytes, &tmW3, &full_q[stage], wc, w_row, pol_w);
+                    if (PAIR) tma_load_2d(st + C::kXBytes + kBW * C::kWRowBytes, &tmW, &full_q[stage], wc, w_row + kBW, pol_w);
                     filled |= 1u << stage;
                     fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -345,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint64_t bdesc = sdesc_kmajor_sw128(x0 + k * 32);
                             const uint32_t accum = (kb | u | k) != 0 ? 1u : 0u;
                             mma_bf16_ts(d_tmem, a0 + k * 8, bdesc, IDESC, accum);
-                            if (GATED) mma_bf16_ts(d_tmem + NT, a0 + 32 + k * 8, bdesc, IDESC, accum);
+                            if (TWO) mma_bf16_ts(d_tmem + NT, a0 + 32 + k * 8, bdesc, IDESC, accum);
                         }
                         mma_commit(&a_empty[slot]);
                         if (++slot == NA) {
@@ -375,18 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int part = (warp - 4) >> 2;  // SwiGLU: the W1 / W3 tile; otherwise the K half
         const int r = q * 32 + lane;       // this thread's weight row in the tile (its TMEM lane)
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const int h = GATED ? part : 0;    // which weight tile of the stage
-        const int kh = GATED ? -1 : part;  // which K half (-1: both)
+        const int h = TWO ? part : 0;    // which weight tile of the stage
+        const int kh = TWO ? -1 : part;  // which K half (-1: both)
         int stage = 0, slot = 0;
         uint32_t phase = 0, sphase = 0;
         bool ok = true;
+        // One TMEM store stays in flight while the next sub-block is converted: the
+        // slot it wrote is signalled (wait::st, then the arrival) just before the next
+        // store, and the last one after the loop.
+        int pend = -1;
         WqTiles tm;
         const float* __restrict__ scales = (GATED && part == 1) ? args.scale3 : args.scale;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             int mt, n;
             tm.locate(tile, s_toff, n_tiles, mt, n);
-            const int w_row = tm.g * args.b_rows_per_group + n * kBW + r;  // global weight row
-            const bool w_ok = n * kBW + r < args.N;
+            const int rr = n * kTileRows + (PAIR ? h * kBW : 0) + r;    // row within the group
+            const int w_row = tm.g * args.b_rows_per_group + rr;         // global weight row
+            const bool w_ok = rr < args.N;
             // 4-bit: the group scales of a stage's two 128-column groups, loaded one stage
             // ahead (each thread's scales are a separate sector, so the load is slow)
             const int ng = WBITS == 4 ? args.K / kGroupCols : 0;
@@ -413,16 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* row = base + (size_t)stage * C::kStageBytes + C::kXBytes +
                                      (size_t)(h * kBW + r) * C::kWRowBytes;
                 for (int u = 0; u < C::kSub; ++u) {
-                    if (!mbar_wait(&a_empty[slot], sphase ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
                     uint32_t v[32];
                     // 16-byte chunks of sub-block u (64 K values) that this thread converts
                     constexpr int kChunks = WBITS == 8 ? 4 : 2;
                     const int cbase = u * kChunks + (kh < 0 ? 0 : kh * (kChunks / 2));
 #pragma unroll
-                    for (int ci = 0; ci < (GATED ? kChunks : kChunks / 2); ++ci) {
+                    for (int ci = 0; ci < (TWO ? kChunks : kChunks / 2); ++ci) {
                         const int c = cbase + ci;
                         const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
                         if constexpr (WBITS == 8) {
@@ -432,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             i8x4_to_bf16(w.w, v[ci * 8 + 6], v[ci * 8 + 7]);
                         } else {
                             const float scf = (u * kBK) / kGroupCols == 0 ? sc0 : sc1;
-                            const uint32_t scu = pack_bf16x2(scf, scf);
+                            const float sb = __bfloat162float(__float2bfloat16_rn(scf));
+                            const uint32_t scu = pack_bf16x2(sb, sb * 0.125f);  // {s, s / 8}, exact
                             uint32_t o[4];
                             i4x8_to_bf16(w.x, scu, o);
                             v[ci * 16 + 0] = o[0], v[ci * 16 + 1] = o[1], v[ci * 16 + 2] = o[2], v[ci * 16 + 3] = o[3];
@@ -444,16 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[ci * 16 + 12] = o[0], v[ci * 16 + 13] = o[1], v[ci * 16 + 14] = o[2], v[ci * 16 + 15] = o[3];
                         }
                     }
+                    if (pend >= 0) {  // the previous store has landed: its slot is ready for the MMA
+                        tmem_st_wait();
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full_a[pend]);
+                        pend = -1;
+                    }
+                    if (!mbar_wait(&a_empty[slot], sphase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     const uint32_t dst = t_row + C::kACol0 + slot * C::kACols + h * 32;
-                    if constexpr (GATED) {
+                    if constexpr (TWO) {
                         tmem_st_32cols(dst, v);  // the whole sub-block of one tile's row
                     } else {
                         tmem_st_16cols(dst + kh * 16, v);  // one K half of the sub-block
                     }
-                    tmem_st_wait();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_a[slot]);
+                    pend = slot;
                     if (++slot == NA) {
                         slot = 0;
                         sphase ^= 1u;
@@ -464,6 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phase ^= 1u;
                 }
             }
+        }
+        tmem_st_wait();  // no store in flight past this point (also on the abort path)
+        if (pend >= 0 && ok) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_a[pend]);
         }
         if (!ok) {
             if (lane == 0) atomicOr(args.err, kErrTimeoutProducer);
@@ -487,16 +513,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int col = n * kBW + r;  // this thread's output column
+            // this thread's output column (PAIR: and the one 128 columns on, from the
+            // second accumulator)
+            const int col = n * kTileRows + r;
             const bool col_ok = col < args.N;
+            const bool col2_ok = PAIR && col + kBW < args.N;
             const size_t wr = (size_t)tm.g * args.b_rows_per_group + (col_ok ? col : 0);
+            const size_t wr2 = (size_t)tm.g * args.b_rows_per_group + (col2_ok ? col + kBW : 0);
             // per-row factors: the 8-bit scales (the 4-bit ones were applied by the converters)
-            float f1 = 1.0f, f3 = 1.0f, b = 0.0f;
+            float f1 = 1.0f, f3 = 1.0f, b = 0.0f, b2 = 0.0f;
             if constexpr (WBITS == 8) {
                 f1 = args.scale[wr];
                 if (GATED) f3 = args.scale3[wr];
+                if (PAIR) f3 = args.scale[wr2];
             }
-            if (!GATED && bias != nullptr) b = __bfloat162float(bias[wr]);
+            if (!GATED && bias != nullptr) {
+                b = __bfloat162float(bias[wr]);
+                if (PAIR) b2 = __bfloat162float(bias[wr2]);
+            }
             const int m0 = mt * NT;
             const int valid = min(NT, s_rows[tm.g] - m0);
             __nv_bfloat16* o = out + (size_t)(s_roff[tm.g] + m0) * args.ldo + col;
@@ -507,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t va[CH], vb[CH];
                 if constexpr (CH == 32) {
                     tmem_ld_32cols(t_lane + c * CH, va);
-                    if constexpr (GATED) tmem_ld_32cols(t_lane + NT + c * CH, vb);
+                    if constexpr (TWO) tmem_ld_32cols(t_lane + NT + c * CH, vb);
                 } else {
                     tmem_ld_16cols(t_lane + c * CH, va);
-                    if constexpr (GATED) tmem_ld_16cols(t_lane + NT + c * CH, vb);
+                    if constexpr (TWO) tmem_ld_16cols(t_lane + NT + c * CH, vb);
                 }
                 tmem_ld_wait();
 #pragma unroll
@@ -524,6 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         y = activate_bf16out<ACT>(z + b);
                     }
                     if (col_ok && m < valid) o[(size_t)m * args.ldo] = __float2bfloat16_rn(y);
+                    if constexpr (PAIR) {
+                        const float y2 = activate_bf16out<ACT>(__uint_as_float(vb[j]) * f3 + b2);
+                        if (col2_ok && m < valid) o[(size_t)m * args.ldo + kBW] = __float2bfloat16_rn(y2);
+                    }
                 }
             }
             tc_fence_before_sync();
@@ -542,28 +580,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int WBITS, int ACT, int NT>
+template <int WBITS, int ACT, int NT, bool PAIR>
 cudaError_t launch_t(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3, const GroupedGemmWqArgs& a,
                      int grid, cudaStream_t st, bool pdl)
 {
-    using C = Cfg<WBITS, ACT == kActSwiglu, NT>;
-    auto kern = k_grouped_gemm_wq<WBITS, ACT, NT>;
+    using C = Cfg<WBITS, ACT == kActSwiglu || PAIR, NT>;
+    auto kern = k_grouped_gemm_wq<WBITS, ACT, NT, PAIR>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmem);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, pdl, x, w, w3, a);
 }
 
+// Two A tiles (SwiGLU, or PAIR) hold two accumulators of NT columns, double-buffered,
+// beside at least two operand slots in the 512 TMEM columns: NT <= 96.
 template <int WBITS, int NT>
 cudaError_t launch_nt(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3, const GroupedGemmWqArgs& a,
                       int act, int grid, cudaStream_t st, bool pdl)
 {
+    constexpr bool P = NT <= 96;
     switch (act) {
-    case kActNone: return launch_t<WBITS, kActNone, NT>(x, w, w3, a, grid, st, pdl);
-    case kActRelu: return launch_t<WBITS, kActRelu, NT>(x, w, w3, a, grid, st, pdl);
-    case kActGeluTanh: return launch_t<WBITS, kActGeluTanh, NT>(x, w, w3, a, grid, st, pdl);
-    case kActGeluErf: return launch_t<WBITS, kActGeluErf, NT>(x, w, w3, a, grid, st, pdl);
+    case kActNone: return launch_t<WBITS, kActNone, NT, P>(x, w, w3, a, grid, st, pdl);
+    case kActRelu: return launch_t<WBITS, kActRelu, NT, P>(x, w, w3, a, grid, st, pdl);
+    case kActGeluTanh: return launch_t<WBITS, kActGeluTanh, NT, P>(x, w, w3, a, grid, st, pdl);
+    case kActGeluErf: return launch_t<WBITS, kActGeluErf, NT, P>(x, w, w3, a, grid, st, pdl);
     default:
-        if constexpr (NT <= 64) return launch_t<WBITS, kActSwiglu, NT>(x, w, w3, a, grid, st, pdl);
+        if constexpr (NT <= 64) return launch_t<WBITS, kActSwiglu, NT, false>(x, w, w3, a, grid, st, pdl);
         return cudaErrorInvalidValue;  // the gated layer's tensor-memory budget caps NT at 64
     }
 }
@@ -605,6 +646,12 @@ __global__ void __launch_bounds__(256) k_quantize_int4(const T* __restrict__ w, 
 }
 
 }  // namespace
+
+int gemm_wq_weight_tiles(int N, int act, int nt)
+{
+    const bool pair = act != kActSwiglu && nt <= 96;
+    return ceil_div(N, pair ? 2 * kBW : kBW);
+}
 
 int gemm_wq_tokens_tile(int rows_per_expert, bool gated)
 {

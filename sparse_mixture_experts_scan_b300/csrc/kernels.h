@@ -211,7 +211,7 @@ struct GroupedGemmWqArgs {
     const int* row_off;    // [G] padded segment starts of the token rows
     const int* rows;       // [G] token rows per group
     int G;
-    int N, n_tiles, K;     // output columns (weight rows per group), tiles of 128, reduction
+    int N, n_tiles, K;     // output columns (weight rows per group), gemm_wq_weight_tiles, reduction
     int b_rows_per_group;
     void* out;             // [rows, ldo] bf16
     int ldo;
@@ -223,6 +223,9 @@ struct GroupedGemmWqArgs {
 // Token rows per tile (32, 64, 96 or 128; at most 64 for SwiGLU) for a layer whose
 // experts hold about rows_per_expert rows.
 int gemm_wq_tokens_tile(int rows_per_expert, bool gated);
+// Weight-row tiles of an N-row layer: 256 rows (two A tiles) without SwiGLU when
+// nt <= 96, else 128 rows.  GroupedGemmWqArgs::n_tiles must be this value.
+int gemm_wq_weight_tiles(int N, int act, int nt);
 cudaError_t launch_gemm_wq(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& w3,
                            const GroupedGemmWqArgs& a, int wbits, int act, int nt, int grid, cudaStream_t st,
                            bool pdl);
