@@ -16,14 +16,17 @@
 // shared memory; the tensor core reads A from TMEM and the token tile (B,
 // K-major, 128-byte swizzle) from shared memory.  The token tile is small
 // (NT = 32 .. 128 rows, as many as the experts hold), so no MMA work is spent
-// on padding rows of 128-row token tiles.
+// on padding rows of 128-row token tiles.  Each weight is converted once per
+// token tile, so NT covers all the rows an expert holds where it can.
 //   8-bit: q in [-127, 127] is exact in bf16; the per-row scale is applied to
 //          the accumulator in the epilogue: sum_k q[n,k] x[m,k] * scale[n].
 //   4-bit: the converter multiplies q in [-7, 7] by its group's scale (groups
-//          of 128 input columns) in packed bf16 arithmetic: bf16(q * bf16(scale)).
-// One thread of the epilogue holds one weight row (its TMEM lane) for NT
-// tokens: scale, bias and activation are per-thread scalars, and SwiGLU pairs
-// the W1 and W3 accumulators of the same row.
+//          of 128 input columns) in packed bf16 arithmetic: bf16(q * bf16(s)).
+// Two A tiles share each token tile: with SwiGLU the W1 and W3 tiles of the same
+// 128 rows (the epilogue pairs their accumulators), otherwise (NT <= 96, PAIR) two
+// consecutive 128-row tiles, so a tile covers 256 weight rows.  One thread of the
+// epilogue holds one weight row (its TMEM lane) of each A tile for NT tokens:
+// scale, bias and activation are per-thread scalars.
 //
 // Per CTA (one per SM, 512 threads):
 //   warp 0      TMA, per shared-memory stage of KS = 128 (8-bit) or 256 (4-bit) K
@@ -32,8 +35,9 @@
 //               the token tile as KS / 64 boxes [NT x 64] bf16;
 //   warp 1      TMEM allocation and tcgen05.mma (M = 128, N = NT, K = 16, A from TMEM);
 //   warps 4-11  converters, two per TMEM lane quarter (warp w writes lanes
-//               32 (w % 4) .. + 31): with SwiGLU one converts the W1 tile and the
-//               other the W3 tile, otherwise each converts one half of the K block;
+//               32 (w % 4) .. + 31): with two A tiles each converts one of them,
+//               otherwise each converts one half of the K block; one TMEM store
+//               stays in flight while the next sub-block is converted;
 //   warps 12-15 epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
 // The shared-memory stages (S, as many as fit: they keep the weight stream's bytes
 // in flight) and the TMEM operand slots (NA of 64 K values each, as many as the
