@@ -376,10 +376,14 @@ moe_status_t prepare(const moe_params_t* params, const moe_inputs_t* in, moe_out
         ok = ok && encode_bf16_2d(&c.mB3, gated ? in->W3 : in->W1, ES * L.F, L.d, b1_rows);
         if (L.rows_cap > 0)
             ok = ok && encode_bf16_2d(&c.mA1, c.at<void>(L.off_xp), L.rows_cap, L.d, 128) &&
-                 encode_bf16_2d(&c.mA2, c.at<void>(L.off_h), L.rows_cap, L.F, 128);
+                 encode_bf16_2d(&c.mA2, c.at<void>(L.off_h), L.rows_cap, L.F, 128) &&
+                 encode_bf16_2d(&c.mA1p, c.at<void>(L.off_xp), L.rows_cap, L.d, kABoxRows) &&
+                 encode_bf16_2d(&c.mA2p, c.at<void>(L.off_h), L.rows_cap, L.F, kABoxRows);
         if (L.S > 0)
             ok = ok && encode_bf16_2d(&c.mAs1, in->x, L.T, L.d, 128) &&
-                 encode_bf16_2d(&c.mAs2, c.at<void>(L.off_hs), L.t_pad, (uint64_t)L.S * L.F, 128);
+                 encode_bf16_2d(&c.mAs2, c.at<void>(L.off_hs), L.t_pad, (uint64_t)L.S * L.F, 128) &&
+                 encode_bf16_2d(&c.mAs1p, in->x, L.T, L.d, kABoxRows) &&
+                 encode_bf16_2d(&c.mAs2p, c.at<void>(L.off_hs), L.t_pad, (uint64_t)L.S * L.F, kABoxRows);
         if (!ok) return MOE_ERR_UNSUPPORTED;
     }
     return MOE_OK;
@@ -708,7 +712,11 @@ moe_status_t stage_gemm(Ctx& c)
                 f.mt_s0 = L.rows_cap / kSegRows;
                 tiles += mt_shared * (f.n_tiles_s1 + g2.n_tiles);
             }
-            const CUtensorMap maps[7] = {c.mA1, c.mB1, c.mB3, c.mA2, c.mB2, c.mAs1, c.mAs2};
+            // experts of about one M-tile (the layer streams its weights): most M-tiles are
+            // partial, so load only their valid rows
+            f.partial_a = mt_routed <= L.E ? 1 : 0;
+            const CUtensorMap maps[11] = {c.mA1,  c.mB1,  c.mB3,  c.mA2,  c.mB2, c.mAs1,
+                                          c.mAs2, c.mA1p, c.mA2p, c.mAs1p, c.mAs2p};
             e = launch_ffn_fused_tc(maps, f, act1, grid_for(tiles, 1), c.st, take_pdl(c));
         } else if (mt_routed > 0) {
             e = launch_gemm_tc(c.mA1, c.mB1, c.mB3, g1, act1, c.bn1, grid_for(mt_routed * g1.n_tiles, 1), c.st,

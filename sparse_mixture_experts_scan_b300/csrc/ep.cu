@@ -424,12 +424,16 @@ extern "C" moe_status_t moe_forward_ep(const moe_params_t* params, int32_t G, co
     const bool use_tc = bf16 && !(p.flags & MOE_FLAG_FFMA_EXPERTS);
     const bool gated = p.act == MOE_ACT_SWIGLU;
     const int E_loc = P.E_loc;
-    CUtensorMap maps[kEpMaxRanks][5];
+    CUtensorMap maps[kEpMaxRanks][11] = {};  // the fused kernel's maps (no shared experts: 5, 6, 9, 10 unused)
     if (use_tc) {
         const int b1_rows = gated ? 128 : 256;
         for (int q = 0; q < G; ++q) {
             const size_t w13 = (size_t)q * E_loc * p.d_ff * p.d_model * esz;
             bool ok = host::encode_bf16_2d(&maps[q][0], at<void>(workspace, P.off_xr[q]), P.rows_recv, p.d_model, 128) &&
+                      host::encode_bf16_2d(&maps[q][7], at<void>(workspace, P.off_xr[q]), P.rows_recv, p.d_model,
+                                           kABoxRows) &&
+                      host::encode_bf16_2d(&maps[q][8], at<void>(workspace, P.off_h[q]), P.rows_recv, p.d_ff,
+                                           kABoxRows) &&
                       host::encode_bf16_2d(&maps[q][1], offset_bytes(inputs->W1, w13), (uint64_t)E_loc * p.d_ff,
                                            p.d_model, b1_rows) &&
                       host::encode_bf16_2d(&maps[q][2], offset_bytes(gated ? inputs->W3 : inputs->W1, w13),

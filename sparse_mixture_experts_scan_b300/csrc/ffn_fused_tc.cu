@@ -44,6 +44,7 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kRing = 4;
+constexpr uint32_t kABoxBytes = kABoxRows * kBK * 2;  // one A box: 32 rows x 128 bytes
 
 template <int BN>
 struct FCfg {
@@ -118,7 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_ffn_fused_tc(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmAs1,
-                   const __grid_constant__ CUtensorMap tmAs2, const FusedFfnArgs args)
+                   const __grid_constant__ CUtensorMap tmAs2, const __grid_constant__ CUtensorMap tmA1p,
+                   const __grid_constant__ CUtensorMap tmA2p, const __grid_constant__ CUtensorMap tmAs1p,
+                   const __grid_constant__ CUtensorMap tmAs2p, const FusedFfnArgs args)
 {
     using C = FCfg<BN>;
     constexpr bool GATED = (ACT1 == kActSwiglu);
@@ -169,9 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATED) tma_prefetch_desc(&tmB3);
         tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB2);
+        tma_prefetch_desc(&tmA1p);
+        tma_prefetch_desc(&tmA2p);
         if (args.S > 0) {
             tma_prefetch_desc(&tmAs1);
             tma_prefetch_desc(&tmAs2);
+            tma_prefetch_desc(&tmAs1p);
+            tma_prefetch_desc(&tmAs2p);
         }
     }
     if (warp == 1) {
@@ -247,6 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_global();
                 }
                 const int a_row = (kind == 1 || kind == 2) ? s_roff[g] + m * kBM : m * kBM;
+                // a full M-tile's A is one box; with partial_a a partial one's the 32-row boxes
+                // that hold valid rows (rows past them stay stale in shared memory; their
+                // accumulator rows are never stored)
+                const int a_valid = min(kBM, ((kind == 1 || kind == 2) ? s_rows[g] : args.shared_rows) - m * kBM);
+                const int a_boxes = args.partial_a ? (a_valid + kABoxRows - 1) / kABoxRows : kBM / kABoxRows;
+                const uint32_t stage_bytes = (uint32_t)a_boxes * kABoxBytes + C::B_BYTES;
+                const CUtensorMap* mA = kind == 0 ? &tmAs1 : kind == 1 ? &tmA1 : kind == 2 ? &tmA2 : &tmAs2;
+                const CUtensorMap* mAp = kind == 0 ? &tmAs1p : kind == 1 ? &tmA1p : kind == 2 ? &tmA2p : &tmAs2p;
                 const int b_row = kind == 2 ? g * args.b2_rows_per_group + n * BN
                                   : kind == 1 ? g * args.b1_rows_per_group + n * OUT1
                                   : kind == 0 ? args.b1_row0 + n * OUT1
@@ -257,22 +272,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], stage_bytes);
                     uint8_t* dA = sA + stage * C::A_BYTES;
                     uint8_t* dB = sB + stage * C::B_BYTES;
                     // each TMA names its kernel-parameter tensor map directly
+                    if (a_boxes * kABoxRows == kBM) {
+                        tma_load_2d(dA, mA, &full[stage], kb * kBK, a_row, pol_act);
+                    } else {
+                        for (int i = 0; i < a_boxes; ++i)
+                            tma_load_2d(dA + i * kABoxBytes, mAp, &full[stage], kb * kBK, a_row + i * kABoxRows,
+                                        pol_act);
+                    }
                     if (kind == 2) {
-                        tma_load_2d(dA, &tmA2, &full[stage], kb * kBK, a_row, pol_act);
                         tma_load_2d(dB, &tmB2, &full[stage], kb * kBK, b_row, pol_w);
                     } else if (kind == 3) {
                         // K column kb * 64 of the concatenated hidden layer: expert seg, column kc
                         const int seg = (kb * kBK) / args.seg_k2, kc = kb * kBK - seg * args.seg_k2;
-                        tma_load_2d(dA, &tmAs2, &full[stage], kb * kBK, a_row, pol_act);
                         tma_load_2d(dB, &tmB2, &full[stage], kc, (args.b2_group0 + seg) * args.b2_rows_per_group + n * BN,
                                     pol_w);
                     } else {
-                        const CUtensorMap* mA = kind == 0 ? &tmAs1 : &tmA1;
-                        tma_load_2d(dA, mA, &full[stage], kb * kBK, a_row, pol_act);
                         tma_load_2d(dB, &tmB1, &full[stage], kb * kBK, b_row, pol_w);
                         if (GATED) tma_load_2d(dB + C::B_BYTES / 2, &tmB3, &full[stage], kb * kBK, b_row, pol_w);
                     }
@@ -459,11 +477,13 @@ cudaError_t launch_t(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, c
     const size_t smem = FCfg<BN>::SMEM;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    // without shared experts the two shared-expert maps are never read: pass the first map
+    // without shared experts the shared-expert maps are never read: pass the routed ones
     const CUtensorMap& s1 = a.S > 0 ? maps[5] : maps[0];
     const CUtensorMap& s2 = a.S > 0 ? maps[6] : maps[0];
+    const CUtensorMap& s1p = a.S > 0 ? maps[9] : maps[7];
+    const CUtensorMap& s2p = a.S > 0 ? maps[10] : maps[7];
     return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, pdl, maps[0], maps[1], maps[2], maps[3],
-                         maps[4], s1, s2, a);
+                         maps[4], s1, s2, maps[7], maps[8], s1p, s2p, a);
 }
 
 }  // namespace

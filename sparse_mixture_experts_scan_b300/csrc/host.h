@@ -57,6 +57,7 @@ struct Ctx {
     bool pdl = false;  // false until this call has launched its first kernel
     int bn1, bn2;  // MMA N of GEMM1 / GEMM2 (tcgen05 path)
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mAs1, mAs2, mX, mW, mWn;
+    CUtensorMap mA1p, mA2p, mAs1p, mAs2p;  // the A maps with kABoxRows-row boxes (partial M-tiles)
     bool q8 = false;              // int8 expert weights
     CUtensorMap mQ1, mQ3, mQ2;    // their uint8 maps
     bool routed_experts = true;   // stage_gemm runs the routed experts (false: shared experts only)

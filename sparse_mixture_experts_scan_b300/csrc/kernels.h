@@ -115,6 +115,12 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t st,
 cudaError_t launch_dispatch_scan_only(const DispatchArgs& a, cudaStream_t st);
 
 // ---- stage 3: grouped GEMMs ------------------------------------------------
+// k_ffn_fused_tc loads the token rows (A operand) of a full 128-row M-tile as one box;
+// with FusedFfnArgs::partial_a, those of a partial M-tile as the boxes of kABoxRows rows
+// that hold valid rows (an expert's last M-tile is mostly padding when it holds few rows,
+// and the padding rows were never written): its maps 7-10 are the A maps 0, 3, 5, 6 with
+// such boxes.
+constexpr int kABoxRows = 32;
 // tcgen05 kernel: act is kActNone (plain GEMM), kActRelu, kActGeluTanh,
 // kActGeluErf (bias allowed) or kActSwiglu (gated: B rows from W1 and W3).
 cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
@@ -168,9 +174,13 @@ struct FusedFfnArgs {
     void* y;
     const int32_t* row_token;
     const float* row_gate;
+    // nonzero: a partial M-tile loads only the kABoxRows-row A boxes that hold valid rows
+    // (maps 7-10); zero: every M-tile is one 128-row box
+    int partial_a;
 };
-// maps: A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2), As1 (x), As2 (Hs) (the last
-// two are read only when S > 0; the array may then hold 5 maps); MMA N = 256.
+// maps (11): A1 (Xp), B1 (W1), B3 (W3 or W1), A2 (H), B2 (W2), As1 (x), As2 (Hs), then
+// A1, A2, As1, As2 again with kABoxRows-row boxes (the A maps have 128-row boxes); the
+// shared-expert maps 5, 6, 9, 10 are read only when S > 0.  MMA N = 256.
 cudaError_t launch_ffn_fused_tc(const CUtensorMap* maps, const FusedFfnArgs& a, int act1, int grid,
                                 cudaStream_t st, bool pdl);
 
