@@ -540,6 +540,9 @@ extern "C" moe_status_t moe_forward_ep(const moe_params_t* params, int32_t G, co
             f.mt_done = sync + 2;
             f.mt_max = P.sync_n - 2;
             f.err = ctx[q].err();
+            // owners whose experts hold about one M-tile each load only the valid rows of
+            // a partial M-tile (maps 7 and 8), as the single-rank layer does
+            f.partial_a = mt <= E_loc ? 1 : 0;
             const int grid = std::max(1, std::min(mt * (f.n_tiles1 + f.n_tiles2), sms));
             e = launch_ffn_fused_tc(maps[q], f, p.act, grid, st, next_pdl());
         } else {
