@@ -347,7 +347,8 @@ def algorithmic_gemm_work(cfg, out, direct=False):
 
     Bytes: weights of every expert that received >= 1 kept row (W1, W3, W2), the
     permuted activations read once, the hidden activations written and read once,
-    the expert outputs written once (shared experts: all T rows; with the combine
+    the expert outputs written once (shared experts: x read once, their S * d_ff hidden
+    columns written and read once and one summed output row per token; with the combine
     finished in the stage, the kept rows of y plus their token and gate).  Flops: 2 per
     multiply-add on kept rows only."""
     import torch
@@ -366,8 +367,8 @@ def algorithmic_gemm_work(cfg, out, direct=False):
     else:
         w_bytes = touched * nmat * cfg.d * cfg.F * esz
     srows = cfg.S * cfg.T
-    act_bytes = (rows * (cfg.d + 2 * cfg.F + cfg.d) + cfg.T * cfg.d * (1 if cfg.S else 0)
-                 + srows * (2 * cfg.F + cfg.d)) * esz + (rows * 8 if direct else 0)
+    act_bytes = (rows * (cfg.d + 2 * cfg.F + cfg.d) + (2 * cfg.T * cfg.d if cfg.S else 0)
+                 + srows * 2 * cfg.F) * esz + (rows * 8 if direct else 0)
     flops = cfg.expert_flops(rows)
     return {"bytes": w_bytes + act_bytes, "weight_bytes": w_bytes, "flops": flops,
             "kept_rows": rows, "touched_experts": touched}
